@@ -1,0 +1,479 @@
+"""Benchmark of the MoE decode layer on one GB300 (or N replicas).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload r1_decode_t128] [--seed S]
+
+A step is one pass of the whole hot path over one batch: routing, FP8
+quantisation of x, dispatch permutation, grouped GEMM gate/up, SiLU-mul +
+requantisation, grouped GEMM down, combine.  Inputs are seeded synthetic
+tensors of the workload's shape, resident in HBM before timing starts; the
+11 GB of expert weights streamed per step are far larger than L2, so no L2
+flush is needed between steps.
+
+Prints one JSON line (rank 0).  `value` is tokens/s over all ranks;
+`roofline` describes the dominant kernel (grouped GEMM gate/up) against the
+measured HBM copy bandwidth; `e2e` is the same metric through the layer's
+public call with pinned host buffers copied in and out each step;
+`cpu_baseline` times the CPU oracle on a bounded sample of the workload.
+--impl reference times the CPU oracle itself as the reference arm.
+Several GPUs run independent replicas (the layer has no exchange step on one
+node here): the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s at R1 shape (bs 128/1024); HBM GB/s and % of roofline"
+DEFAULT_WORKLOAD = "r1_decode_t128"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p.get("bf16_tflops", 1900.0)), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during timing."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workload
+def setup(shape, seed, device):
+    import torch
+    import moe_expert_layer_07_gb300 as moe
+    import synth
+
+    inp = synth.make_inputs(shape, seed=seed, device=device)
+    log2phys = None
+    info = {}
+    if shape.balanced_perm:
+        # calibration: route the batch without a permutation, count rows per
+        # expert from the dispatch offsets, balance, re-lay the weights
+        probe = moe.MoELayer(shape, inp)
+        out = torch.empty((shape.tokens, shape.hidden), device=device)
+        probe.forward(inp["x"], out)
+        off = probe.view("expert_offsets", torch.int32, (shape.groups + 1,)).cpu().numpy()
+        counts = np.diff(off)[:shape.num_experts].astype(np.int64)
+        log2phys, phys2log, mom = moe.balance_permutation(counts, shape.num_sets)
+        naive = counts.reshape(shape.num_sets, -1).sum(1)
+        info = {"set_imbalance": round(mom, 4),
+                "set_imbalance_contiguous": round(float(naive.max() / naive.mean()), 4)}
+        del probe
+        inp = synth.relayout_experts(inp, shape, phys2log)
+        torch.cuda.empty_cache()
+    layer = moe.MoELayer(shape, inp, log2phys=log2phys)
+    return inp, layer, log2phys, info
+
+
+class Stepper:
+    """The hot path as its C-ABI steps on one stream, CUDA events around each."""
+
+    NAMES = ["route", "quant_x", "permute", "gemm_gate_up", "silu_requant", "gemm_down", "combine"]
+
+    def __init__(self, layer, x, out):
+        import torch
+        import moe_expert_layer_07_gb300 as moe
+        self.moe, self.torch = moe, torch
+        self.layer, self.x, self.out = layer, x, out
+        s = layer.shape
+        self.fp8 = s.dtype == "fp8"
+        L, ws = layer.layout, layer.ws
+        base = ws.data_ptr()
+        self.p = {n: base + getattr(L, n) for n in
+                  ("status", "logits", "topk_ids", "topk_w", "xq", "xs", "expert_offsets",
+                   "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "gate_up",
+                   "h", "h_scales", "y")}
+        self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
+        self.k = {}
+        self.events = []
+
+    def step(self, record=False):
+        moe, p, lay, s = self.moe, self.p, self.layer, self.layer.shape
+        cfg, w = lay.cfg, lay._keep
+        T, G, H, I = s.tokens, s.groups, s.hidden, s.inter
+        rows = T * (s.top_k + s.num_shared)
+        ev = []
+
+        def mark():
+            if record:
+                e = self.torch.cuda.Event(enable_timing=True)
+                e.record()
+                ev.append(e)
+
+        mark()
+        moe.route(cfg, T, self.x, w["wg"], w.get("e_bias"), w.get("logit_offset"),
+                  w.get("log2phys"), p["logits"], p["topk_ids"], p["topk_w"], p["status"])
+        mark()
+        if self.fp8:
+            moe.act_requant(cfg, moe.ACT_IDENTITY, T, self.x, p["xq"], p["xs"])
+        mark()
+        moe.permute(cfg, T, p["topk_ids"], p["xq"] if self.fp8 else self.x,
+                    p["xs"] if self.fp8 else None, p["expert_offsets"], p["src_of_row"],
+                    p["row_of_slot"], p["xp"], p["xp_scales"] if self.fp8 else None,
+                    p["perm_scratch"], self.perm_bytes, p["status"])
+        mark()
+        moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"] if self.fp8 else None,
+                         p["expert_offsets"], w["w13"], w.get("w13_s"), p["gate_up"],
+                         moe.OUT_F32, p["status"])
+        mark()
+        moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, p["gate_up"], p["h"],
+                        p["h_scales"] if self.fp8 else None, rows_dev=p["expert_offsets"] + 4 * G)
+        mark()
+        moe.grouped_gemm(cfg, G, H, I, rows, p["h"], p["h_scales"] if self.fp8 else None,
+                         p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_BF16,
+                         p["status"])
+        mark()
+        moe.combine(cfg, T, p["y"], p["row_of_slot"], p["topk_w"], p["expert_offsets"], self.out,
+                    moe.OUT_F32)
+        mark()
+        if record:
+            self.events.append(ev)
+
+    def kernel_ms(self):
+        """Average ms per step of each stage over the recorded steps."""
+        acc = {n: 0.0 for n in self.NAMES}
+        for ev in self.events:
+            for i, n in enumerate(self.NAMES):
+                acc[n] += ev[i].elapsed_time(ev[i + 1])
+        k = max(1, len(self.events))
+        return {n: v / k for n, v in acc.items()}
+
+
+def algorithmic_bytes(shape, offsets):
+    """Bytes the method must move, per stage, given the rows per group."""
+    T, H, I, E, S, k = (shape.tokens, shape.hidden, shape.inter, shape.num_experts,
+                        shape.num_shared, shape.top_k)
+    fp8 = shape.dtype == "fp8"
+    eb = 1 if fp8 else 2
+    rows = T * (k + S)
+    counts = np.diff(offsets)
+    active = int((counts > 0).sum())
+    w13 = 2 * I * H * eb + (4 * (2 * I // 128) * (H // 128) if fp8 else 0)
+    w2 = H * I * eb + (4 * (H // 128) * (I // 128) if fp8 else 0)
+    sc_h = 4 * (H // 128) if fp8 else 0
+    sc_i = 4 * (I // 128) if fp8 else 0
+    b = {}
+    b["route"] = 2 * T * H + 2 * E * H + 4 * T * E * 2 + 8 * T * k
+    b["quant_x"] = (2 * T * H + T * H + T * sc_h) if fp8 else 0
+    b["permute"] = 4 * T * k * 3 + rows * (H * eb + sc_h) * 2
+    b["gemm_gate_up"] = active * w13 + rows * (H * eb + sc_h) + rows * 2 * I * 4
+    b["silu_requant"] = rows * 2 * I * 4 + rows * (I * eb + sc_i)
+    b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 2
+    b["combine"] = T * (k + S) * H * 2 + 8 * T * k + T * H * 4
+    flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)
+    return b, active, flops
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_sample_rate(shape, inp, log2phys, n_tokens, seed=0):
+    """Tokens/s of the CPU oracle on `n_tokens` tokens of the workload."""
+    import synth
+    import oracle
+    from oracle import layer as olayer
+    npin = synth.to_numpy(inp, log2phys)
+    rng = np.random.default_rng(seed)
+    sample = np.sort(rng.choice(shape.tokens, n_tokens, replace=False))
+    sub = dict(npin)
+    sub["x_bits"] = np.ascontiguousarray(npin["x_bits"][sample])
+    sub_shape = shape.with_tokens(n_tokens)
+    t0 = time.perf_counter()
+    olayer.layer_forward(sub_shape, sub)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt, oracle.num_threads(), npin, sample
+
+
+# ----------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--cpu-tokens", type=int, default=None,
+                    help="tokens of the CPU-oracle sample (default: sized to ~10-30 s)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args()
+
+    import torch
+    import torch.distributed as dist
+    import synth
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    shape = synth.CONFIGS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        return reference_arm(args, shape)
+
+    if world > 1:
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    from __graft_entry__ import build
+    if rank == 0 or world == 1:
+        build()
+    if world > 1:
+        dist.barrier()
+    import moe_expert_layer_07_gb300 as moe
+
+    inp, layer, log2phys, perm_info = setup(shape, args.seed + rank, device)
+    T, H = shape.tokens, shape.hidden
+    x = inp["x"]
+    out = torch.empty((T, H), dtype=torch.float32, device=device)
+    stepper = Stepper(layer, x, out)
+    for _ in range(args.warmup):
+        stepper.step()
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError(f"device status {layer.status()} after warm-up")
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        start.record()
+        for _ in range(args.steps):
+            stepper.step(record=True)
+        end.record()
+        torch.cuda.synchronize()
+        barrier()
+    elapsed_ms = start.elapsed_time(end)
+    if world > 1:
+        t = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    status = layer.status()
+    kms = stepper.kernel_ms()
+    offsets = layer.view("expert_offsets", torch.int32, (shape.groups + 1,)).cpu().numpy()
+    bytes_per, active, flops = algorithmic_bytes(shape, offsets)
+    ms_step = elapsed_ms / args.steps
+    value = T * world * args.steps / (elapsed_ms / 1e3)
+
+    hbm_peak, bf16_peak, peak_src = load_peaks()
+    layer_bytes = sum(bytes_per.values())
+    gu_ms = kms["gemm_gate_up"]
+    achieved = bytes_per["gemm_gate_up"] / (gu_ms / 1e3) / 1e9
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as f:
+            tr = json.load(f).get(args.workload, {}).get("gemm_gate_up")
+        traffic = tr if tr else None
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = end_to_end(layer, shape, x, device, args.steps, args.warmup, world)
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        n = args.cpu_tokens or default_cpu_tokens(shape)
+        rate, dt, cores, _, _ = oracle_sample_rate(shape, inp, log2phys, n, seed=args.seed)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} of {T} tokens of the same workload (routing + expert FFNs + "
+                         f"combine in fp64), {dt:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8e4m3" if shape.dtype == "fp8" else "bf16", "data": "synthetic",
+        "config": {"workload": shape.name, "tokens": T, "hidden": H, "inter": shape.inter,
+                   "experts": shape.num_experts, "shared": shape.num_shared,
+                   "top_k": shape.top_k, "parallelism": "replicas" if world > 1 else "single",
+                   "l2": "inputs larger than L2 (expert weights streamed each step), no flush",
+                   **perm_info},
+        "hbm_gbs": layer_bytes / (ms_step / 1e3) / 1e9,
+        "layer_roofline_frac": (layer_bytes / (hbm_peak * 1e9)) / (ms_step / 1e3),
+        "active_experts": active,
+        "kernels_ms": {k: round(v, 5) for k, v in kms.items()},
+        "roofline": {"bound": "hbm", "kernel": "grouped_gemm gate/up", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)"},
+        "tensor_pipe_frac_of_bf16x2": (flops / (ms_step / 1e3)) / (2 * bf16_peak * 1e12),
+        "gpu_launches": args.steps * moe.layer_kernel_count(layer.cfg, T),
+        "device_status": status,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def default_cpu_tokens(shape):
+    # about 10-30 s of oracle work on a 16-core host
+    if shape.hidden >= 7168:
+        return min(shape.tokens, 32)
+    return shape.tokens
+
+
+def end_to_end(layer, shape, x_dev, device, steps, warmup, world):
+    import torch
+    T, H = shape.tokens, shape.hidden
+    x_host = x_dev.cpu().pin_memory()
+    out_host = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(x_dev)
+    od = torch.empty((T, H), dtype=torch.float32, device=device)
+    for _ in range(warmup):
+        layer.forward_host(x_host, out_host, xd, od)
+    torch.cuda.synchronize()
+    n = max(1, steps // 2)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(n):
+        layer.forward_host(x_host, out_host, xd, od)
+    e.record()
+    torch.cuda.synchronize()
+    ms = s.elapsed_time(e)
+    return {"value": T * world * n / (ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": T * H * 2, "d2h_bytes_per_step": T * H * 4,
+            "steps": n, "api": "MoELayer.forward_host -> moe_layer_forward"}
+
+
+def reference_arm(args, shape):
+    """The CPU oracle as the reference: tokens/s on bounded samples."""
+    import torch
+    import synth
+    import oracle
+    from oracle import layer as olayer
+
+    oracle.build()
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = synth.make_inputs(shape, seed=args.seed, device=device)
+    log2phys = None
+    if shape.balanced_perm:
+        from oracle import routing as orouting
+        def bits(t):
+            return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+        bias = None if inp["e_bias"] is None else inp["e_bias"].cpu().numpy()
+        off = None if inp["logit_offset"] is None else inp["logit_offset"].cpu().numpy()
+        l = orouting.gate_logits(bits(inp["x"]), bits(inp["wg"]), off)
+        _, _, logical = orouting.route(l, shape, bias)
+        counts = np.bincount(logical.reshape(-1), minlength=shape.num_experts)
+        log2phys, p2l = balanced_perm_host(counts, shape.num_sets)
+        inp = synth.relayout_experts(inp, shape, p2l)
+    npin = synth.to_numpy(inp, log2phys)
+    per_step = max(1, min(shape.tokens, 2 if shape.hidden >= 7168 else shape.tokens // 4))
+    rng = np.random.default_rng(args.seed)
+    t_total, n_total = 0.0, 0
+    for i in range(args.warmup + args.steps):
+        sample = np.sort(rng.choice(shape.tokens, per_step, replace=False))
+        sub = dict(npin)
+        sub["x_bits"] = np.ascontiguousarray(npin["x_bits"][sample])
+        t0 = time.perf_counter()
+        olayer.layer_forward(shape.with_tokens(per_step), sub)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            t_total += dt
+            n_total += per_step
+    value = n_total / t_total
+    cores = oracle.num_threads()
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t_total / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "impl": "reference",
+            "dtype": "f64", "data": "synthetic",
+            "config": {"workload": shape.name, "tokens": shape.tokens, "hidden": shape.hidden},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{per_step} tokens per step of the same workload"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def balanced_perm_host(counts, num_sets):
+    import moe_expert_layer_07_gb300 as moe
+    from moe_expert_layer_07_gb300 import _build
+    _build.build()
+    l2p, p2l, _ = moe.balance_permutation(counts, num_sets)
+    return l2p, p2l
+
+
+if __name__ == "__main__":
+    sys.exit(main())

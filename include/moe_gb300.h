@@ -1,0 +1,256 @@
+/*
+ * moe_gb300 — the DeepSeek-style Mixture-of-Experts FFN layer at decode time,
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer (Moreh report "21K output tokens/s DeepSeek inference on MI300X
+ * with Expert Parallelism", sections "Overview" and "Parallelisation"):
+ * a light gate routes each token to top_k of E small SwiGLU experts, an
+ * always-on shared expert runs for every token, and the expert outputs are
+ * summed with the routing weights.  Expert-parallel dispatch/combine (the
+ * all-to-all of section "Compute-communication overlap") becomes, on one
+ * GPU, a permutation of token rows into per-expert contiguous rows and a
+ * weighted gather back.
+ *
+ * Conventions for every call below
+ *   - Pointers are DEVICE pointers unless the argument says "host".
+ *   - All buffers are allocated by the caller; the library allocates no
+ *     memory.  Row-major layouts, innermost dimension last, no padding.
+ *     Every device pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Device calls only enqueue work: none synchronises the host
+ *     or reads device data back, and sizes that depend on the routing
+ *     (rows per expert) stay on the device, so every device call can be
+ *     captured in a CUDA graph (the report's section "Using HIP Graphs":
+ *     tensor sizes kept static so that dispatch and combine can live inside
+ *     the captured graph).
+ *   - Return value: MOE_OK (0) or a negative MOE_ERR_* code.  Argument and
+ *     shape errors are returned before anything is enqueued.  Problems only
+ *     the device can see (an expert id out of range, inconsistent offsets,
+ *     a pipeline wait that ran out of time) set bits MOE_DEV_* in a device
+ *     status word (int32) instead; kernels never trap.  `dev_status` may be
+ *     NULL (no report).
+ *
+ * Notation: T tokens, H hidden, I expert intermediate width, E routed
+ * experts, S shared experts, k = top_k, G = E + S groups, R = T*k routed
+ * rows, R_tot = R + S*T rows.  Groups 0..E-1 are the routed experts in
+ * PHYSICAL order, groups E..G-1 the shared experts.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- codes ------------------------------------------------------------ */
+enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,        /* null pointer, bad enum, T < 0, misalignment */
+    MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* a dimension this build does not handle */
+    MOE_ERR_WORKSPACE_TOO_SMALL = -3,
+    MOE_ERR_CUDA = -4,               /* a CUDA runtime call failed */
+    MOE_ERR_TIMEOUT = -5,            /* the device reported MOE_DEV_TIMEOUT */
+    MOE_ERR_DEVICE_FAULT = -6        /* the device reported another MOE_DEV_* bit */
+};
+enum {                               /* bits of the device status word */
+    MOE_DEV_BAD_EXPERT_ID = 1,       /* a topk id / log2phys entry outside [0, E) */
+    MOE_DEV_BAD_OFFSETS = 2,         /* expert_offsets not non-decreasing within [0, rows] */
+    MOE_DEV_TIMEOUT = 4              /* a bounded pipeline wait expired (about 1 s) */
+};
+enum { MOE_SCORING_SOFTMAX = 0, MOE_SCORING_SIGMOID = 1 };
+enum { MOE_DTYPE_BF16 = 0, MOE_DTYPE_FP8_BLOCK128 = 1 };
+enum { MOE_OUT_F32 = 0, MOE_OUT_BF16 = 1 };
+enum { MOE_ACT_IDENTITY = 0, MOE_ACT_SILU_MUL = 1 };
+
+/* ---- layer description -------------------------------------------------- */
+typedef struct moe_config {
+    int32_t hidden;          /* H; multiple of 128 */
+    int32_t inter;           /* I, width of every expert (routed and shared); multiple of 128 */
+    int32_t num_experts;     /* E routed experts, 1..1024 */
+    int32_t num_shared;      /* S shared experts, 0..4, each of width I */
+    int32_t top_k;           /* k, 1..16 */
+    int32_t num_groups;      /* expert groups for group-limited routing (1 = none); divides E */
+    int32_t topk_groups;     /* groups kept */
+    int32_t group_topn;      /* a group's score is the sum of its best group_topn scores */
+    int32_t scoring;         /* MOE_SCORING_* */
+    int32_t norm_topk;       /* 1: divide the chosen weights by their sum */
+    int32_t dtype;           /* MOE_DTYPE_*: weights/activations of the expert GEMMs */
+    int32_t max_tokens;      /* largest T the workspace of moe_layer_forward is sized for */
+    float routed_scaling;    /* factor on the routed weights (not on shared experts) */
+} moe_config;
+
+/* Device pointers to the layer's weights. */
+typedef struct moe_weights {
+    const void *w_gate;       /* bf16 [E, H], LOGICAL expert order */
+    const float *e_bias;      /* fp32 [E] logical, selection-only bias (sigmoid); NULL = none */
+    const float *logit_offset;/* fp32 [E] logical, added to the gate logits; NULL = none */
+    const int32_t *log2phys;  /* int32 [E]: physical slot of each logical expert; NULL = identity */
+    const void *w13;          /* [G, 2I, H]: rows [0, I) gate proj, [I, 2I) up proj; e4m3 or bf16 */
+    const float *w13_scales;  /* fp32 [G, 2I/128, H/128], one per 128x128 block (FP8 only) */
+    const void *w2;           /* [G, H, I] down proj; e4m3 or bf16 */
+    const float *w2_scales;   /* fp32 [G, H/128, I/128] (FP8 only) */
+} moe_weights;
+
+/* ---- routing -------------------------------------------------------------
+ * Gate logits l[t,e] = sum_h x[t,h] Wg[e,h] (+ logit_offset[e]) and top-k
+ * selection (report, section "Overview": a light gating network chooses a
+ * few experts per token; section "Load balancing across GPUs": after the
+ * experts are permuted the gate must emit ids in the new order).
+ *   x        bf16 [T, H];  w_gate bf16 [E, H] (logical order)
+ *   e_bias   fp32 [E] or NULL (sigmoid scoring only)
+ *   logit_offset fp32 [E] or NULL;  log2phys int32 [E] or NULL
+ *   logits   fp32 [T, E], written (the gate logits, logical order)
+ *   topk_ids int32 [T, k], written: PHYSICAL ids, slot j in descending
+ *            selection score (ties: lower logical id first)
+ *   topk_w   fp32 [T, k], written: routing weights of the slots
+ * Logits are summed in a fixed order (lane-sliced fp32 FMA chains, then a
+ * butterfly), so the ids are reproducible bit for bit.  Sigmoid scoring:
+ * s = fp32(sigmoid(l)) evaluated in fp64, selection by s + bias, groups
+ * scored by the sum of their top group_topn, weights s/sum(s) (x scaling).
+ * Softmax scoring: selection by l, weights from an fp64 softmax over E. */
+MOE_API int moe_route(const moe_config *cfg, int32_t T, const void *x, const void *w_gate,
+              const float *e_bias, const float *logit_offset, const int32_t *log2phys,
+              float *logits, int32_t *topk_ids, float *topk_w,
+              int32_t *dev_status, void *stream);
+
+/* ---- activation quantisation ----------------------------------------------
+ * mode MOE_ACT_IDENTITY (FP8 layers): in bf16 [rows, H] -> out e4m3 [rows, H]
+ *   and out_scales fp32 [rows, H/128]: per row and 128-column group,
+ *   scale = amax/448 (IEEE fp32 division; 1 if amax = 0),
+ *   code = e4m3(v / scale), round to nearest even, saturating.
+ * mode MOE_ACT_SILU_MUL: in fp32 [rows, 2I] (gate | up halves), h =
+ *   silu(gate) * up in fp32; FP8 layers quantise h as above into
+ *   out e4m3 [rows, I] + out_scales [rows, I/128]; BF16 layers write
+ *   out bf16 [rows, I] (out_scales unused, may be NULL).
+ * rows_dev: NULL, or a device int32 holding the number of rows to process
+ *   (clamped to `rows`); e.g. expert_offsets + G.
+ * (SGLang/H20 article, section "MoE": the block-scale handling of the MoE
+ * GEMMs; the activation format is the R1 FP8 layout, per token x 128.) */
+MOE_API int moe_act_requant(const moe_config *cfg, int32_t mode, int32_t rows,
+                    const int32_t *rows_dev, const void *in, void *out,
+                    float *out_scales, void *stream);
+
+/* ---- dispatch (permutation into per-expert rows) ---------------------------
+ * topk_ids int32 [T, k] physical ids.  Routed slot i = t*k + j goes to row
+ * expert_offsets[e] + (number of earlier slots with the same expert), so
+ * rows of an expert are in increasing slot order (deterministic).  Shared
+ * expert s of token t goes to row expert_offsets[E + s] + t.
+ *   x_rows     e4m3 [T, H] (FP8) or bf16 [T, H] (BF16): rows to gather
+ *   x_scales   fp32 [T, H/128] (FP8 only)
+ *   expert_offsets int32 [G + 1], written: first row of every group
+ *   src_of_row int32 [R_tot], written: the slot of each row (routed slots
+ *              t*k + j; shared slots R + s*T + t)
+ *   row_of_slot int32 [T, k], written (-1 for a slot whose id was invalid)
+ *   xp         [R_tot, H] gathered rows (e4m3 or bf16), xp_scales fp32
+ *              [R_tot, H/128] (FP8 only)
+ *   ws         scratch of moe_permute_workspace_size bytes
+ * (report, sections "Overview" and "Compute-communication overlap": the
+ * dispatch that carries each token to its experts.) */
+MOE_API int moe_permute_workspace_size(const moe_config *cfg, int32_t T, size_t *bytes /* host */);
+MOE_API int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_ids,
+                const void *x_rows, const float *x_scales,
+                int32_t *expert_offsets, int32_t *src_of_row, int32_t *row_of_slot,
+                void *xp, float *xp_scales, void *ws, size_t ws_bytes,
+                int32_t *dev_status, void *stream);
+
+/* ---- grouped GEMM -----------------------------------------------------------
+ * For every group g and row r in [expert_offsets[g], expert_offsets[g+1]):
+ *   C[r, n] = sum_k A[r, k] * W[g, n, k]
+ * FP8 (cfg->dtype = MOE_DTYPE_FP8_BLOCK128): A e4m3 [rows, K] with a_scales
+ *   fp32 [rows, K/128]; W e4m3 [groups, N, K] with w_scales fp32
+ *   [groups, N/128, K/128]; every 128-wide K block is scaled by
+ *   a_scale[r, kb] * w_scale[g, n/128, kb] (fp32 accumulation).
+ * BF16: A bf16 [rows, K], W bf16 [groups, N, K], scales unused.
+ * C: fp32 or bf16 (c_dtype = MOE_OUT_*) [rows, N]; rows outside every group
+ *   are not written.  expert_offsets: device int32 [groups + 1].
+ * N multiple of 128; K multiple of 128 (FP8) or 64 (BF16); groups <= 1024.
+ * Tensor cores (tcgen05, accumulators in tensor memory) fed by TMA; weight
+ * rows sit on the MMA's M side and the few token rows of an expert on its
+ * N side (the SGLang/H20 article, section "SwapAB GEMM": map the token
+ * dimension to the fine-grained side of the MMA for small, variable rows
+ * per expert). */
+MOE_API int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32_t k_dim,
+                     int32_t rows, const void *a, const float *a_scales,
+                     const int32_t *expert_offsets, const void *w, const float *w_scales,
+                     void *c, int32_t c_dtype, int32_t *dev_status, void *stream);
+
+/* ---- combine -------------------------------------------------------------------
+ * out[t, :] = sum_s Y[expert_offsets[E+s] + t, :]
+ *           + sum_j topk_w[t, j] * Y[row_of_slot[t, j], :]    (fp32, shared
+ * first, then j ascending; slots with row -1 are skipped).
+ *   y bf16 [R_tot, H]; out fp32 or bf16 [T, H] (out_dtype = MOE_OUT_*).
+ * A gather per token: no atomics, no scatter (report, section "Overview":
+ * the combine that brings expert outputs back to their tokens). */
+MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
+                const float *topk_w, const int32_t *expert_offsets, void *out,
+                int32_t out_dtype, void *stream);
+
+/* ---- the whole layer -------------------------------------------------------------
+ * route -> (FP8: quantise x) -> permute -> grouped GEMM gate/up ->
+ * SiLU-mul (+ FP8 requantisation) -> grouped GEMM down -> combine, all on
+ * `stream`, all intermediates inside `ws` (size from moe_workspace_size for
+ * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..
+ * max_tokens.  The workspace's device status word is cleared at the start
+ * of every call; read it with moe_get_device_status after the stream has
+ * finished. */
+MOE_API int moe_workspace_size(const moe_config *cfg, size_t *bytes /* host */);
+MOE_API int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, const void *x,
+                      void *out, int32_t out_dtype, void *ws, size_t ws_bytes, void *stream);
+
+/* Byte offsets of the intermediates inside the layer workspace (host), for
+ * callers that want to read routing results or rows per expert. */
+typedef struct moe_ws_layout {
+    size_t status, logits, topk_ids, topk_w, xq, xs, expert_offsets, src_of_row,
+        row_of_slot, perm_scratch, xp, xp_scales, gate_up, h, h_scales, y, total;
+} moe_ws_layout;
+MOE_API int moe_workspace_layout(const moe_config *cfg, moe_ws_layout *layout /* host */);
+
+/* Synchronously reads the status word of a layer workspace (device) into
+ * *status (host).  Returns MOE_OK when no bit is set, MOE_ERR_TIMEOUT when
+ * MOE_DEV_TIMEOUT is set, MOE_ERR_DEVICE_FAULT for any other bit. */
+MOE_API int moe_get_device_status(const void *ws, int32_t *status /* host */);
+
+/* Static text for a MOE_OK / MOE_ERR_* code. */
+MOE_API const char *moe_status_string(int32_t code);
+
+/* Number of kernels moe_layer_forward enqueues for this configuration. */
+MOE_API int moe_layer_kernel_count(const moe_config *cfg, int32_t T);
+
+/* Self-test of the bounded waits (no counterpart on the pages: a robustness
+ * check of this library).  Launches one warp that waits on a completed
+ * mbarrier (must succeed) and on one nothing arrives on (must give up after
+ * limit_ns, 1e3..1e8, setting MOE_DEV_TIMEOUT in *dev_status).  Writes
+ * *dev_result = 1 (first wait passed) | 2 (second wait gave up).  The
+ * kernel always returns; nothing traps. */
+MOE_API int moe_selftest_bounded_wait(int32_t *dev_status, int64_t limit_ns, int32_t *dev_result,
+                                      void *stream);
+
+/* ---- host: balanced expert permutation ----------------------------------------------
+ * Report, section "Load balancing across GPUs": from measured activation
+ * counts, group the E experts into num_sets sets of E/num_sets with totals
+ * as even as possible (a variant of balanced number partitioning) and
+ * renumber them so each set is contiguous.  Objective: minimise the largest
+ * set total.  Exact (branch and bound) when E <= 16, otherwise
+ * cardinality-constrained greedy (largest first into the lightest open set)
+ * followed by improving pairwise swaps.  Set s holds physical ids
+ * [s*m, (s+1)*m), m = E/num_sets, logical ids ascending inside a set.
+ *   counts    host int64 [E], >= 0
+ *   log2phys  host int32 [E], written; phys2log host int32 [E], written
+ *   max_over_mean host, written (may be NULL): largest set total / mean
+ * Pure host code; usable without a GPU. */
+MOE_API int expert_balance_permutation(const int64_t *counts, int32_t num_experts, int32_t num_sets,
+                               int32_t *log2phys, int32_t *phys2log, double *max_over_mean);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

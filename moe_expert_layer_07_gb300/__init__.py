@@ -1,0 +1,266 @@
+"""moe_expert_layer_07_gb300: the DeepSeek-style MoE decode layer on one GB300.
+
+A thin ctypes binding of the C-ABI library libmoe_gb300.so (declared in
+include/moe_gb300.h).  The functions here only marshal arguments: every step
+of the layer runs in the library's CUDA kernels.  PyTorch supplies device
+memory and streams.  If the library has not been built, importing the
+compute entry points raises: there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as LIB_PATH
+
+__all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_requant",
+           "permute", "permute_workspace_size", "grouped_gemm", "combine", "layer_forward",
+           "workspace_size", "workspace_layout", "get_device_status", "status_string",
+           "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
+           "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
+           "ACT_SILU_MUL"]
+
+SOFTMAX, SIGMOID = 0, 1
+BF16, FP8 = 0, 1
+OUT_F32, OUT_BF16 = 0, 1
+ACT_IDENTITY, ACT_SILU_MUL = 0, 1
+DEV_BAD_EXPERT_ID, DEV_BAD_OFFSETS, DEV_TIMEOUT = 1, 2, 4
+
+
+class MoEError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        super().__init__(f"{where}: {status_string(code)} ({code})")
+        self.code = code
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in
+                ("hidden", "inter", "num_experts", "num_shared", "top_k", "num_groups",
+                 "topk_groups", "group_topn", "scoring", "norm_topk", "dtype", "max_tokens")] + \
+               [("routed_scaling", ctypes.c_float)]
+
+
+class Weights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w_gate", "e_bias", "logit_offset", "log2phys", "w13", "w13_scales", "w2",
+                 "w2_scales")]
+
+
+class WsLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("status", "logits", "topk_ids", "topk_w", "xq", "xs", "expert_offsets",
+                 "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "gate_up",
+                 "h", "h_scales", "y", "total")]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_CP = ctypes.POINTER(Config)
+
+_SIGS = {
+    "moe_route": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "moe_act_requant": [_CP, _I, _I, _P, _P, _P, _P, _P],
+    "moe_permute_workspace_size": [_CP, _I, ctypes.POINTER(ctypes.c_size_t)],
+    "moe_permute": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
+    "moe_grouped_gemm": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P],
+    "moe_combine": [_CP, _I, _P, _P, _P, _P, _P, _I, _P],
+    "moe_workspace_size": [_CP, ctypes.POINTER(ctypes.c_size_t)],
+    "moe_layer_forward": [_CP, ctypes.POINTER(Weights), _I, _P, _P, _I, _P, ctypes.c_size_t, _P],
+    "moe_workspace_layout": [_CP, ctypes.POINTER(WsLayout)],
+    "moe_get_device_status": [_P, ctypes.POINTER(ctypes.c_int32)],
+    "moe_layer_kernel_count": [_CP, _I],
+    "expert_balance_permutation": [_P, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_double)],
+    "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
+}
+
+
+def lib():
+    """The loaded library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                              "(there is no non-CUDA fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, args in _SIGS.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.moe_status_string.argtypes = [ctypes.c_int32]
+        L.moe_status_string.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().moe_status_string(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise MoEError(rc, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def make_config(shape, max_tokens: int | None = None) -> Config:
+    """Config from any object with the layer's fields (e.g. synth.MoEShape)."""
+    return Config(hidden=shape.hidden, inter=shape.inter, num_experts=shape.num_experts,
+                  num_shared=shape.num_shared, top_k=shape.top_k, num_groups=shape.num_groups,
+                  topk_groups=shape.topk_groups, group_topn=shape.group_topn,
+                  scoring=SIGMOID if shape.scoring == "sigmoid" else SOFTMAX,
+                  norm_topk=int(bool(shape.norm_topk)),
+                  dtype=FP8 if shape.dtype == "fp8" else BF16,
+                  max_tokens=shape.tokens if max_tokens is None else max_tokens,
+                  routed_scaling=float(shape.routed_scaling))
+
+
+def route(cfg: Config, T, x, w_gate, e_bias, logit_offset, log2phys, logits, topk_ids, topk_w,
+          status=None, stream=None):
+    _check(lib().moe_route(ctypes.byref(cfg), T, _ptr(x), _ptr(w_gate), _ptr(e_bias),
+                           _ptr(logit_offset), _ptr(log2phys), _ptr(logits), _ptr(topk_ids),
+                           _ptr(topk_w), _ptr(status), _stream(stream)), "moe_route")
+
+
+def act_requant(cfg: Config, mode, rows, inp, out, out_scales=None, rows_dev=None, stream=None):
+    _check(lib().moe_act_requant(ctypes.byref(cfg), mode, rows, _ptr(rows_dev), _ptr(inp),
+                                 _ptr(out), _ptr(out_scales), _stream(stream)), "moe_act_requant")
+
+
+def permute_workspace_size(cfg: Config, T: int) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_permute_workspace_size(ctypes.byref(cfg), T, ctypes.byref(n)),
+           "moe_permute_workspace_size")
+    return n.value
+
+
+def permute(cfg: Config, T, topk_ids, x_rows, x_scales, expert_offsets, src_of_row,
+            row_of_slot, xp, xp_scales, ws, ws_bytes, status=None, stream=None):
+    _check(lib().moe_permute(ctypes.byref(cfg), T, _ptr(topk_ids), _ptr(x_rows), _ptr(x_scales),
+                             _ptr(expert_offsets), _ptr(src_of_row), _ptr(row_of_slot),
+                             _ptr(xp), _ptr(xp_scales), _ptr(ws), ws_bytes, _ptr(status),
+                             _stream(stream)), "moe_permute")
+
+
+def grouped_gemm(cfg: Config, groups, n_out, k_dim, rows, a, a_scales, expert_offsets, w,
+                 w_scales, c, c_dtype, status=None, stream=None):
+    _check(lib().moe_grouped_gemm(ctypes.byref(cfg), groups, n_out, k_dim, rows, _ptr(a),
+                                  _ptr(a_scales), _ptr(expert_offsets), _ptr(w), _ptr(w_scales),
+                                  _ptr(c), c_dtype, _ptr(status), _stream(stream)),
+           "moe_grouped_gemm")
+
+
+def combine(cfg: Config, T, y, row_of_slot, topk_w, expert_offsets, out, out_dtype, stream=None):
+    _check(lib().moe_combine(ctypes.byref(cfg), T, _ptr(y), _ptr(row_of_slot), _ptr(topk_w),
+                             _ptr(expert_offsets), _ptr(out), out_dtype, _stream(stream)),
+           "moe_combine")
+
+
+def workspace_size(cfg: Config) -> int:
+    n = ctypes.c_size_t()
+    _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
+    return n.value
+
+
+def workspace_layout(cfg: Config) -> WsLayout:
+    L = WsLayout()
+    _check(lib().moe_workspace_layout(ctypes.byref(cfg), ctypes.byref(L)), "moe_workspace_layout")
+    return L
+
+
+def layer_kernel_count(cfg: Config, T: int) -> int:
+    return int(lib().moe_layer_kernel_count(ctypes.byref(cfg), T))
+
+
+def layer_forward(cfg: Config, weights: Weights, T, x, out, out_dtype, ws, ws_bytes, stream=None):
+    _check(lib().moe_layer_forward(ctypes.byref(cfg), ctypes.byref(weights), T, _ptr(x), _ptr(out),
+                                   out_dtype, _ptr(ws), ws_bytes, _stream(stream)),
+           "moe_layer_forward")
+
+
+def get_device_status(ws) -> int:
+    v = ctypes.c_int32()
+    lib().moe_get_device_status(_ptr(ws), ctypes.byref(v))
+    return v.value
+
+
+def balance_permutation(counts, num_sets: int):
+    """Host call: (log2phys, phys2log, max_over_mean) from per-expert counts."""
+    import numpy as np
+    c = np.ascontiguousarray(counts, dtype=np.int64)
+    E = len(c)
+    l2p = np.empty(E, dtype=np.int32)
+    p2l = np.empty(E, dtype=np.int32)
+    mom = ctypes.c_double()
+    _check(lib().expert_balance_permutation(c.ctypes.data, E, num_sets, l2p.ctypes.data,
+                                            p2l.ctypes.data, ctypes.byref(mom)),
+           "expert_balance_permutation")
+    return l2p, p2l, mom.value
+
+
+class MoELayer:
+    """One MoE layer: device weights, a workspace and the forward call.
+
+    weights: dict of device tensors with keys wg, e_bias, logit_offset, w13,
+    w13_s, w2, w2_s (expert weights in physical order, shared experts last)
+    and optionally log2phys (int32).
+    """
+
+    def __init__(self, shape, weights: dict, max_tokens: int | None = None, log2phys=None):
+        import torch
+        self.cfg = make_config(shape, max_tokens)
+        self.shape = shape
+        self._keep = dict(weights)
+        if log2phys is not None:
+            self._keep["log2phys"] = torch.as_tensor(log2phys, dtype=torch.int32,
+                                                     device=weights["w13"].device)
+        k = self._keep
+        self.weights = Weights(w_gate=_ptr(k["wg"]), e_bias=_ptr(k.get("e_bias")),
+                               logit_offset=_ptr(k.get("logit_offset")),
+                               log2phys=_ptr(k.get("log2phys")), w13=_ptr(k["w13"]),
+                               w13_scales=_ptr(k.get("w13_s")), w2=_ptr(k["w2"]),
+                               w2_scales=_ptr(k.get("w2_s")))
+        self.ws_bytes = workspace_size(self.cfg)
+        self.layout = workspace_layout(self.cfg)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=weights["w13"].device)
+
+    def forward(self, x, out, out_dtype=OUT_F32, T=None, stream=None):
+        """x bf16 [T, H] and out [T, H] (fp32 or bf16) device tensors."""
+        T = x.shape[0] if T is None else T
+        layer_forward(self.cfg, self.weights, T, x, out, out_dtype, self.ws, self.ws_bytes, stream)
+        return out
+
+    def forward_host(self, x_host, out_host, x_dev, out_dev, out_dtype=OUT_F32, stream=None):
+        """End to end from pinned host memory: copy x in, run, copy out back."""
+        x_dev.copy_(x_host, non_blocking=True)
+        self.forward(x_dev, out_dev, out_dtype, stream=stream)
+        out_host.copy_(out_dev, non_blocking=True)
+        return out_host
+
+    def view(self, name, dtype, shape):
+        """A tensor view of one intermediate inside the workspace."""
+        import math
+        import torch
+        off = getattr(self.layout, name)
+        n = math.prod(shape)
+        nbytes = n * torch.empty((), dtype=dtype).element_size()
+        return self.ws[off:off + nbytes].view(dtype).view(*shape)
+
+    def status(self) -> int:
+        return get_device_status(self.ws)

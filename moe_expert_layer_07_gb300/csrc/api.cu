@@ -1,0 +1,289 @@
+// The C ABI: argument checks, workspace layout, the layer's launch sequence,
+// device status.  Every entry point validates before enqueuing anything and
+// never synchronises the host (except moe_get_device_status, which exists to).
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace moe {
+
+int check_config(const moe_config *c) {
+    if (!c) return MOE_ERR_INVALID_ARG;
+    if (c->scoring != MOE_SCORING_SOFTMAX && c->scoring != MOE_SCORING_SIGMOID)
+        return MOE_ERR_INVALID_ARG;
+    if (c->dtype != MOE_DTYPE_BF16 && c->dtype != MOE_DTYPE_FP8_BLOCK128) return MOE_ERR_INVALID_ARG;
+    if (c->hidden <= 0 || c->inter <= 0 || c->num_experts <= 0 || c->top_k <= 0 ||
+        c->num_shared < 0 || c->max_tokens < 0 || c->num_groups <= 0)
+        return MOE_ERR_INVALID_ARG;
+    if (c->hidden % 128 || c->inter % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->num_experts > 1024 || c->num_shared > 4 || c->top_k > 16) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (c->num_groups > 32 || c->num_experts % c->num_groups) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const int gs = c->num_experts / c->num_groups;
+    if (c->num_groups > 1) {
+        if (c->topk_groups <= 0 || c->topk_groups > c->num_groups) return MOE_ERR_INVALID_ARG;
+        if (c->group_topn <= 0 || c->group_topn > gs) return MOE_ERR_INVALID_ARG;
+        if (c->top_k > c->topk_groups * gs) return MOE_ERR_INVALID_ARG;
+    } else if (c->top_k > c->num_experts) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    if (!(c->routed_scaling == c->routed_scaling)) return MOE_ERR_INVALID_ARG;   // NaN
+    return MOE_OK;
+}
+
+int sm_count() {
+    static int counts[64];
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 1;
+    std::call_once(once[dev], [&] {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 1;
+        counts[dev] = n > 0 ? n : 1;
+    });
+    return counts[dev];
+}
+
+namespace {
+
+bool al16(const void *p) { return p == nullptr || aligned16(p); }
+
+int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
+    const int64_t E = cfg->num_experts, k = cfg->top_k, H = cfg->hidden, I = cfg->inter;
+    const int64_t G = groups_of(cfg), Rt = total_rows(cfg, Tm);
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    size_t off = 0;
+    auto take = [&](int64_t bytes) {
+        const size_t o = off;
+        off = align_up(off + (size_t)bytes);
+        return o;
+    };
+    L->status = take(4);
+    L->logits = take(4 * Tm * E);
+    L->topk_ids = take(4 * Tm * k);
+    L->topk_w = take(4 * Tm * k);
+    L->xq = take(fp8 ? Tm * H : 0);
+    L->xs = take(fp8 ? 4 * Tm * (H / 128) : 0);
+    L->expert_offsets = take(4 * (G + 1));
+    L->src_of_row = take(4 * Rt);
+    L->row_of_slot = take(4 * Tm * k);
+    L->perm_scratch = take((int64_t)permute_scratch_bytes(cfg, (int)Tm));
+    L->xp = take(Rt * H * (fp8 ? 1 : 2));
+    L->xp_scales = take(fp8 ? 4 * Rt * (H / 128) : 0);
+    L->gate_up = take(4 * Rt * 2 * I);
+    L->h = take(Rt * I * (fp8 ? 1 : 2));
+    L->h_scales = take(fp8 ? 4 * Rt * (I / 128) : 0);
+    L->y = take(2 * Rt * H);
+    L->total = off;
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+const char *moe_status_string(int32_t code) {
+    switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_FAULT: return "device reported invalid data";
+    default: return "unknown status";
+    }
+}
+
+int moe_route(const moe_config *cfg, int32_t T, const void *x, const void *w_gate,
+              const float *e_bias, const float *logit_offset, const int32_t *log2phys,
+              float *logits, int32_t *topk_ids, float *topk_w, int32_t *dev_status,
+              void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !w_gate || !logits || !topk_ids || !topk_w) return MOE_ERR_INVALID_ARG;
+    if (!al16(x) || !al16(w_gate)) return MOE_ERR_INVALID_ARG;
+    if (e_bias && cfg->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+    return launch_route(cfg, T, x, w_gate, e_bias, logit_offset, log2phys, logits, topk_ids,
+                        topk_w, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int moe_act_requant(const moe_config *cfg, int32_t mode, int32_t rows, const int32_t *rows_dev,
+                    const void *in, void *out, float *out_scales, void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (rows < 0 || (mode != MOE_ACT_IDENTITY && mode != MOE_ACT_SILU_MUL))
+        return MOE_ERR_INVALID_ARG;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    if (mode == MOE_ACT_IDENTITY && !fp8) return MOE_ERR_INVALID_ARG;
+    if (rows == 0) return MOE_OK;
+    if (!in || !out || (fp8 && !out_scales)) return MOE_ERR_INVALID_ARG;
+    if (!al16(in) || !al16(out)) return MOE_ERR_INVALID_ARG;
+    return launch_act_requant(cfg, mode, rows, rows_dev, in, out, out_scales,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int moe_permute_workspace_size(const moe_config *cfg, int32_t T, size_t *bytes) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (T < 0 || !bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = permute_scratch_bytes(cfg, T);
+    return MOE_OK;
+}
+
+int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_ids, const void *x_rows,
+                const float *x_scales, int32_t *expert_offsets, int32_t *src_of_row,
+                int32_t *row_of_slot, void *xp, float *xp_scales, void *ws, size_t ws_bytes,
+                int32_t *dev_status, void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (T < 0 || !expert_offsets) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    if (T > 0 && (!topk_ids || !x_rows || !src_of_row || !row_of_slot || !xp ||
+                  (fp8 && (!x_scales || !xp_scales))))
+        return MOE_ERR_INVALID_ARG;
+    if (!al16(x_rows) || !al16(xp)) return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < permute_scratch_bytes(cfg, T) || (T > 0 && !ws))
+        return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return launch_permute(cfg, T, topk_ids, x_rows, x_scales, expert_offsets, src_of_row,
+                          row_of_slot, xp, xp_scales, ws, dev_status,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32_t k_dim,
+                     int32_t rows, const void *a, const float *a_scales,
+                     const int32_t *expert_offsets, const void *w, const float *w_scales,
+                     void *c, int32_t c_dtype, int32_t *dev_status, void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    if (groups <= 0 || rows < 0 || n_out <= 0 || k_dim <= 0) return MOE_ERR_INVALID_ARG;
+    if (c_dtype != MOE_OUT_F32 && c_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
+    if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (n_out % 128 || k_dim % (fp8 ? 128 : 64)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)groups * n_out > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!a || !w || !c || !expert_offsets || (fp8 && (!a_scales || !w_scales)))
+        return MOE_ERR_INVALID_ARG;
+    if (!al16(a) || !al16(w) || !al16(c)) return MOE_ERR_INVALID_ARG;
+    return launch_grouped_gemm(fp8, groups, n_out, k_dim, rows, a, a_scales, expert_offsets, w,
+                               w_scales, c, c_dtype, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
+                const float *topk_w, const int32_t *expert_offsets, void *out, int32_t out_dtype,
+                void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (T < 0 || (out_dtype != MOE_OUT_F32 && out_dtype != MOE_OUT_BF16)) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!y || !row_of_slot || !topk_w || !expert_offsets || !out) return MOE_ERR_INVALID_ARG;
+    if (!al16(y) || !al16(out)) return MOE_ERR_INVALID_ARG;
+    return launch_combine(cfg, T, y, row_of_slot, topk_w, expert_offsets, out, out_dtype,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int moe_workspace_layout(const moe_config *cfg, moe_ws_layout *L) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (!L) return MOE_ERR_INVALID_ARG;
+    return layout(cfg, cfg->max_tokens, L);
+}
+
+int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    moe_ws_layout L;
+    int rc = moe_workspace_layout(cfg, &L);
+    if (rc) return rc;
+    *bytes = L.total;
+    return MOE_OK;
+}
+
+int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
+    if (check_config(cfg) || T <= 0) return 0;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    // route, (quantise x), permute, gemm, act, gemm, combine
+    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count() + 1 + 1 + 1 + 1;
+}
+
+int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, const void *x,
+                      void *out, int32_t out_dtype, void *ws, size_t ws_bytes, void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (!w || !ws || T < 0 || T > cfg->max_tokens) return MOE_ERR_INVALID_ARG;
+    if (out_dtype != MOE_OUT_F32 && out_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    if (T > 0 && (!x || !out)) return MOE_ERR_INVALID_ARG;
+    if (!w->w_gate || !w->w13 || !w->w2 || (fp8 && (!w->w13_scales || !w->w2_scales)))
+        return MOE_ERR_INVALID_ARG;
+    if (w->e_bias && cfg->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (!al16(x) || !al16(out) || !al16(ws) || !al16(w->w_gate) || !al16(w->w13) ||
+        !al16(w->w2))
+        return MOE_ERR_INVALID_ARG;
+    moe_ws_layout L;
+    layout(cfg, cfg->max_tokens, &L);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *base = static_cast<uint8_t *>(ws);
+    int32_t *status = reinterpret_cast<int32_t *>(base + L.status);
+    MOE_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s));
+    if (T == 0) return MOE_OK;
+
+    const int E = cfg->num_experts, G = groups_of(cfg), H = cfg->hidden, I = cfg->inter;
+    const int rows = (int)total_rows(cfg, T);
+    float *logits = reinterpret_cast<float *>(base + L.logits);
+    int32_t *ids = reinterpret_cast<int32_t *>(base + L.topk_ids);
+    float *tw = reinterpret_cast<float *>(base + L.topk_w);
+    int32_t *offsets = reinterpret_cast<int32_t *>(base + L.expert_offsets);
+    int32_t *src = reinterpret_cast<int32_t *>(base + L.src_of_row);
+    int32_t *ros = reinterpret_cast<int32_t *>(base + L.row_of_slot);
+    (void)E;
+
+    rc = launch_route(cfg, T, x, w->w_gate, w->e_bias, w->logit_offset, w->log2phys, logits, ids,
+                      tw, status, s);
+    if (rc) return rc;
+    const void *rows_src = x;
+    const float *rows_scales = nullptr;
+    if (fp8) {
+        rc = launch_act_requant(cfg, MOE_ACT_IDENTITY, T, nullptr, x, base + L.xq,
+                                reinterpret_cast<float *>(base + L.xs), s);
+        if (rc) return rc;
+        rows_src = base + L.xq;
+        rows_scales = reinterpret_cast<const float *>(base + L.xs);
+    }
+    rc = launch_permute(cfg, T, ids, rows_src, rows_scales, offsets, src, ros, base + L.xp,
+                        reinterpret_cast<float *>(base + L.xp_scales), base + L.perm_scratch,
+                        status, s);
+    if (rc) return rc;
+    rc = launch_grouped_gemm(fp8, G, 2 * I, H, rows, base + L.xp,
+                             reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
+                             w->w13_scales, base + L.gate_up, MOE_OUT_F32, status, s);
+    if (rc) return rc;
+    rc = launch_act_requant(cfg, MOE_ACT_SILU_MUL, rows, offsets + G, base + L.gate_up,
+                            base + L.h, reinterpret_cast<float *>(base + L.h_scales), s);
+    if (rc) return rc;
+    rc = launch_grouped_gemm(fp8, G, H, I, rows, base + L.h,
+                             reinterpret_cast<const float *>(base + L.h_scales), offsets, w->w2,
+                             w->w2_scales, base + L.y, MOE_OUT_BF16, status, s);
+    if (rc) return rc;
+    return launch_combine(cfg, T, base + L.y, ros, tw, offsets, out, out_dtype, s);
+}
+
+int moe_get_device_status(const void *ws, int32_t *status) {
+    if (!ws || !status) return MOE_ERR_INVALID_ARG;
+    int32_t v = 0;
+    // the status word is the first field of the layer workspace
+    if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    *status = v;
+    if (v == 0) return MOE_OK;
+    return (v & MOE_DEV_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_FAULT;
+}
+
+}  // extern "C"

@@ -1,0 +1,169 @@
+// Balanced expert permutation (Moreh report "21K output tokens/s DeepSeek
+// inference on MI300X with Expert Parallelism", section "Load balancing
+// across GPUs"): group the experts into equal-size sets whose summed
+// activation counts are as even as possible, then renumber them so every
+// set is a contiguous block of physical ids.  The report calls it a variant
+// of balanced number partitioning and gives no algorithm; this one minimises
+// the largest set total:
+//   E <= 16  exact branch and bound (items in decreasing count, a new set is
+//            opened only as the first empty one, bound = current best);
+//   E > 16   greedy (largest count first into the lightest set with room)
+//            followed by improving swaps between the heaviest set and any
+//            other, best swap first, until none lowers the heaviest set.
+// Host-only code.
+#include <algorithm>
+#include <cstdint>
+#include <numeric>
+#include <vector>
+
+#include "../../include/moe_gb300.h"
+
+namespace {
+
+struct Partition {
+    std::vector<int> set_of;   // per expert
+    std::vector<int64_t> load;
+};
+
+Partition greedy(const std::vector<int64_t> &c, int S, int m) {
+    const int E = (int)c.size();
+    std::vector<int> order(E);
+    std::iota(order.begin(), order.end(), 0);
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return c[a] > c[b]; });
+    Partition p;
+    p.set_of.assign(E, -1);
+    p.load.assign(S, 0);
+    std::vector<int> size(S, 0);
+    for (int e : order) {
+        int best = -1;
+        for (int s = 0; s < S; ++s)
+            if (size[s] < m && (best < 0 || p.load[s] < p.load[best])) best = s;
+        p.set_of[e] = best;
+        p.load[best] += c[e];
+        ++size[best];
+    }
+    return p;
+}
+
+void improve_by_swaps(const std::vector<int64_t> &c, int S, Partition &p) {
+    const int E = (int)c.size();
+    for (int iter = 0; iter < 100000; ++iter) {
+        int A = 0;
+        for (int s = 1; s < S; ++s)
+            if (p.load[s] > p.load[A]) A = s;
+        int64_t best_new = p.load[A];
+        int ba = -1, bb = -1;
+        for (int a = 0; a < E; ++a) {
+            if (p.set_of[a] != A) continue;
+            for (int b = 0; b < E; ++b) {
+                const int B = p.set_of[b];
+                if (B == A || c[b] >= c[a]) continue;
+                const int64_t d = c[a] - c[b];
+                const int64_t nm = std::max(p.load[A] - d, p.load[B] + d);
+                if (nm < best_new) {
+                    best_new = nm;
+                    ba = a;
+                    bb = b;
+                }
+            }
+        }
+        if (ba < 0) return;
+        const int B = p.set_of[bb];
+        const int64_t d = c[ba] - c[bb];
+        p.load[A] -= d;
+        p.load[B] += d;
+        std::swap(p.set_of[ba], p.set_of[bb]);
+    }
+}
+
+struct Exact {
+    const std::vector<int64_t> &c;
+    std::vector<int> order;
+    int S, m;
+    std::vector<int64_t> load;
+    std::vector<int> size, assign, best_assign;
+    int64_t best;
+
+    Exact(const std::vector<int64_t> &counts, int S_, int m_, const Partition &seed)
+        : c(counts), S(S_), m(m_) {
+        const int E = (int)c.size();
+        order.resize(E);
+        std::iota(order.begin(), order.end(), 0);
+        std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return c[a] > c[b]; });
+        load.assign(S, 0);
+        size.assign(S, 0);
+        assign.assign(E, -1);
+        best_assign = seed.set_of;
+        best = *std::max_element(seed.load.begin(), seed.load.end());
+    }
+    void run(int i, int64_t cur_max) {
+        if (cur_max >= best) return;
+        if (i == (int)order.size()) {
+            best = cur_max;
+            best_assign = assign;
+            return;
+        }
+        const int e = order[i];
+        bool tried_empty = false;
+        for (int s = 0; s < S; ++s) {
+            if (size[s] == m) continue;
+            if (size[s] == 0) {
+                if (tried_empty) continue;   // empty sets are interchangeable
+                tried_empty = true;
+            }
+            load[s] += c[e];
+            ++size[s];
+            assign[e] = s;
+            run(i + 1, std::max(cur_max, load[s]));
+            assign[e] = -1;
+            --size[s];
+            load[s] -= c[e];
+        }
+    }
+};
+
+}  // namespace
+
+extern "C" int expert_balance_permutation(const int64_t *counts, int32_t num_experts,
+                                          int32_t num_sets, int32_t *log2phys, int32_t *phys2log,
+                                          double *max_over_mean) {
+    if (!counts || !log2phys || !phys2log || num_experts <= 0 || num_sets <= 0 ||
+        num_experts % num_sets)
+        return MOE_ERR_INVALID_ARG;
+    const int E = num_experts, S = num_sets, m = E / S;
+    std::vector<int64_t> c(counts, counts + E);
+    for (int64_t v : c)
+        if (v < 0) return MOE_ERR_INVALID_ARG;
+
+    Partition p = greedy(c, S, m);
+    improve_by_swaps(c, S, p);
+    if (E <= 16) {
+        Exact ex(c, S, m, p);
+        ex.run(0, 0);
+        p.set_of = ex.best_assign;
+        p.load.assign(S, 0);
+        for (int e = 0; e < E; ++e) p.load[p.set_of[e]] += c[e];
+    }
+
+    // Sets are numbered by their lowest logical id; inside a set, logical ids ascend.
+    std::vector<int> first(S, E);
+    for (int e = 0; e < E; ++e) first[p.set_of[e]] = std::min(first[p.set_of[e]], e);
+    std::vector<int> set_rank(S);
+    std::iota(set_rank.begin(), set_rank.end(), 0);
+    std::sort(set_rank.begin(), set_rank.end(), [&](int a, int b) { return first[a] < first[b]; });
+    std::vector<int> slot_of_set(S);
+    for (int r = 0; r < S; ++r) slot_of_set[set_rank[r]] = r;
+    std::vector<int> fill(S, 0);
+    for (int e = 0; e < E; ++e) {
+        const int s = slot_of_set[p.set_of[e]];
+        const int phys = s * m + fill[s]++;
+        log2phys[e] = phys;
+        phys2log[phys] = e;
+    }
+    if (max_over_mean) {
+        const int64_t total = std::accumulate(c.begin(), c.end(), (int64_t)0);
+        const int64_t mx = *std::max_element(p.load.begin(), p.load.end());
+        *max_over_mean = total > 0 ? (double)mx * S / (double)total : 1.0;
+    }
+    return MOE_OK;
+}

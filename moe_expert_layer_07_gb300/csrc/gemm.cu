@@ -1,0 +1,495 @@
+// Grouped GEMM over per-expert row blocks on the 5th-generation tensor cores.
+//
+//   C[r, n] = sum_k A[r, k] W[g, n, k]   for rows r of group g
+//
+// Weight rows are the MMA's M side (128 per tile) and the few token rows of
+// an expert its N side (16..BN per tile), so that a decode-sized expert with
+// a handful of rows still streams its weights at full tile efficiency.  The
+// SGLang/H20 article (section "SwapAB GEMM") makes the same swap on Hopper,
+// where WGMMA fixes M = 64; tcgen05 with M = 128 and N a multiple of 16 is
+// the analogue here.
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0      TMA producer: per K-block a 128 x 128-byte weight box and
+//               ceil(rows/16) 16 x 128-byte activation boxes, 128-byte
+//               swizzled, into a STAGES-deep shared-memory ring.
+//   warp 1      MMA issuer (one thread): tcgen05.mma, K = 32 bytes per
+//               instruction, accumulators in tensor memory, completion
+//               signalled with tcgen05.commit.
+//   warps 2-5   epilogue: tcgen05.ld of the accumulator (thread = weight
+//               row), then
+//                 FP8: per 128-wide K block, the block's partial product is
+//                 scaled by w_scale[g, m/128, kb] * a_scale[r, kb] and added
+//                 to fp32 registers (two TMEM buffers alternate so the next
+//                 block's MMAs run meanwhile);
+//                 BF16: one accumulation over all of K (two TMEM buffers
+//                 alternate between tiles);
+//               and stores C (coalesced: a warp writes 32 consecutive n).
+// Work units are (group, 128-row weight tile, BN-row activation tile); the
+// tile table is built on the device from expert_offsets, so no host sync is
+// needed and the launch can be captured in a graph.  Every wait is bounded:
+// after about a second the CTA records MOE_DEV_TIMEOUT, drains its copies
+// and MMAs, frees its tensor memory and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kMaxGroups = 1024;
+constexpr int kThreads = 192;
+constexpr int kBoxRows = 16;   // activation rows per TMA box
+
+template <bool FP8, int BN, int STAGES>
+struct GemmShape {
+    static constexpr int kABytes = kBM * 128;
+    static constexpr int kBBytes = BN * 128;
+    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kSmemBytes = STAGES * kStageBytes + 1024;
+    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kKPerStage = FP8 ? 128 : 64;   // elements of K per stage
+    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN");
+    static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns must be a power of two");
+    static_assert(kSmemBytes <= 227 * 1024 - 9 * 1024, "shared memory");
+};
+
+struct GemmArgs {
+    int groups, n_out, k_dim, rows;
+    const int32_t *offsets;
+    const float *a_scales;
+    const float *w_scales;
+    void *c;
+    int c_bf16;
+    int32_t *status;
+};
+
+struct Tile {
+    int g, mt, row0, nvalid;
+};
+
+template <int BN>
+__device__ __forceinline__ Tile decode_tile(int t, int G, const int *s_tiles, const int *s_off) {
+    int lo = 0, hi = G;   // s_tiles[lo] <= t < s_tiles[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_tiles[mid] <= t) lo = mid;
+        else hi = mid;
+    }
+    Tile tl;
+    tl.g = lo;
+    const int rows = s_off[lo + 1] - s_off[lo];
+    const int ntn = (rows + BN - 1) / BN;
+    const int local = t - s_tiles[lo];
+    tl.mt = local / ntn;
+    const int nt = local - tl.mt * ntn;
+    tl.row0 = s_off[lo] + nt * BN;
+    tl.nvalid = min(BN, rows - nt * BN);
+    return tl;
+}
+
+template <bool FP8, int BN, int STAGES>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmA, const GemmArgs args) {
+    using S = GemmShape<FP8, BN, STAGES>;
+    extern __shared__ uint8_t dsmem[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
+    __shared__ __align__(8) uint64_t acc_full[2];
+    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_abort, s_bad;
+    __shared__ int s_off[kMaxGroups + 1];
+    __shared__ int s_tiles[kMaxGroups + 1];
+
+    using namespace ptx;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t smem_base = (smem_u32(dsmem) + 1023u) & ~1023u;
+    const int G = args.groups;
+    const int MT = args.n_out / kBM;
+    const int KB = args.k_dim / S::kKPerStage;
+    volatile int *abort_flag = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 4);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        s_abort = 0;
+        s_bad = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), S::kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmA);
+    }
+    for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = args.offsets[i];
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+        const int a = s_off[g], b = s_off[g + 1];
+        if (a < 0 || b < a || b > args.rows) s_bad = 1;
+    }
+    __syncthreads();
+    if (warp == 0) {   // tile prefix over groups: lane L owns a contiguous run
+        const int per = (G + 31) / 32;
+        const int g0 = lane * per;
+        int local = 0;
+        for (int q = 0; q < per; ++q) {
+            const int g = g0 + q;
+            if (g < G) local += MT * ((s_off[g + 1] - s_off[g] + BN - 1) / BN);
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int run = incl - local;
+        for (int q = 0; q < per; ++q) {
+            const int g = g0 + q;
+            if (g < G) {
+                s_tiles[g] = run;
+                run += MT * ((s_off[g + 1] - s_off[g] + BN - 1) / BN);
+            }
+        }
+        if (lane == 31) s_tiles[G] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+    const int total_tiles = s_bad ? 0 : s_tiles[G];
+    if (s_bad && threadIdx.x == 0 && blockIdx.x == 0 && args.status)
+        atomicOr(args.status, MOE_DEV_BAD_OFFSETS);
+
+    if (warp == 0) {
+        // ------------------------------ TMA producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();   // weights: read once
+            const uint64_t pol_a = policy_evict_last();    // activations: re-read
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, parity_bits = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
+                const int nbox = (tl.nvalid + kBoxRows - 1) / kBoxRows;
+                const uint32_t bytes = S::kABytes + nbox * kBoxRows * 128;
+                const int wrow = tl.g * args.n_out + tl.mt * kBM;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_base + stage * S::kStageBytes;
+                    const uint32_t sb = sa + S::kABytes;
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    tma_load_2d(sa, &tmW, kb * S::kKPerStage, wrow, fb, pol_w);
+                    for (int b = 0; b < nbox; ++b)
+                        tma_load_2d(sb + b * kBoxRows * 128, &tmA, kb * S::kKPerStage,
+                                    tl.row0 + b * kBoxRows, fb, pol_a);
+                    issued |= 1u << stage;
+                    parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {   // let every copy in flight land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if ((issued >> s) & 1u)
+                        wait_drain(smem_u32(&full_bar[s]), (parity_bits >> s) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, ab = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
+                const int nmma = ((tl.nvalid + 15) / 16) * 16;
+                const uint32_t idesc = FP8 ? idesc_e4m3(kBM, nmma) : idesc_bf16(kBM, nmma);
+                if (!FP8) {
+                    if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (FP8) {
+                        if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
+                                          args.status, MOE_DEV_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                    }
+                    if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_base + stage * S::kStageBytes;
+                    const uint64_t da = sdesc_k_sw128(sa);
+                    const uint64_t db = sdesc_k_sw128(sa + S::kABytes);
+                    const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K
+                        const uint32_t acc = FP8 ? (kk > 0) : (kb > 0 || kk > 0);
+                        if (FP8) mma_f8f6f4(d, da + 2 * kk, db + 2 * kk, idesc, acc);
+                        else mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, acc);
+                    }
+                    mma_commit(smem_u32(&empty_bar[stage]));
+                    if (FP8) {
+                        mma_commit(smem_u32(&acc_full[ab]));
+                        ab ^= 1;
+                        if (ab == 0) aphase ^= 1u;
+                    }
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                if (!FP8) {
+                    mma_commit(smem_u32(&acc_full[ab]));
+                    ab ^= 1;
+                    if (ab == 0) aphase ^= 1u;
+                }
+            }
+            // every MMA issued by this thread completes before teardown
+            mma_commit(smem_u32(&drain_bar));
+            wait_drain(smem_u32(&drain_bar), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                    // TMEM lanes [32q, 32q + 32)
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+        const int m_local = q * 32 + lane;
+        int ab = 0;
+        uint32_t aphase = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
+            const int nchunks = (tl.nvalid + 15) / 16;
+            const int m_glob = tl.mt * kBM + m_local;
+            if (FP8) {
+                float acc[BN];
+#pragma unroll
+                for (int n = 0; n < BN; ++n) acc[n] = 0.0f;
+                const float *wsp = args.w_scales + ((size_t)tl.g * MT + tl.mt) * KB;
+                const float *xsp = args.a_scales + (size_t)tl.row0 * KB;
+                float nsw = __ldg(wsp);
+                float nx[BN / 32];
+#pragma unroll
+                for (int h = 0; h < BN / 32; ++h)
+                    nx[h] = (h * 32 + lane < tl.nvalid) ? __ldg(xsp + (size_t)(h * 32 + lane) * KB) : 0.0f;
+                for (int kb = 0; kb < KB; ++kb) {
+                    float sx[BN / 32];
+#pragma unroll
+                    for (int h = 0; h < BN / 32; ++h) sx[h] = nx[h] * nsw;
+                    if (kb + 1 < KB) {   // next block's scales, while this block's MMAs run
+                        nsw = __ldg(wsp + kb + 1);
+#pragma unroll
+                        for (int h = 0; h < BN / 32; ++h)
+                            nx[h] = (h * 32 + lane < tl.nvalid)
+                                        ? __ldg(xsp + (size_t)(h * 32 + lane) * KB + kb + 1)
+                                        : 0.0f;
+                    }
+                    if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
+                                      MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t v[BN / 16][16];
+#pragma unroll
+                    for (int c = 0; c < BN / 16; ++c)
+                        if (c < nchunks) {
+                            tmem_ld16(lane_base + (uint32_t)(ab * BN + c * 16), v[c]);
+                            tmem_wait_ld(v[c]);
+                        }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+                    ab ^= 1;
+                    if (ab == 0) aphase ^= 1u;
+#pragma unroll
+                    for (int c = 0; c < BN / 16; ++c)
+                        if (c < nchunks) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int n = c * 16 + j;
+                                const float scale = __shfl_sync(0xffffffffu, sx[n / 32], n & 31);
+                                acc[n] = fmaf(__uint_as_float(v[c][j]), scale, acc[n]);
+                            }
+                        }
+                }
+                if (!ok) break;
+                if (args.c_bf16) {
+                    __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(args.c);
+#pragma unroll
+                    for (int n = 0; n < BN; ++n)
+                        if (n < tl.nvalid)
+                            C[(size_t)(tl.row0 + n) * args.n_out + m_glob] = __float2bfloat16_rn(acc[n]);
+                } else {
+                    float *C = static_cast<float *>(args.c);
+#pragma unroll
+                    for (int n = 0; n < BN; ++n)
+                        if (n < tl.nvalid) C[(size_t)(tl.row0 + n) * args.n_out + m_glob] = acc[n];
+                }
+            } else {
+                if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
+                                  MOE_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int c = 0; c < BN / 16; ++c)
+                    if (c < nchunks) {
+                        uint32_t v[16];
+                        tmem_ld16(lane_base + (uint32_t)(ab * BN + c * 16), v);
+                        tmem_wait_ld(v);
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const int n = c * 16 + j;
+                            if (n < tl.nvalid) {
+                                const size_t idx = (size_t)(tl.row0 + n) * args.n_out + m_glob;
+                                if (args.c_bf16)
+                                    static_cast<__nv_bfloat16 *>(args.c)[idx] =
+                                        __float2bfloat16_rn(__uint_as_float(v[j]));
+                                else
+                                    static_cast<float *>(args.c)[idx] = __uint_as_float(v[j]);
+                            }
+                        }
+                    }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+                ab ^= 1;
+                if (ab == 0) aphase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, S::kTmemCols);
+    }
+}
+
+// ---- host side ---------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// Row-major [outer, inner] matrix, box of 128 bytes x box_rows, 128-byte swizzle.
+bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint64_t outer,
+               uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    const uint32_t esize = fp8 ? 1 : 2;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * esize};
+    cuuint32_t box[2] = {128 / esize, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                     const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <bool FP8, int BN, int STAGES>
+int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t s) {
+    using Sh = GemmShape<FP8, BN, STAGES>;
+    auto kern = grouped_gemm_kernel<FP8, BN, STAGES>;
+    static std::once_flag attr_once[64];
+    static int attr_rc[64];
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    std::call_once(attr_once[dev], [&] {
+        attr_rc[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            Sh::kSmemBytes) == cudaSuccess
+                           ? 0
+                           : 1;
+    });
+    if (attr_rc[dev]) return MOE_ERR_CUDA;
+    CUtensorMap tmW, tmA;
+    if (!encode_2d(&tmW, w, FP8, (uint64_t)args.k_dim, (uint64_t)args.groups * args.n_out, kBM))
+        return MOE_ERR_CUDA;
+    if (!encode_2d(&tmA, a, FP8, (uint64_t)args.k_dim, (uint64_t)args.rows, kBoxRows))
+        return MOE_ERR_CUDA;
+    const int64_t tiles_bound =
+        (int64_t)(args.n_out / kBM) * (args.groups + ceil_div(args.rows, BN));
+    const int grid = (int)std::min<int64_t>(sm_count(), tiles_bound);
+    if (grid <= 0) return MOE_OK;
+    kern<<<grid, kThreads, Sh::kSmemBytes, s>>>(tmW, tmA, args);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+}  // namespace
+
+int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, const void *a,
+                        const float *a_scales, const int32_t *offsets, const void *w,
+                        const float *w_scales, void *c, int c_dtype, int32_t *status,
+                        cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    GemmArgs args;
+    args.groups = groups;
+    args.n_out = n_out;
+    args.k_dim = k_dim;
+    args.rows = rows;
+    args.offsets = offsets;
+    args.a_scales = a_scales;
+    args.w_scales = w_scales;
+    args.c = c;
+    args.c_bf16 = c_dtype == MOE_OUT_BF16;
+    args.status = status;
+    if (fp8) return launch_impl<true, 64, 8>(args, a, w, s);
+    return launch_impl<false, 64, 8>(args, a, w, s);
+}
+
+}  // namespace moe

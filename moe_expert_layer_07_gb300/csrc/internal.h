@@ -1,0 +1,66 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_gb300.h"
+
+namespace moe {
+
+// Every buffer is 256-byte aligned inside a workspace.
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t v, size_t a = kAlign) { return (v + a - 1) / a * a; }
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Validates a configuration; returns MOE_OK or an error code.
+int check_config(const moe_config *cfg);
+
+// Rows of the permuted activations for T tokens.
+inline int64_t total_rows(const moe_config *cfg, int64_t T) {
+    return T * (int64_t)(cfg->top_k + cfg->num_shared);
+}
+inline int groups_of(const moe_config *cfg) { return cfg->num_experts + cfg->num_shared; }
+
+// Number of streaming multiprocessors of the current device (cached).
+int sm_count();
+
+// ---- launchers (validated arguments; return MOE_OK or MOE_ERR_CUDA) ----
+int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate,
+                 const float *e_bias, const float *logit_offset, const int32_t *log2phys,
+                 float *logits, int32_t *topk_ids, float *topk_w, int32_t *status,
+                 cudaStream_t s);
+int launch_act_requant(const moe_config *cfg, int mode, int rows, const int32_t *rows_dev,
+                       const void *in, void *out, float *out_scales, cudaStream_t s);
+size_t permute_scratch_bytes(const moe_config *cfg, int T);
+int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const void *x_rows,
+                   const float *x_scales, int32_t *offsets, int32_t *src_of_row,
+                   int32_t *row_of_slot, void *xp, float *xp_scales, void *ws,
+                   int32_t *status, cudaStream_t s);
+int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, const void *a,
+                        const float *a_scales, const int32_t *offsets, const void *w,
+                        const float *w_scales, void *c, int c_dtype, int32_t *status,
+                        cudaStream_t s);
+int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *row_of_slot,
+                   const float *topk_w, const int32_t *offsets, void *out, int out_dtype,
+                   cudaStream_t s);
+
+// Kernel launches per call, for the layer's launch count.
+int route_kernel_count();
+int permute_kernel_count();
+
+}  // namespace moe
+
+#define MOE_CUDA_TRY(expr)                                   \
+    do {                                                     \
+        cudaError_t _e = (expr);                             \
+        if (_e != cudaSuccess) return MOE_ERR_CUDA;          \
+    } while (0)
+
+#define MOE_LAUNCH_CHECK()                                   \
+    do {                                                     \
+        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA; \
+    } while (0)

@@ -1,0 +1,314 @@
+// Gating and top-k routing (Moreh report "21K output tokens/s DeepSeek
+// inference on MI300X with Expert Parallelism", section "Overview": a light
+// gating network picks a few experts per token; section "Load balancing
+// across GPUs": the gate emits ids in the permuted expert order).
+//
+// Two kernels:
+//  gate_logits_kernel  l[t,e] = sum_h x[t,h] Wg[e,h] on CUDA cores with a
+//                      fixed order: lane L of a warp owns the 16-byte chunks
+//                      c = L, L+32, ... of the hidden dimension (elements
+//                      h with (h/8) mod 32 == L), accumulates them in
+//                      increasing h with fp32 FMA, and the 32 lane partials
+//                      meet in an xor butterfly (16, 8, 4, 2, 1).  A bf16
+//                      product is exact in fp32, so the result is a fixed
+//                      sequence of rounded additions: the routing decision
+//                      is reproducible bit for bit.  A warp computes a tile
+//                      of 4 tokens x 8 experts (32 accumulators per lane).
+//  route_select_kernel one warp per token: sigmoid (fp64, rounded to fp32)
+//                      or softmax scores, group scores from each group's
+//                      best group_topn, top groups, then top_k experts by
+//                      repeated warp-wide arg-max with ties to the lower
+//                      index; weights; ids mapped through log2phys.
+#include <cuda_bf16.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTB = 4;   // tokens per warp tile
+constexpr int kEB = 8;   // experts per warp tile
+constexpr int kLogitWarps = 4;
+static_assert(kTB * kEB == 32, "one output per lane");
+
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+
+__device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b, float acc) {
+    acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
+    acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
+    acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
+    acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
+    acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
+    acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
+    acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
+    acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
+    return acc;
+}
+
+__global__ void __launch_bounds__(kLogitWarps * 32)
+    gate_logits_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wg,
+                       const float *__restrict__ offset, float *__restrict__ logits, int T,
+                       int E, int H) {
+    const int lane = threadIdx.x & 31;
+    const int warp = blockIdx.x * kLogitWarps + (threadIdx.x >> 5);
+    const int e_tiles = (E + kEB - 1) / kEB;
+    const int t0 = (warp / e_tiles) * kTB;
+    const int e0 = (warp % e_tiles) * kEB;
+    if (t0 >= T) return;   // warp-uniform
+
+    float acc[kTB][kEB];
+#pragma unroll
+    for (int i = 0; i < kTB; ++i)
+#pragma unroll
+        for (int j = 0; j < kEB; ++j) acc[i][j] = 0.0f;
+
+    const int chunks = H / 8;
+    const uint4 zero = make_uint4(0, 0, 0, 0);
+    for (int c = lane; c < chunks; c += 32) {
+        uint4 xv[kTB], wv[kEB];
+#pragma unroll
+        for (int i = 0; i < kTB; ++i)
+            xv[i] = (t0 + i < T)
+                        ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * H) + c)
+                        : zero;
+#pragma unroll
+        for (int j = 0; j < kEB; ++j)
+            wv[j] = (e0 + j < E)
+                        ? __ldg(reinterpret_cast<const uint4 *>(wg + (size_t)(e0 + j) * H) + c)
+                        : zero;
+#pragma unroll
+        for (int i = 0; i < kTB; ++i)
+#pragma unroll
+            for (int j = 0; j < kEB; ++j) acc[i][j] = dot8(xv[i], wv[j], acc[i][j]);
+    }
+
+    float mine = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kTB; ++i)
+#pragma unroll
+        for (int j = 0; j < kEB; ++j) {
+            float v = acc[i][j];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
+            if (lane == i * kEB + j) mine = v;
+        }
+    const int t = t0 + lane / kEB, e = e0 + lane % kEB;
+    if (t < T && e < E) logits[(size_t)t * E + e] = offset ? __fadd_rn(mine, offset[e]) : mine;
+}
+
+struct SelectArgs {
+    int T, E, k, groups, topk_groups, topn, sigmoid, norm;
+    float scaling;
+    const float *logits, *bias;
+    const int32_t *log2phys;
+    int32_t *ids;
+    float *w;
+    int32_t *status;
+};
+
+// warp-wide arg-max with ties to the lower index; every lane gets the result
+__device__ __forceinline__ void warp_argmax(float &v, int &i) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+        if (ov > v || (ov == v && oi < i)) {
+            v = ov;
+            i = oi;
+        }
+    }
+}
+
+template <int PL>   // experts per lane: expert e = q*32 + lane, q < PL
+__global__ void __launch_bounds__(256) route_select_kernel(const SelectArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (t >= a.T) return;   // warp-uniform
+    const float *lrow = a.logits + (size_t)t * a.E;
+
+    float l[PL], s[PL], sel[PL];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int q = 0; q < PL; ++q) {
+        const int e = q * 32 + lane;
+        const bool ok = e < a.E;
+        l[q] = ok ? lrow[e] : 0.0f;
+        if (a.sigmoid) {
+            s[q] = (float)(1.0 / (1.0 + exp(-(double)l[q])));
+            sel[q] = (ok && a.bias) ? __fadd_rn(s[q], a.bias[e]) : s[q];
+        } else {
+            s[q] = l[q];
+            sel[q] = l[q];
+        }
+        if (ok) valid |= 1u << q;
+    }
+    uint32_t allowed = valid;
+
+    if (a.groups > 1) {
+        const int gs = a.E / a.groups;
+        float my_gscore = -FLT_MAX;
+        for (int g = 0; g < a.groups; ++g) {
+            uint32_t taken = 0;
+            float sum = 0.0f;
+            for (int r = 0; r < a.topn; ++r) {
+                float bv = -FLT_MAX;
+                int bi = INT_MAX;
+#pragma unroll
+                for (int q = 0; q < PL; ++q) {
+                    const int e = q * 32 + lane;
+                    if (((valid >> q) & 1u) && !((taken >> q) & 1u) && e >= g * gs &&
+                        e < (g + 1) * gs && (sel[q] > bv || (sel[q] == bv && e < bi))) {
+                        bv = sel[q];
+                        bi = e;
+                    }
+                }
+                warp_argmax(bv, bi);
+                if (bi != INT_MAX && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+                sum = (r == 0) ? bv : __fadd_rn(sum, bv);
+            }
+            if (lane == g) my_gscore = sum;
+        }
+        uint32_t gmask = 0;
+        for (int r = 0; r < a.topk_groups; ++r) {
+            float v = (lane < a.groups && !((gmask >> lane) & 1u)) ? my_gscore : -FLT_MAX;
+            int i = (lane < a.groups && !((gmask >> lane) & 1u)) ? lane : INT_MAX;
+            warp_argmax(v, i);
+            if (i != INT_MAX) gmask |= 1u << i;
+        }
+#pragma unroll
+        for (int q = 0; q < PL; ++q) {
+            const int e = q * 32 + lane;
+            if (((valid >> q) & 1u) && !((gmask >> (e / gs)) & 1u)) allowed &= ~(1u << q);
+        }
+    }
+
+    // top-k by repeated arg-max; lane j keeps slot j
+    uint32_t chosen = 0;
+    int my_id = 0;
+    float my_score = 0.0f;   // sigmoid s or softmax logit of slot `lane`
+    for (int j = 0; j < a.k; ++j) {
+        float bv = -FLT_MAX;
+        int bi = INT_MAX;
+#pragma unroll
+        for (int q = 0; q < PL; ++q) {
+            const int e = q * 32 + lane;
+            if (((allowed >> q) & 1u) && !((chosen >> q) & 1u) &&
+                (sel[q] > bv || (sel[q] == bv && e < bi))) {
+                bv = sel[q];
+                bi = e;
+            }
+        }
+        warp_argmax(bv, bi);
+        if (bi == INT_MAX) {   // fewer candidates than k (rejected on the host)
+            if (lane == 0 && a.status) atomicOr(a.status, MOE_DEV_BAD_EXPERT_ID);
+            return;
+        }
+        const int owner = bi & 31, oq = bi >> 5;
+        float sv = 0.0f;
+#pragma unroll
+        for (int q = 0; q < PL; ++q)
+            if (q == oq) sv = s[q];
+        sv = __shfl_sync(0xffffffffu, sv, owner);
+        if (lane == owner) chosen |= 1u << oq;
+        if (lane == j) {
+            my_id = bi;
+            my_score = sv;
+        }
+    }
+
+    float w = 0.0f;
+    if (a.sigmoid) {
+        float total = 0.0f;
+        for (int j = 0; j < a.k; ++j) total = __fadd_rn(total, __shfl_sync(0xffffffffu, my_score, j));
+        w = a.norm ? __fmul_rn(__fdiv_rn(my_score, total), a.scaling)
+                   : __fmul_rn(my_score, a.scaling);
+    } else {
+        float m = -FLT_MAX;
+#pragma unroll
+        for (int q = 0; q < PL; ++q)
+            if ((valid >> q) & 1u) m = fmaxf(m, l[q]);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        double denom = 0.0;
+        if (a.norm) {
+            for (int j = 0; j < a.k; ++j)
+                denom += exp((double)__shfl_sync(0xffffffffu, my_score, j) - (double)m);
+        } else {
+            double part = 0.0;
+#pragma unroll
+            for (int q = 0; q < PL; ++q)
+                if ((valid >> q) & 1u) part += exp((double)l[q] - (double)m);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+            denom = part;
+        }
+        w = (float)(exp((double)my_score - (double)m) / denom * (double)a.scaling);
+    }
+
+    if (lane < a.k) {
+        int id = my_id;
+        if (a.log2phys) {
+            id = a.log2phys[my_id];
+            if (id < 0 || id >= a.E) {
+                if (a.status) atomicOr(a.status, MOE_DEV_BAD_EXPERT_ID);
+                id = -1;
+            }
+        }
+        a.ids[(size_t)t * a.k + lane] = id;
+        a.w[(size_t)t * a.k + lane] = w;
+    }
+}
+
+template <int PL>
+void launch_select(const SelectArgs &a, cudaStream_t s) {
+    route_select_kernel<PL><<<(a.T + 7) / 8, 256, 0, s>>>(a);
+}
+
+}  // namespace
+
+int route_kernel_count() { return 2; }
+
+int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate,
+                 const float *e_bias, const float *logit_offset, const int32_t *log2phys,
+                 float *logits, int32_t *topk_ids, float *topk_w, int32_t *status,
+                 cudaStream_t s) {
+    if (T == 0) return MOE_OK;
+    const int E = cfg->num_experts, H = cfg->hidden;
+    const int warps = (int)(ceil_div(T, kTB) * ceil_div(E, kEB));
+    gate_logits_kernel<<<(warps + kLogitWarps - 1) / kLogitWarps, kLogitWarps * 32, 0, s>>>(
+        static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(w_gate), logit_offset,
+        logits, T, E, H);
+    MOE_LAUNCH_CHECK();
+
+    SelectArgs a;
+    a.T = T;
+    a.E = E;
+    a.k = cfg->top_k;
+    a.groups = cfg->num_groups;
+    a.topk_groups = cfg->topk_groups;
+    a.topn = cfg->group_topn;
+    a.sigmoid = cfg->scoring == MOE_SCORING_SIGMOID;
+    a.norm = cfg->norm_topk;
+    a.scaling = cfg->routed_scaling;
+    a.logits = logits;
+    a.bias = e_bias;
+    a.log2phys = log2phys;
+    a.ids = topk_ids;
+    a.w = topk_w;
+    a.status = status;
+    const int pl = (int)ceil_div(E, 32);
+    if (pl <= 1) launch_select<1>(a, s);
+    else if (pl <= 2) launch_select<2>(a, s);
+    else if (pl <= 4) launch_select<4>(a, s);
+    else if (pl <= 8) launch_select<8>(a, s);
+    else if (pl <= 16) launch_select<16>(a, s);
+    else launch_select<32>(a, s);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -92,7 +92,7 @@ CONFIGS = {
                              norm_topk=True, routed_scaling=2.5, dtype="fp8",
                              bias_std=0.01, zipf_s=1.0, balanced_perm=True,
                              num_sets=4),
-    "bf16_mini": MoEShape("bf16_mini", tokens=29, hidden=512, inter=192,
+    "bf16_mini": MoEShape("bf16_mini", tokens=29, hidden=512, inter=384,
                           num_experts=8, num_shared=2, top_k=3,
                           scoring="softmax", norm_topk=True),
     # R1 hidden/intermediate sizes with 32 experts: a few GB on the device,

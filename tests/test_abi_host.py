@@ -1,0 +1,153 @@
+"""The C-ABI library on the host (no GPU needed): it loads, exports every
+function include/moe_gb300.h declares, rejects bad arguments before any
+launch, and its host-only balanced permutation matches the oracle."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import moe_expert_layer_07_gb300 as moe
+import synth
+from oracle import balance
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_gb300.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from moe_expert_layer_07_gb300 import _build
+    _build.build()
+    return moe.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    names = re.findall(r"\b([a-z_][a-z0-9_]*)\s*\(", text)
+    return sorted({n for n in names if n.startswith(("moe_", "expert_")) and n != "moe_config"})
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = declared_functions()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in the header but not exported"
+
+
+def test_status_strings(L):
+    assert moe.status_string(0) == "ok"
+    for code in (-1, -2, -3, -4, -5, -6):
+        assert moe.status_string(code) not in ("ok", "unknown status")
+    assert moe.status_string(-99) == "unknown status"
+
+
+def test_workspace_size_r1_decode(L):
+    shape = synth.CONFIGS["r1_decode_t128"]
+    cfg = moe.make_config(shape)
+    n = moe.workspace_size(cfg)
+    lay = moe.workspace_layout(cfg)
+    assert lay.total == n and lay.status == 0
+    rows = 128 * 9
+    # the largest buffers: fp32 gate/up [rows, 4096], bf16 y [rows, 7168], fp8 xp [rows, 7168]
+    floor = rows * 4096 * 4 + rows * 7168 * 2 + rows * 7168
+    assert floor < n < floor * 1.2
+    offs = [lay.status, lay.logits, lay.topk_ids, lay.topk_w, lay.xq, lay.xs, lay.expert_offsets,
+            lay.src_of_row, lay.row_of_slot, lay.perm_scratch, lay.xp, lay.xp_scales, lay.gate_up,
+            lay.h, lay.h_scales, lay.y]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+
+
+def test_bad_arguments_are_rejected_before_launch(L):
+    shape = synth.CONFIGS["r1_mini"]
+    cfg = moe.make_config(shape)
+    P = ctypes.c_void_p
+    fake = P(0x1000)   # never dereferenced: every call below fails validation first
+    # null pointers
+    assert L.moe_route(ctypes.byref(cfg), 4, None, fake, None, None, None, fake, fake, fake,
+                       None, None) == -1
+    # misaligned activation pointer
+    assert L.moe_route(ctypes.byref(cfg), 4, P(0x1001), fake, None, None, None, fake, fake, fake,
+                       None, None) == -1
+    # shapes the kernels do not handle
+    bad = moe.make_config(shape)
+    bad.hidden = 1000
+    assert L.moe_route(ctypes.byref(bad), 4, fake, fake, None, None, None, fake, fake, fake,
+                       None, None) == -2
+    assert L.moe_grouped_gemm(ctypes.byref(cfg), 3, 200, 128, 10, fake, fake, fake, fake, fake,
+                              fake, 0, None, None) == -2
+    assert L.moe_grouped_gemm(ctypes.byref(cfg), 2000, 128, 128, 10, fake, fake, fake, fake,
+                              fake, fake, 0, None, None) == -2
+    # workspace too small
+    need = moe.permute_workspace_size(cfg, 37)
+    assert L.moe_permute(ctypes.byref(cfg), 37, fake, fake, fake, fake, fake, fake, fake, fake,
+                         fake, need - 1, None, None) == -3
+    # identity quantisation needs an FP8 layer; unknown enums
+    b16 = moe.make_config(synth.CONFIGS["bf16_mini"])
+    assert L.moe_act_requant(ctypes.byref(b16), moe.ACT_IDENTITY, 4, None, fake, fake, fake,
+                             None) == -1
+    assert L.moe_act_requant(ctypes.byref(cfg), 7, 4, None, fake, fake, fake, None) == -1
+    # softmax takes no selection bias
+    assert L.moe_route(ctypes.byref(b16), 4, fake, fake, fake, None, None, fake, fake, fake,
+                       None, None) == -1
+    # group-limited routing that cannot supply k candidates
+    g = moe.make_config(shape)
+    g.topk_groups = 1
+    g.top_k = 8   # 1 group of 4 experts
+    assert L.moe_route(ctypes.byref(g), 4, fake, fake, None, None, None, fake, fake, fake,
+                       None, None) == -1
+    # T beyond max_tokens
+    w = moe.Weights(w_gate=0x1000, w13=0x1000, w2=0x1000, w13_scales=0x1000, w2_scales=0x1000)
+    assert L.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 38, fake, fake, 0, fake,
+                               1 << 40, None) == -1
+    assert L.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 4, fake, fake, 0, fake,
+                               16, None) == -3
+    # zero tokens enqueue nothing and succeed
+    assert L.moe_route(ctypes.byref(cfg), 0, None, None, None, None, None, None, None, None,
+                       None, None) == 0
+    assert L.moe_combine(ctypes.byref(cfg), 0, None, None, None, None, None, 0, None) == 0
+
+
+@pytest.mark.parametrize("E,S", [(4, 2), (6, 3), (8, 2), (8, 4), (12, 3), (12, 4), (12, 6)])
+def test_balance_is_optimal_on_tiny_counts(L, E, S):
+    rng = np.random.default_rng(E * 7 + S)
+    for trial in range(4):
+        counts = rng.integers(0, 100, size=E)
+        if trial == 0:
+            counts = np.sort(counts)[::-1].copy()
+        l2p, p2l, mom = moe.balance_permutation(counts, S)
+        assert sorted(l2p.tolist()) == list(range(E))
+        assert np.array_equal(p2l[l2p], np.arange(E))
+        loads = balance.set_loads(counts, l2p, S)
+        assert loads.max() == balance.optimum_max_load(counts.tolist(), S)
+        assert abs(mom - balance.imbalance(loads)) < 1e-12
+        m = E // S
+        for s in range(S):   # logical ids ascend inside a set
+            members = p2l[s * m:(s + 1) * m]
+            assert list(members) == sorted(members)
+
+
+@pytest.mark.parametrize("skew", [0.5, 1.0, 1.2])
+def test_balance_on_skewed_large_counts_reaches_lower_bound(L, skew):
+    rng = np.random.default_rng(11)
+    counts = (1e4 / np.arange(1, 257) ** skew).astype(np.int64)[rng.permutation(256)]
+    l2p, p2l, mom = moe.balance_permutation(counts, 8)
+    loads = balance.set_loads(counts, l2p, 8)
+    # no partition beats the mean, nor the heaviest expert with the 31 lightest others
+    srt = np.sort(counts)
+    lower = max(int(np.ceil(counts.sum() / 8)), int(counts.max() + srt[:31].sum()))
+    assert lower <= loads.max() <= 1.01 * lower
+    assert mom <= balance.imbalance(balance.contiguous_loads(counts, 8))
+
+
+def test_balance_rejects_bad_arguments(L):
+    c = np.ones(10, np.int64)
+    out = np.empty(10, np.int32)
+    assert L.expert_balance_permutation(c.ctypes.data, 10, 3, out.ctypes.data, out.ctypes.data,
+                                        None) == -1
+    c[2] = -1
+    assert L.expert_balance_permutation(c.ctypes.data, 10, 5, out.ctypes.data, out.ctypes.data,
+                                        None) == -1

@@ -1,0 +1,451 @@
+"""GPU parity: every step of the hot path and the whole layer against the CPU
+oracle, through the C ABI, on seeded inputs of the workloads' shapes.
+
+Sizes: the small R1- and BF16-shaped layers run in full against the oracle
+(several tiles in every dimension, ragged tails); the full-size R1 layers
+(128, 1024 and 4096 tokens) are checked bit for bit on routing and dispatch
+for every token and on the layer output for a seeded sample of tokens, in
+the same launch configuration the benchmark times.  Tolerances are stated
+in tests/_gpu_common.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import moe_expert_layer_07_gb300 as moe
+import synth
+from oracle import layer as olayer
+from oracle import permute as opermute
+from oracle import quant as oquant
+from oracle import routing as orouting
+
+from _gpu_common import (BF16_TOL, FP8_TOL, W_RTOL, Workload, build_library, check_close,
+                         fp8_codes_equal, oracle_layer, rms, to_np)
+
+pytestmark = pytest.mark.gpu
+
+SMALL = ["tiny_bf16", "v2lite_bf16", "r1_mini", "r1_mini_zipf", "bf16_mini"]
+FULL = ["r1_decode_t128", "r1_zipf_t1024", "r1_prefill_t4096"]
+SAMPLE = {"r1_decode_t128": 16, "r1_zipf_t1024": 16, "r1_prefill_t4096": 16}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    return build_library()
+
+
+_cache = {}
+
+
+def workload(name, seed=0, perm=None, T=None):
+    key = (name, seed, perm, T)
+    if key not in _cache:
+        if any(k[0] in FULL for k in _cache) and name in FULL:
+            for k in [k for k in _cache if k[0] in FULL]:
+                del _cache[k]          # one full-size layer resident at a time
+            torch.cuda.empty_cache()
+        shape = synth.CONFIGS[name]
+        if T is not None:
+            shape = shape.with_tokens(T)
+        _cache[key] = Workload(shape, seed=seed, perm=perm)
+    return _cache[key]
+
+
+def run_route(wl, T=None):
+    s = wl.shape
+    T = s.tokens if T is None else T
+    dev = wl.dev
+    logits = torch.full((T, s.num_experts), float("nan"), device="cuda")
+    ids = torch.full((T, s.top_k), -7, dtype=torch.int32, device="cuda")
+    w = torch.full((T, s.top_k), float("nan"), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    l2p = None if wl.log2phys is None else torch.as_tensor(wl.log2phys, device="cuda")
+    moe.route(moe.make_config(s), T, dev["x"], dev["wg"], dev["e_bias"], dev["logit_offset"],
+              l2p, logits, ids, w, st)
+    torch.cuda.synchronize()
+    return to_np(logits), to_np(ids), to_np(w), int(st.item())
+
+
+# ------------------------------------------------------------------ routing
+@pytest.mark.parametrize("name", SMALL + FULL)
+def test_route_bit_exact(lib, name):
+    wl = workload(name)
+    logits, ids, w, st = run_route(wl)
+    n = wl.np
+    ref_l = orouting.gate_logits(n["x_bits"], n["wg_bits"], n["logit_offset"])
+    assert np.array_equal(logits.view(np.uint32), ref_l.view(np.uint32)), "logits differ"
+    phys, ref_w, _ = orouting.route(ref_l, wl.shape, n["e_bias"], n["log2phys"])
+    assert np.array_equal(ids, phys)
+    np.testing.assert_allclose(w, ref_w, rtol=W_RTOL, atol=0)
+    assert st == 0
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 33])
+def test_route_small_batches(lib, T):
+    wl = workload("r1_mini", seed=3, T=T)
+    logits, ids, w, st = run_route(wl)
+    n = wl.np
+    ref_l = orouting.gate_logits(n["x_bits"], n["wg_bits"], n["logit_offset"])
+    phys, ref_w, _ = orouting.route(ref_l, wl.shape, n["e_bias"], None)
+    assert np.array_equal(ids, phys) and st == 0
+    np.testing.assert_allclose(w, ref_w, rtol=W_RTOL, atol=0)
+
+
+def test_route_with_random_permutation(lib):
+    wl = workload("r1_mini", seed=5, perm="random")
+    _, ids, w, _ = run_route(wl)
+    n = wl.np
+    ref_l = orouting.gate_logits(n["x_bits"], n["wg_bits"], n["logit_offset"])
+    phys, ref_w, logical = orouting.route(ref_l, wl.shape, n["e_bias"], n["log2phys"])
+    assert np.array_equal(ids, phys) and np.array_equal(ids, wl.log2phys[logical])
+
+
+# ------------------------------------------------------------ quantisation
+def _quant_x(cfg, x, T, H):
+    q = torch.empty((T, H), dtype=torch.uint8, device="cuda")
+    s = torch.empty((T, H // 128), dtype=torch.float32, device="cuda")
+    moe.act_requant(cfg, moe.ACT_IDENTITY, T, x, q, s)
+    torch.cuda.synchronize()
+    return to_np(q), to_np(s)
+
+
+@pytest.mark.parametrize("name", ["r1_mini", "r1_decode_t128"])
+def test_quant_x_bit_exact(lib, name):
+    wl = workload(name)
+    s = wl.shape
+    q, sc = _quant_x(moe.make_config(s), wl.dev["x"], s.tokens, s.hidden)
+    rq, rs = oquant.quant_groups_fp8(oquant.bf16_from_bits(wl.np["x_bits"]))
+    assert fp8_codes_equal(q, rq) and np.array_equal(sc, rs)
+
+
+def test_quant_x_ties_zeros_and_extremes(lib):
+    s = synth.CONFIGS["r1_mini"]
+    H = s.hidden
+    x = torch.randn(6, H, device="cuda").to(torch.bfloat16)
+    x[0] = 0                                       # all-zero row: scale 1, codes 0
+    x[1, :128] = 0.53125                           # midpoints of the e4m3 grid ...
+    x[1, 1::2] = -3.125
+    x[1, 0] = 448.0                                # ... with scale exactly 1
+    x[2] *= 1e-30                                  # tiny magnitudes
+    x[3] *= 1e30                                   # huge magnitudes
+    x[4, 128:256] = 0
+    q, sc = _quant_x(moe.make_config(s), x, 6, H)
+    bits = x.view(torch.int16).cpu().numpy().view(np.uint16)
+    rq, rs = oquant.quant_groups_fp8(oquant.bf16_from_bits(bits))
+    assert fp8_codes_equal(q, rq) and np.array_equal(sc, rs)
+    assert sc[1, 0] == 1.0 and sc[0].tolist() == [1.0] * (H // 128)
+
+
+@pytest.mark.parametrize("fp8", [True, False])
+def test_silu_mul_requant(lib, fp8):
+    s = synth.CONFIGS["r1_mini" if fp8 else "bf16_mini"]
+    cfg = moe.make_config(s)
+    rows, I = 37, s.inter
+    g = (torch.randn(rows, 2 * I, device="cuda") * 3).contiguous()
+    g[5] = 0                                        # a zero row
+    rows_dev = torch.tensor([30], dtype=torch.int32, device="cuda")
+    if fp8:
+        out = torch.full((rows, I), 0x55, dtype=torch.uint8, device="cuda")
+        sc = torch.full((rows, I // 128), -1.0, device="cuda")
+    else:
+        out = torch.zeros((rows, I), dtype=torch.bfloat16, device="cuda")
+        sc = None
+    moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, g, out, sc, rows_dev=rows_dev)
+    torch.cuda.synchronize()
+    h = olayer.silu_mul(to_np(g)[:30])
+    if fp8:
+        rq, rs = oquant.quant_groups_fp8(h.astype(np.float32))
+        q = to_np(out)
+        gs = to_np(sc)
+        np.testing.assert_allclose(gs[:30], rs, rtol=1e-6, atol=0)
+        deq = oquant.dequant_groups_fp8(q[:30], gs[:30])
+        ref = oquant.dequant_groups_fp8(rq, rs)
+        diff = ~np.isclose(deq, ref, rtol=0, atol=0)
+        # a code may differ only where fp32 silu rounding straddles a midpoint:
+        # by one e4m3 step, rarely
+        assert diff.mean() < 1e-3
+        step = np.maximum(np.abs(ref) * 2.0 ** -3, np.repeat(rs, 128, axis=1) * 2.0 ** -9)
+        assert np.all(np.abs(deq - ref)[diff] <= step[diff] * 1.0001)
+        assert np.all(q[30:] == 0x55) and np.all(gs[30:] == -1.0)
+    else:
+        hb = to_np(out.float())
+        ref = oquant.bf16_round(h)
+        assert np.all(np.abs(hb[:30] - ref) <= np.abs(ref) * 2.0 ** -8)
+        assert np.all(hb[30:] == 0)
+
+
+# ------------------------------------------------------------------ permute
+def run_permute(cfg, s, ids_t, x_rows, x_scales):
+    T, k, E, S, H = ids_t.shape[0], s.top_k, s.num_experts, s.num_shared, s.hidden
+    rows = T * (k + S)
+    fp8 = s.dtype == "fp8"
+    off = torch.full((E + S + 1,), -5, dtype=torch.int32, device="cuda")
+    src = torch.full((rows,), -5, dtype=torch.int32, device="cuda")
+    ros = torch.full((T, k), -5, dtype=torch.int32, device="cuda")
+    xp = torch.zeros((rows, H), dtype=torch.uint8 if fp8 else torch.bfloat16, device="cuda")
+    xps = torch.zeros((rows, H // 128), device="cuda") if fp8 else None
+    nws = moe.permute_workspace_size(cfg, T)
+    ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.permute(cfg, T, ids_t, x_rows, x_scales, off, src, ros, xp, xps, ws, nws, st)
+    torch.cuda.synchronize()
+    return dict(off=to_np(off), src=to_np(src), ros=to_np(ros), xp=xp, xps=xps,
+                status=int(st.item()))
+
+
+@pytest.mark.parametrize("name", ["r1_mini", "bf16_mini", "v2lite_bf16", "r1_decode_t128",
+                                  "r1_prefill_t4096"])
+def test_permute_bit_exact(lib, name):
+    wl = workload(name)
+    s = wl.shape
+    cfg = moe.make_config(s)
+    _, ids, _, _ = run_route(wl)
+    ids_t = torch.as_tensor(ids, device="cuda")
+    if s.dtype == "fp8":
+        xq = torch.empty((s.tokens, s.hidden), dtype=torch.uint8, device="cuda")
+        xs = torch.empty((s.tokens, s.hidden // 128), device="cuda")
+        moe.act_requant(cfg, moe.ACT_IDENTITY, s.tokens, wl.dev["x"], xq, xs)
+        rows_src, rows_sc = xq, xs
+    else:
+        rows_src, rows_sc = wl.dev["x"], None
+    r = run_permute(cfg, s, ids_t, rows_src, rows_sc)
+    off, src, ros = opermute.permute(ids, s.num_experts, s.num_shared)
+    assert np.array_equal(r["off"], off)
+    assert np.array_equal(r["src"], src)
+    assert np.array_equal(r["ros"], ros)
+    tok = opermute.token_of_slot(src, s.tokens, s.top_k)
+    assert torch.equal(r["xp"], rows_src[torch.as_tensor(tok, device="cuda")])
+    if rows_sc is not None:
+        assert torch.equal(r["xps"], rows_sc[torch.as_tensor(tok, device="cuda")])
+    assert r["status"] == 0
+
+
+def test_permute_edge_cases(lib):
+    s = synth.CONFIGS["bf16_mini"]
+    cfg = moe.make_config(s)
+    T, k, E = 40, s.top_k, s.num_experts
+    x = torch.randn(T, s.hidden, device="cuda").to(torch.bfloat16)
+    # every token to the same experts (others empty); then invalid ids
+    ids = np.tile(np.array([3, 0, 6], np.int32), (T, 1))
+    r = run_permute(cfg, s, torch.as_tensor(ids, device="cuda"), x, None)
+    off, src, ros = opermute.permute(ids, E, s.num_shared)
+    assert np.array_equal(r["off"], off) and np.array_equal(r["ros"], ros)
+    assert np.array_equal(r["src"], src) and r["status"] == 0
+    bad = ids.copy()
+    bad[7, 1] = -1
+    bad[9, 2] = E
+    r = run_permute(cfg, s, torch.as_tensor(bad, device="cuda"), x, None)
+    assert r["status"] & moe.DEV_BAD_EXPERT_ID
+    assert r["ros"][7, 1] == -1 and r["ros"][9, 2] == -1
+    valid = np.ones_like(bad, bool)
+    valid[7, 1] = valid[9, 2] = False
+    counts = np.bincount(bad[valid], minlength=E)
+    assert np.array_equal(np.diff(r["off"])[:E], counts)
+
+
+# ------------------------------------------------------------- grouped GEMM
+GEMM_ROWS = [0, 1, 15, 16, 17, 0, 63, 64, 65, 129, 3]
+
+
+@pytest.mark.parametrize("fp8,N,K,out_bf16", [(True, 256, 384, False), (True, 384, 1024, True),
+                                              (False, 256, 320, False), (False, 128, 512, True)])
+def test_grouped_gemm(lib, fp8, N, K, out_bf16):
+    s = synth.CONFIGS["r1_mini" if fp8 else "bf16_mini"]
+    cfg = moe.make_config(s)
+    counts = np.array(GEMM_ROWS)
+    G = len(counts)
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(off[-1]) + 5                      # 5 trailing rows outside every group
+    g = torch.Generator(device="cuda").manual_seed(7)
+    a32 = torch.randn(rows, K, device="cuda", generator=g)
+    w32 = torch.randn(G, N, K, device="cuda", generator=g) * 0.05
+    if fp8:
+        a = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+        asc = torch.empty((rows, K // 128), device="cuda")
+        cfg_q = moe.make_config(synth.MoEShape("q", rows, K, 128, 1, 0, 1, dtype="fp8"))
+        moe.act_requant(cfg_q, moe.ACT_IDENTITY, rows, a32.to(torch.bfloat16), a, asc)
+        w, wsc = synth.block_quantize_e4m3(w32)
+    else:
+        a, asc = a32.to(torch.bfloat16), None
+        w, wsc = w32.to(torch.bfloat16), None
+    c = torch.full((rows, N), float("nan"), device="cuda",
+                   dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.grouped_gemm(cfg, G, N, K, rows, a, asc, torch.as_tensor(off, device="cuda"), w, wsc, c,
+                     moe.OUT_BF16 if out_bf16 else moe.OUT_F32, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    if fp8:
+        ref = olayer.grouped_gemm(s, off, to_np(a), to_np(w), to_np(asc), to_np(wsc))
+    else:
+        ref = olayer.grouped_gemm(s, off, to_np(a.view(torch.int16)).view(np.uint16),
+                                  to_np(w.view(torch.int16)).view(np.uint16))
+    got = to_np(c.float())
+    inside = off[-1]
+    check_close(got[:inside], ref[:inside], 1e-3 if not out_bf16 else 1e-4, bf16_out=out_bf16)
+    assert np.all(np.isnan(got[inside:]))
+
+
+def test_grouped_gemm_rejects_inconsistent_offsets(lib):
+    s = synth.CONFIGS["r1_mini"]
+    cfg = moe.make_config(s)
+    K, N, rows = 128, 128, 32
+    a = torch.zeros((rows, K), dtype=torch.uint8, device="cuda")
+    asc = torch.ones((rows, 1), device="cuda")
+    w = torch.zeros((2, N, K), dtype=torch.uint8, device="cuda")
+    wsc = torch.ones((2, 1, 1), device="cuda")
+    c = torch.full((rows, N), 3.0, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    off = torch.tensor([0, 20, 10], dtype=torch.int32, device="cuda")   # decreasing
+    moe.grouped_gemm(cfg, 2, N, K, rows, a, asc, off, w, wsc, c, moe.OUT_F32, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & moe.DEV_BAD_OFFSETS
+    assert torch.all(c == 3.0)                  # nothing was written
+
+
+# ------------------------------------------------------------------ combine
+@pytest.mark.parametrize("out_bf16", [False, True])
+def test_combine(lib, out_bf16):
+    s = synth.CONFIGS["v2lite_bf16"]
+    cfg = moe.make_config(s)
+    T, k, E, S, H = 50, s.top_k, s.num_experts, s.num_shared, s.hidden
+    rng = np.random.default_rng(3)
+    ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
+    off, src, ros = opermute.permute(ids, E, S)
+    rows = int(off[-1])
+    y = torch.randn(rows, H, device="cuda").to(torch.bfloat16)
+    w = torch.rand(T, k, device="cuda")
+    out = torch.empty((T, H), device="cuda", dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    moe.combine(cfg, T, y, torch.as_tensor(ros, device="cuda"), w,
+                torch.as_tensor(off, device="cuda"), out, moe.OUT_BF16 if out_bf16 else moe.OUT_F32)
+    torch.cuda.synchronize()
+    ref = olayer.combine(to_np(y.float()), ros, to_np(w), off, E, S)
+    check_close(to_np(out.float()), ref, 1e-5, bf16_out=out_bf16)
+
+
+# ------------------------------------------------------------- whole layer
+def run_layer(wl, T=None, out_bf16=False, layer=None):
+    s = wl.shape
+    T = s.tokens if T is None else T
+    layer = layer or wl.layer()
+    out = torch.full((max(T, 1), s.hidden), float("nan"), device="cuda",
+                     dtype=torch.bfloat16 if out_bf16 else torch.float32)
+    layer.forward(wl.dev["x"][:T] if T else wl.dev["x"][:1], out,
+                  moe.OUT_BF16 if out_bf16 else moe.OUT_F32, T=T)
+    torch.cuda.synchronize()
+    return layer, out
+
+
+def _check_layer_routing(layer, s, ref):
+    T, k, E, S = s.tokens, s.top_k, s.num_experts, s.num_shared
+    ids = to_np(layer.view("topk_ids", torch.int32, (T, k)))
+    off = to_np(layer.view("expert_offsets", torch.int32, (E + S + 1,)))
+    assert np.array_equal(ids, ref["topk_ids"])
+    assert np.array_equal(off, ref["expert_offsets"])
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_layer_parity_small(lib, name):
+    wl = workload(name)
+    s = wl.shape
+    layer, out = run_layer(wl)
+    ref = oracle_layer(wl)
+    _check_layer_routing(layer, s, ref)
+    tol = FP8_TOL if s.dtype == "fp8" else BF16_TOL
+    rel = check_close(to_np(out), ref["out"], tol)
+    assert layer.status() == 0
+    print(f"{name}: max|gpu-oracle|/rms = {rel:.2e}")
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_layer_parity_full_size(lib, name):
+    wl = workload(name)
+    s = wl.shape
+    layer, out = run_layer(wl)
+    rng = np.random.default_rng(1234)
+    tokens = np.sort(rng.choice(s.tokens, SAMPLE[name], replace=False))
+    ref = oracle_layer(wl, tokens=tokens)
+    _check_layer_routing(layer, s, ref)
+    rel = check_close(to_np(out)[tokens], ref["out"], FP8_TOL)
+    assert layer.status() == 0
+    print(f"{name}: max|gpu-oracle|/rms over {len(tokens)} tokens = {rel:.2e}")
+    if s.balanced_perm:
+        assert wl.imbalance <= wl.naive_imbalance
+        print(f"{name}: set imbalance balanced {wl.imbalance:.4f}, contiguous {wl.naive_imbalance:.4f}")
+
+
+def test_layer_bf16_output_and_partial_batch(lib):
+    wl = workload("r1_mini")
+    s = wl.shape
+    layer = wl.layer()
+    _, out = run_layer(wl, out_bf16=True, layer=layer)
+    ref = oracle_layer(wl)
+    check_close(to_np(out.float()), ref["out"], FP8_TOL, bf16_out=True)
+    # T below max_tokens reuses the same workspace
+    T = 20
+    _, out2 = run_layer(wl, T=T, layer=layer)
+    ref20 = olayer.layer_forward(s.with_tokens(T), {**wl.np, "x_bits": wl.np["x_bits"][:T]})
+    check_close(to_np(out2)[:T], ref20["out"], FP8_TOL)
+
+
+def test_layer_single_token_and_empty(lib):
+    wl = workload("r1_mini", seed=2, T=1)
+    _, out = run_layer(wl)
+    check_close(to_np(out), oracle_layer(wl)["out"], FP8_TOL)
+    layer = wl.layer()
+    out = torch.full((1, wl.shape.hidden), 5.0, device="cuda")
+    layer.forward(wl.dev["x"], out, T=0)
+    torch.cuda.synchronize()
+    assert torch.all(out == 5.0) and layer.status() == 0
+
+
+def test_layer_all_tokens_on_few_experts(lib):
+    # a large bias on experts 0..7 sends every token to them (several N tiles
+    # per expert, a ragged last tile); the other experts receive no rows
+    shape = synth.CONFIGS["r1_mini"].with_tokens(130)
+    wl = Workload(shape, seed=4)
+    wl.dev["e_bias"] = wl.dev["e_bias"].clone()
+    wl.dev["e_bias"][:8] += 10.0
+    wl._np = None
+    layer, out = run_layer(wl)
+    ref = oracle_layer(wl)
+    assert set(np.unique(ref["topk_ids"]).tolist()) == set(range(8))
+    _check_layer_routing(layer, shape, ref)
+    check_close(to_np(out), ref["out"], FP8_TOL)
+
+
+def test_layer_deterministic_and_graph_capturable(lib):
+    wl = workload("r1_mini")
+    layer, out1 = run_layer(wl)
+    _, out2 = run_layer(wl, layer=layer)
+    assert torch.equal(out1, out2)
+    out3 = torch.zeros_like(out1)
+    x = wl.dev["x"]
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x, out3)                  # warm-up outside capture
+    torch.cuda.current_stream().wait_stream(s)
+    graph = torch.cuda.CUDAGraph()
+    out3.zero_()
+    with torch.cuda.graph(graph):
+        layer.forward(x, out3)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out1, out3)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(lib):
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    res = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = moe.lib().moe_selftest_bounded_wait(st.data_ptr(), 2_000_000, res.data_ptr(),
+                                             torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(res.item()) == 3 and int(st.item()) & moe.DEV_TIMEOUT
+    # the context is still usable
+    wl = workload("bf16_mini")
+    _, out = run_layer(wl)
+    check_close(to_np(out), oracle_layer(wl)["out"], BF16_TOL)
