@@ -162,7 +162,9 @@ def test_silu_mul_requant(lib, fp8):
         np.testing.assert_allclose(gs[:30], rs, rtol=1e-6, atol=0)
         deq = oquant.dequant_groups_fp8(q[:30], gs[:30])
         ref = oquant.dequant_groups_fp8(rq, rs)
-        diff = ~np.isclose(deq, ref, rtol=0, atol=0)
+        qn = np.where(q[:30] == 0x80, 0, q[:30])
+        rn = np.where(rq == 0x80, 0, rq)
+        diff = qn != rn
         # a code may differ only where fp32 silu rounding straddles a midpoint:
         # by one e4m3 step, rarely
         assert diff.mean() < 1e-3
