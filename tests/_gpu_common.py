@@ -88,8 +88,10 @@ def check_close(gpu, ref, tol, bf16_out=False):
     ref = np.asarray(ref, np.float64)
     r = rms(ref)
     bound = tol * r
-    if bf16_out:
-        bound = bound + np.abs(ref) * 2.0 ** -9
+    if bf16_out:   # plus half a bf16 unit in the last place of the value
+        a = np.abs(ref)
+        _, ex = np.frexp(np.where(a > 0, a, 1.0))
+        bound = bound + np.where(a > 0, np.ldexp(1.0, ex.astype(np.int64) - 1 - 8), 0.0)
     err = np.abs(gpu - ref)
     worst = float((err / np.maximum(bound, 1e-300)).max()) if err.size else 0.0
     assert np.all(err <= bound), f"max err {err.max():.3e} vs rms {r:.3e} (ratio {worst:.3f})"
