@@ -191,7 +191,7 @@ class Stepper:
                         p["h_scales"] if self.fp8 else None, rows_dev=p["expert_offsets"] + 4 * G)
         mark()
         moe.grouped_gemm(cfg, G, H, I, rows, p["h"], p["h_scales"] if self.fp8 else None,
-                         p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_BF16,
+                         p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_F32,
                          p["status"])
         mark()
         moe.combine(cfg, T, p["y"], p["row_of_slot"], p["topk_w"], p["expert_offsets"], self.out,
@@ -229,8 +229,8 @@ def algorithmic_bytes(shape, offsets):
     b["permute"] = 4 * T * k * 3 + rows * (H * eb + sc_h) * 2
     b["gemm_gate_up"] = active * w13 + rows * (H * eb + sc_h) + rows * 2 * I * 4
     b["silu_requant"] = rows * 2 * I * 4 + rows * (I * eb + sc_i)
-    b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 2
-    b["combine"] = T * (k + S) * H * 2 + 8 * T * k + T * H * 4
+    b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4
+    b["combine"] = T * (k + S) * H * 4 + 8 * T * k + T * H * 4
     flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)
     return b, active, flops
 

@@ -187,7 +187,8 @@ MOE_API int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_ou
  * out[t, :] = sum_s Y[expert_offsets[E+s] + t, :]
  *           + sum_j topk_w[t, j] * Y[row_of_slot[t, j], :]    (fp32, shared
  * first, then j ascending; slots with row -1 are skipped).
- *   y bf16 [R_tot, H]; out fp32 or bf16 [T, H] (out_dtype = MOE_OUT_*).
+ *   y fp32 [R_tot, H] (the experts' outputs); out fp32 or bf16 [T, H]
+ *   (out_dtype = MOE_OUT_*).
  * A gather per token: no atomics, no scatter (report, section "Overview":
  * the combine that brings expert outputs back to their tokens). */
 MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
@@ -196,7 +197,8 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
 
 /* ---- the whole layer -------------------------------------------------------------
  * route -> (FP8: quantise x) -> permute -> grouped GEMM gate/up ->
- * SiLU-mul (+ FP8 requantisation) -> grouped GEMM down -> combine, all on
+ * SiLU-mul (+ FP8 requantisation) -> grouped GEMM down (fp32 expert
+ * outputs) -> combine, all on
  * `stream`, all intermediates inside `ws` (size from moe_workspace_size for
  * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..
  * max_tokens.  The workspace's device status word is cleared at the start

@@ -74,7 +74,7 @@ int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
     L->gate_up = take(4 * Rt * 2 * I);
     L->h = take(Rt * I * (fp8 ? 1 : 2));
     L->h_scales = take(fp8 ? 4 * Rt * (I / 128) : 0);
-    L->y = take(2 * Rt * H);
+    L->y = take(4 * Rt * H);
     L->total = off;
     return MOE_OK;
 }
@@ -271,7 +271,7 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     if (rc) return rc;
     rc = launch_grouped_gemm(fp8, G, H, I, rows, base + L.h,
                              reinterpret_cast<const float *>(base + L.h_scales), offsets, w->w2,
-                             w->w2_scales, base + L.y, MOE_OUT_BF16, status, s);
+                             w->w2_scales, base + L.y, MOE_OUT_F32, status, s);
     if (rc) return rc;
     return launch_combine(cfg, T, base + L.y, ros, tw, offsets, out, out_dtype, s);
 }

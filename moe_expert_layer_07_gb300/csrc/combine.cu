@@ -5,7 +5,8 @@
 //
 //   out[t] = sum_s Y[expert_offsets[E+s] + t] + sum_j w[t,j] Y[row_of_slot[t,j]]
 //
-// A gather per token in fp32 (shared experts first, then j ascending):
+// Y holds each expert's fp32 output rows.  A gather per token in fp32
+// (shared experts first, then j ascending):
 // every output element is written once by one thread, no atomics.
 #include <cuda_bf16.h>
 
@@ -18,18 +19,9 @@ constexpr int kThreads = 128;
 constexpr int kMaxK = 16;
 constexpr int kMaxShared = 4;
 
-__device__ __forceinline__ void add8(float (&acc)[8], const uint4 &v, float w) {
-    const uint32_t u[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        acc[2 * q] = fmaf(w, __uint_as_float(u[q] << 16), acc[2 * q]);
-        acc[2 * q + 1] = fmaf(w, __uint_as_float(u[q] & 0xffff0000u), acc[2 * q + 1]);
-    }
-}
-
 // grid: (T, column blocks); each thread handles 8 consecutive columns
 __global__ void __launch_bounds__(kThreads)
-    combine_kernel(const uint16_t *__restrict__ y, const int32_t *__restrict__ row_of_slot,
+    combine_kernel(const float *__restrict__ y, const int32_t *__restrict__ row_of_slot,
                    const float *__restrict__ topk_w, const int32_t *__restrict__ offsets,
                    void *__restrict__ out, int out_bf16, int T, int H, int E, int S, int k) {
     __shared__ long rows[kMaxShared + kMaxK];
@@ -50,16 +42,16 @@ __global__ void __launch_bounds__(kThreads)
     for (int r = 0; r < S + k; ++r) {
         const long row = rows[r];
         if (row < 0) continue;
-        const uint4 val = __ldg(reinterpret_cast<const uint4 *>(y + row * H) + v);
+        const float4 *src = reinterpret_cast<const float4 *>(y + row * H) + 2 * v;
+        const float4 a = __ldg(src), b = __ldg(src + 1);
+        const float val[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
         if (r < S) {
-            const uint32_t u[4] = {val.x, val.y, val.z, val.w};
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(u[q] << 16));
-                acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(u[q] & 0xffff0000u));
-            }
+            for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], val[q]);
         } else {
-            add8(acc, val, wts[r]);
+            const float w = wts[r];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = fmaf(w, val[q], acc[q]);
         }
     }
     if (out_bf16) {
@@ -67,8 +59,8 @@ __global__ void __launch_bounds__(kThreads)
         uint32_t *p = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-            p[q] = *reinterpret_cast<uint32_t *>(&b);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
+            p[q] = *reinterpret_cast<uint32_t *>(&b2);
         }
         reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + (long)t * H)[v] = o;
     } else {
@@ -86,7 +78,7 @@ int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *r
     if (T == 0) return MOE_OK;
     const int H = cfg->hidden;
     dim3 grid(T, (unsigned)ceil_div(H / 8, kThreads));
-    combine_kernel<<<grid, kThreads, 0, s>>>(static_cast<const uint16_t *>(y), row_of_slot, topk_w,
+    combine_kernel<<<grid, kThreads, 0, s>>>(static_cast<const float *>(y), row_of_slot, topk_w,
                                              offsets, out, out_dtype == MOE_OUT_BF16, T, H,
                                              cfg->num_experts, cfg->num_shared, cfg->top_k);
     MOE_LAUNCH_CHECK();

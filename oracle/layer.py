@@ -18,8 +18,12 @@ Readings taken where the pages say nothing:
   * a model with n shared experts of width I has n shared groups;
   * quantisation points are part of the layer: in the FP8 layer x is
     quantised per token and 128-column group, h likewise (from its fp32
-    value, the precision the decision is taken in), and each expert output
-    y is rounded to bf16; in the BF16 layer h and y are rounded to bf16;
+    value, the precision the decision is taken in); in the BF16 layer h is
+    rounded to bf16 (the tensor-core operand format);
+  * an expert output y is not rounded: on one GPU it never crosses a link
+    (the all-to-all combine of the report's section "Compute-communication
+    overlap" is where a narrower wire format would apply), so it is summed
+    into the output at full precision;
   * everything else is exact: products and sums here are fp64.
 """
 from __future__ import annotations
@@ -75,7 +79,7 @@ def silu_mul(g: np.ndarray) -> np.ndarray:
 
 
 def expert_ffn(cfg, x_rows, w13, w2, w13_s=None, w2_s=None, x_scales=None):
-    """One expert's SwiGLU MLP on n rows; returns bf16-valued fp64 [n, H].
+    """One expert's SwiGLU MLP on n rows; returns fp64 [n, H].
 
     FP8 layer: x_rows are e4m3 codes [n, H] with x_scales [n, H/128], the
     weights e4m3 codes with 128x128 block scales.  BF16 layer: x_rows and
@@ -92,7 +96,7 @@ def expert_ffn(cfg, x_rows, w13, w2, w13_s=None, w2_s=None, x_scales=None):
         g = matmul_bf16(a, w13)
         h = bf16_round(silu_mul(g))
         y = matmul_bf16(h, _bits(w2))
-    return bf16_round(y)
+    return y
 
 
 def _bits(a):

@@ -317,7 +317,7 @@ def test_combine(lib, out_bf16):
     ids = rng.integers(0, E, size=(T, k)).astype(np.int32)
     off, src, ros = opermute.permute(ids, E, S)
     rows = int(off[-1])
-    y = torch.randn(rows, H, device="cuda").to(torch.bfloat16)
+    y = torch.randn(rows, H, device="cuda")
     w = torch.rand(T, k, device="cuda")
     out = torch.empty((T, H), device="cuda", dtype=torch.bfloat16 if out_bf16 else torch.float32)
     moe.combine(cfg, T, y, torch.as_tensor(ros, device="cuda"), w,

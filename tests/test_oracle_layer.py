@@ -48,7 +48,7 @@ def _torch_dense_ffn(x_bf16, w13, w2, fp8, w13_s=None, w2_s=None):
         gu = xd @ w13.to(torch.float64).T
         h = (torch.nn.functional.silu(gu[:, :I]) * gu[:, I:]).to(torch.bfloat16).to(torch.float64)
         y = h @ w2.to(torch.float64).T
-    return y.to(torch.bfloat16).to(torch.float64).numpy()
+    return y.numpy()
 
 
 @pytest.mark.parametrize("dtype", ["bf16", "fp8"])
@@ -60,10 +60,11 @@ def test_one_expert_layer_is_dense_ffn(oracle_lib, dtype):
     ref = _torch_dense_ffn(inp["x"], inp["w13"][0], inp["w2"][0], dtype == "fp8",
                            inp["w13_s"][0] if dtype == "fp8" else None,
                            inp["w2_s"][0] if dtype == "fp8" else None)
-    # the only difference left is where fp64 summation order flips a rounding
+    # what is left is fp64 summation order (and, in principle, a rounding
+    # decision of h flipped by it)
     err = np.abs(res["out"] - ref)
     rms = np.sqrt(np.mean(ref ** 2))
-    assert np.mean(err == 0) > 0.99 and err.max() <= 2e-2 * rms
+    assert err.max() <= 1e-9 * rms
 
 
 @pytest.mark.parametrize("name", ["r1_mini", "bf16_mini"])
@@ -93,7 +94,7 @@ def test_shared_experts_only_and_linearity(oracle_lib):
                  for s in range(cfg.num_shared))
     rms = np.sqrt(np.mean(shared ** 2))
     assert np.abs(res["out"] - shared).max() <= 1e-2 * rms
-    # doubling every W2 doubles each bf16 expert output exactly
+    # doubling every W2 doubles each expert output exactly
     doubled = dict(inp)
     doubled["w2"] = inp["w2"] * 2
     a = layer.layer_forward(cfg, synth.to_numpy(inp))["out"]
