@@ -155,6 +155,7 @@ class Stepper:
                    "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "gate_up",
                    "h", "h_scales", "y")}
         self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
+        ws[L.status:L.status + 4].zero_()   # the device status word starts clear
         self.k = {}
         self.events = []
 
