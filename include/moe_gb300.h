@@ -172,7 +172,8 @@ MOE_API int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_id
  * BF16: A bf16 [rows, K], W bf16 [groups, N, K], scales unused.
  * C: fp32 or bf16 (c_dtype = MOE_OUT_*) [rows, N]; rows outside every group
  *   are not written.  expert_offsets: device int32 [groups + 1].
- * N multiple of 128; K multiple of 128 (FP8) or 64 (BF16); groups <= 1024.
+ * N multiple of 128; K multiple of 128 and at most 8192 (FP8) or multiple
+ * of 64 (BF16); groups <= 1024.
  * Tensor cores (tcgen05, accumulators in tensor memory) fed by TMA; weight
  * rows sit on the MMA's M side and the few token rows of an expert on its
  * N side (the SGLang/H20 article, section "SwapAB GEMM": map the token

@@ -20,10 +20,12 @@
 //               row), then
 //                 FP8: per 128-wide K block, the block's partial product is
 //                 scaled by w_scale[g, m/128, kb] * a_scale[r, kb] and added
-//                 to fp32 registers (two TMEM buffers alternate so the next
-//                 block's MMAs run meanwhile);
-//                 BF16: one accumulation over all of K (two TMEM buffers
-//                 alternate between tiles);
+//                 to fp32 registers; four TMEM buffers rotate so the MMAs
+//                 of the next blocks run meanwhile, and the tile's scales
+//                 are copied to shared memory one tile ahead (cp.async,
+//                 completion on an mbarrier);
+//                 BF16: one accumulation over all of K (the four TMEM
+//                 buffers rotate between tiles);
 //               and stores C (coalesced: a warp writes 32 consecutive n).
 // Work units are (group, 128-row weight tile, BN-row activation tile); the
 // tile table is built on the device from expert_offsets, so no host sync is
@@ -46,6 +48,7 @@ constexpr int kBM = 128;
 constexpr int kMaxGroups = 1024;
 constexpr int kThreads = 192;
 constexpr int kBoxRows = 16;   // activation rows per TMA box
+constexpr int kMaxKBlocks = 64; // FP8: K <= 8192
 
 template <bool FP8, int BN, int STAGES>
 struct GemmShape {
@@ -53,11 +56,15 @@ struct GemmShape {
     static constexpr int kBBytes = BN * 128;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kSmemBytes = STAGES * kStageBytes + 1024;
-    static constexpr int kTmemCols = 2 * BN;
+    static constexpr int kAccBufs = 4;                   // TMEM accumulators in flight
+    static constexpr int kTmemCols = kAccBufs * BN;
     static constexpr int kKPerStage = FP8 ? 128 : 64;   // elements of K per stage
-    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 256, "BN");
-    static_assert((kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns must be a power of two");
-    static_assert(kSmemBytes <= 227 * 1024 - 9 * 1024, "shared memory");
+    static constexpr int kXsElems = FP8 ? BN * kMaxKBlocks : 1;
+    static constexpr int kWsElems = FP8 ? kMaxKBlocks : 1;
+    static_assert(BN % 16 == 0 && BN >= 32 && BN <= 64, "BN");
+    static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols <= 512, "TMEM columns");
+    static_assert(kSmemBytes + 8 * kXsElems + 8 * kWsElems + 8 * 1024 <= 227 * 1024,
+                  "shared memory");
 };
 
 struct GemmArgs {
@@ -99,16 +106,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmA, const GemmArgs args) {
     using S = GemmShape<FP8, BN, STAGES>;
+    constexpr int NB = S::kAccBufs;
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
-    __shared__ __align__(8) uint64_t acc_full[2];
-    __shared__ __align__(8) uint64_t acc_empty[2];
+    __shared__ __align__(8) uint64_t acc_full[NB];
+    __shared__ __align__(8) uint64_t acc_empty[NB];
+    __shared__ __align__(8) uint64_t scale_full[2];
+    __shared__ __align__(8) uint64_t scale_empty[2];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_abort, s_bad;
     __shared__ int s_off[kMaxGroups + 1];
     __shared__ int s_tiles[kMaxGroups + 1];
+    // FP8 scales of the tile being reduced (and of the next one): per K block
+    // the weight-block scale, and the activation scale of every row n laid
+    // out [kb][n] so that lanes read consecutive words.
+    __shared__ float s_ws[2][S::kWsElems];
+    __shared__ float s_xs[2][S::kXsElems];
 
     using namespace ptx;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -123,9 +138,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(smem_u32(&full_bar[s]), 1);
             mbar_init(smem_u32(&empty_bar[s]), 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NB; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
             mbar_init(smem_u32(&acc_empty[b]), 4);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&scale_full[b]), 128);   // every epilogue thread's copies
+            mbar_init(smem_u32(&scale_empty[b]), 4);    // every epilogue warp done reading
         }
         mbar_init(smem_u32(&drain_bar), 1);
         s_abort = 0;
@@ -231,16 +250,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
                 const int nmma = ((tl.nvalid + 15) / 16) * 16;
                 const uint32_t idesc = FP8 ? idesc_e4m3(kBM, nmma) : idesc_bf16(kBM, nmma);
-                if (!FP8) {
-                    if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
-                                      args.status, MOE_DEV_TIMEOUT)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                }
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (FP8) {
+                    if (FP8 || kb == 0) {   // FP8: one accumulator per K block
                         if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
                                           args.status, MOE_DEV_TIMEOUT)) {
                             ok = false;
@@ -265,21 +276,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         else mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, acc);
                     }
                     mma_commit(smem_u32(&empty_bar[stage]));
-                    if (FP8) {
+                    if (FP8 || kb == KB - 1) {
                         mma_commit(smem_u32(&acc_full[ab]));
-                        ab ^= 1;
-                        if (ab == 0) aphase ^= 1u;
+                        if (++ab == NB) {
+                            ab = 0;
+                            aphase ^= 1u;
+                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
-                }
-                if (!ok) break;
-                if (!FP8) {
-                    mma_commit(smem_u32(&acc_full[ab]));
-                    ab ^= 1;
-                    if (ab == 0) aphase ^= 1u;
                 }
             }
             // every MMA issued by this thread completes before teardown
@@ -290,38 +297,64 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------ epilogue (warps 2..5)
         const int q = warp & 3;                    // TMEM lanes [32q, 32q + 32)
+        const int etid = threadIdx.x - 64;         // 0..127
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         const int m_local = q * 32 + lane;
         int ab = 0;
         uint32_t aphase = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+
+        // FP8: copy the scales of tile t into buffer b (asynchronously); the
+        // buffer's scale_full barrier completes when all 128 threads' copies land.
+        auto stage_scales = [&](int t, int b) {
+            const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
+            const float *wsp = args.w_scales + ((size_t)tl.g * MT + tl.mt) * KB;
+            const float *xsp = args.a_scales + (size_t)tl.row0 * KB;
+            for (int i = etid; i < KB; i += 128) cp_async4(smem_u32(&s_ws[b][i]), wsp + i);
+            const int n_el = tl.nvalid * KB;
+            for (int i = etid; i < n_el; i += 128) {
+                const int n = i / KB, kb = i - n * KB;
+                cp_async4(smem_u32(&s_xs[b][kb * BN + n]), xsp + i);
+            }
+            cp_async_mbar_arrive(smem_u32(&scale_full[b]));
+        };
+        if (FP8 && (int)blockIdx.x < total_tiles) stage_scales(blockIdx.x, 0);
+
+        int it = 0;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x, ++it) {
             const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
             const int nchunks = (tl.nvalid + 15) / 16;
             const int m_glob = tl.mt * kBM + m_local;
             if (FP8) {
+                // tile iteration `it` reads buffer it&1 (its (it>>1)-th use);
+                // the next tile's scales go to the other buffer, whose previous
+                // use (iteration it-1) must have been released first
+                const int b = it & 1;
+                const int tn = t + (int)gridDim.x;
+                if (tn < total_tiles) {
+                    const uint32_t use = (uint32_t)(it + 1) >> 1;
+                    if (!wait_bounded(smem_u32(&scale_empty[b ^ 1]), (use & 1u) ^ 1u, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    stage_scales(tn, b ^ 1);
+                }
+                if (!wait_bounded(smem_u32(&scale_full[b]), ((uint32_t)it >> 1) & 1u, abort_flag,
+                                  args.status, MOE_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
                 float acc[BN];
 #pragma unroll
                 for (int n = 0; n < BN; ++n) acc[n] = 0.0f;
-                const float *wsp = args.w_scales + ((size_t)tl.g * MT + tl.mt) * KB;
-                const float *xsp = args.a_scales + (size_t)tl.row0 * KB;
-                float nsw = __ldg(wsp);
-                float nx[BN / 32];
-#pragma unroll
-                for (int h = 0; h < BN / 32; ++h)
-                    nx[h] = (h * 32 + lane < tl.nvalid) ? __ldg(xsp + (size_t)(h * 32 + lane) * KB) : 0.0f;
                 for (int kb = 0; kb < KB; ++kb) {
+                    const float sw = s_ws[b][kb];
                     float sx[BN / 32];
 #pragma unroll
-                    for (int h = 0; h < BN / 32; ++h) sx[h] = nx[h] * nsw;
-                    if (kb + 1 < KB) {   // next block's scales, while this block's MMAs run
-                        nsw = __ldg(wsp + kb + 1);
-#pragma unroll
-                        for (int h = 0; h < BN / 32; ++h)
-                            nx[h] = (h * 32 + lane < tl.nvalid)
-                                        ? __ldg(xsp + (size_t)(h * 32 + lane) * KB + kb + 1)
-                                        : 0.0f;
-                    }
+                    for (int h = 0; h < BN / 32; ++h)
+                        sx[h] = (h * 32 + lane < tl.nvalid) ? s_xs[b][kb * BN + h * 32 + lane] * sw
+                                                            : 0.0f;
                     if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
                                       MOE_DEV_TIMEOUT)) {
                         ok = false;
@@ -331,15 +364,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t v[BN / 16][16];
 #pragma unroll
                     for (int c = 0; c < BN / 16; ++c)
-                        if (c < nchunks) {
-                            tmem_ld16(lane_base + (uint32_t)(ab * BN + c * 16), v[c]);
-                            tmem_wait_ld(v[c]);
-                        }
+                        if (c < nchunks) tmem_ld16(lane_base + (uint32_t)(ab * BN + c * 16), v[c]);
+#pragma unroll
+                    for (int c = 0; c < BN / 16; ++c)
+                        if (c < nchunks) tmem_wait_ld(v[c]);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
-                    ab ^= 1;
-                    if (ab == 0) aphase ^= 1u;
+                    if (++ab == NB) {
+                        ab = 0;
+                        aphase ^= 1u;
+                    }
 #pragma unroll
                     for (int c = 0; c < BN / 16; ++c)
                         if (c < nchunks) {
@@ -352,6 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                 }
                 if (!ok) break;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&scale_empty[b]));
                 if (args.c_bf16) {
                     __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(args.c);
 #pragma unroll
@@ -393,10 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
-                ab ^= 1;
-                if (ab == 0) aphase ^= 1u;
+                if (++ab == NB) {
+                    ab = 0;
+                    aphase ^= 1u;
+                }
             }
         }
+        if (FP8) asm volatile("cp.async.wait_all;" ::: "memory");   // copies land before exit
     }
 
     tc_fence_before();
@@ -488,8 +528,8 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     args.c = c;
     args.c_bf16 = c_dtype == MOE_OUT_BF16;
     args.status = status;
-    if (fp8) return launch_impl<true, 64, 8>(args, a, w, s);
-    return launch_impl<false, 64, 8>(args, a, w, s);
+    if (fp8) return launch_impl<true, 64, 7>(args, a, w, s);
+    return launch_impl<false, 64, 7>(args, a, w, s);
 }
 
 }  // namespace moe

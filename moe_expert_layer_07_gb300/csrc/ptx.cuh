@@ -61,6 +61,7 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity,
         if ((it & 63u) == 0) {
             if (*abort_flag) return false;
             if (globaltimer() - t0 > limit_ns || it >= kWaitMaxPolls) {
+                if (mbar_try_wait(bar, parity)) return true;   // completed meanwhile
                 *abort_flag = 1;
                 if (status) atomicOr(status, timeout_bit);
                 return false;
@@ -76,6 +77,18 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
         if (globaltimer() - t0 > kWaitLimitNs || it >= kWaitMaxPolls) return false;
     }
     return true;
+}
+
+// ---- cp.async (4-byte global -> shared) ------------------------------------
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src))
+                 : "memory");
+}
+// The mbarrier receives one arrival once this thread's earlier cp.async
+// copies have landed (the arrival counts toward the barrier's init count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
 // ---- TMA -------------------------------------------------------------------

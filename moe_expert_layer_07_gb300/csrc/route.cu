@@ -68,22 +68,30 @@ __global__ void __launch_bounds__(kLogitWarps * 32)
 
     const int chunks = H / 8;
     const uint4 zero = make_uint4(0, 0, 0, 0);
-    for (int c = lane; c < chunks; c += 32) {
-        uint4 xv[kTB], wv[kEB];
+    uint4 xv[kTB], wv[kEB], xn[kTB], wn[kEB];
+    auto load = [&](int c, uint4 (&xd)[kTB], uint4 (&wd)[kEB]) {
 #pragma unroll
         for (int i = 0; i < kTB; ++i)
-            xv[i] = (t0 + i < T)
+            xd[i] = (c < chunks && t0 + i < T)
                         ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * H) + c)
                         : zero;
 #pragma unroll
         for (int j = 0; j < kEB; ++j)
-            wv[j] = (e0 + j < E)
+            wd[j] = (c < chunks && e0 + j < E)
                         ? __ldg(reinterpret_cast<const uint4 *>(wg + (size_t)(e0 + j) * H) + c)
                         : zero;
+    };
+    load(lane, xv, wv);
+    for (int c = lane; c < chunks; c += 32) {
+        load(c + 32, xn, wn);   // next chunk's loads overlap this chunk's FMAs
 #pragma unroll
         for (int i = 0; i < kTB; ++i)
 #pragma unroll
             for (int j = 0; j < kEB; ++j) acc[i][j] = dot8(xv[i], wv[j], acc[i][j]);
+#pragma unroll
+        for (int i = 0; i < kTB; ++i) xv[i] = xn[i];
+#pragma unroll
+        for (int j = 0; j < kEB; ++j) wv[j] = wn[j];
     }
 
     float mine = 0.0f;
@@ -123,10 +131,12 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i) {
     }
 }
 
+// One warp (one CTA) per token: the fp64 sigmoid runs on the SMs' narrow
+// FP64 pipes, so tokens are spread over as many SMs as possible.
 template <int PL>   // experts per lane: expert e = q*32 + lane, q < PL
-__global__ void __launch_bounds__(256) route_select_kernel(const SelectArgs a) {
+__global__ void __launch_bounds__(32) route_select_kernel(const SelectArgs a) {
     const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int t = blockIdx.x;
     if (t >= a.T) return;   // warp-uniform
     const float *lrow = a.logits + (size_t)t * a.E;
 
@@ -265,7 +275,7 @@ __global__ void __launch_bounds__(256) route_select_kernel(const SelectArgs a) {
 
 template <int PL>
 void launch_select(const SelectArgs &a, cudaStream_t s) {
-    route_select_kernel<PL><<<(a.T + 7) / 8, 256, 0, s>>>(a);
+    route_select_kernel<PL><<<a.T, 32, 0, s>>>(a);
 }
 
 }  // namespace
