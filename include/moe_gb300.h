@@ -162,6 +162,32 @@ MOE_API int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_id
                 void *xp, float *xp_scales, void *ws, size_t ws_bytes,
                 int32_t *dev_status, void *stream);
 
+/* moe_permute without a workspace argument.  The pages have no counterpart:
+ * this entry serves callers that cannot allocate device memory, such as a
+ * plugin inside a framework that owns every device allocation, or a
+ * runtime held to a fixed, pre-reserved memory budget.  Arguments and
+ * results are those of moe_permute minus ws/ws_bytes.
+ *   - Scratch lives in a static device array inside the library, 1 MiB per
+ *     device (moe_permute_static_scratch_capacity()), held by every GPU that
+ *     loads the library until the process exits.  A call whose scratch need
+ *     (moe_permute_workspace_size) exceeds it returns
+ *     MOE_ERR_UNSUPPORTED_SHAPE before enqueuing anything; for the R1
+ *     shape (256 experts, top 8) that is above 21824 tokens.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and leaves its contents
+ *     behind; nothing in it needs to start at zero (a call reads only words
+ *     it wrote earlier).  Calls that overlap on the GPU (other streams, or
+ *     concurrent graph branches) race on it: serialise them.
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call. */
+MOE_API int moe_permute_static_scratch(const moe_config *cfg, int32_t T, const int32_t *topk_ids,
+                                       const void *x_rows, const float *x_scales,
+                                       int32_t *expert_offsets, int32_t *src_of_row,
+                                       int32_t *row_of_slot, void *xp, float *xp_scales,
+                                       int32_t *dev_status, void *stream);
+MOE_API size_t moe_permute_static_scratch_capacity(void);
+
 /* ---- grouped GEMM -----------------------------------------------------------
  * For every group g and row r in [expert_offsets[g], expert_offsets[g+1]):
  *   C[r, n] = sum_k A[r, k] * W[g, n, k]

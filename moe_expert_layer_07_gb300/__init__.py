@@ -14,7 +14,7 @@ import os
 from ._build import LIB as LIB_PATH
 
 __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_requant",
-           "permute", "permute_workspace_size", "grouped_gemm", "combine", "layer_forward",
+           "permute", "permute_workspace_size", "permute_static_scratch", "grouped_gemm", "combine", "layer_forward",
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
            "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
            "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
@@ -72,6 +72,7 @@ _SIGS = {
     "moe_layer_kernel_count": [_CP, _I],
     "expert_balance_permutation": [_P, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_double)],
     "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
+    "moe_permute_static_scratch": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
 }
 
 
@@ -87,6 +88,8 @@ def lib():
             fn = getattr(L, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        L.moe_permute_static_scratch_capacity.argtypes = []
+        L.moe_permute_static_scratch_capacity.restype = ctypes.c_size_t
         L.moe_status_string.argtypes = [ctypes.c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -156,6 +159,17 @@ def permute(cfg: Config, T, topk_ids, x_rows, x_scales, expert_offsets, src_of_r
                              _ptr(expert_offsets), _ptr(src_of_row), _ptr(row_of_slot),
                              _ptr(xp), _ptr(xp_scales), _ptr(ws), ws_bytes, _ptr(status),
                              _stream(stream)), "moe_permute")
+
+
+def permute_static_scratch(cfg: Config, T, topk_ids, x_rows, x_scales, expert_offsets,
+                           src_of_row, row_of_slot, xp, xp_scales, status=None, stream=None):
+    """moe_permute with its scratch in the library's static device array, for
+    callers that cannot allocate device memory (limits: include/moe_gb300.h)."""
+    _check(lib().moe_permute_static_scratch(ctypes.byref(cfg), T, _ptr(topk_ids), _ptr(x_rows),
+                                            _ptr(x_scales), _ptr(expert_offsets),
+                                            _ptr(src_of_row), _ptr(row_of_slot), _ptr(xp),
+                                            _ptr(xp_scales), _ptr(status), _stream(stream)),
+           "moe_permute_static_scratch")
 
 
 def grouped_gemm(cfg: Config, groups, n_out, k_dim, rows, a, a_scales, expert_offsets, w,
