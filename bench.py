@@ -342,10 +342,11 @@ def main():
     achieved = bytes_per["gemm_gate_up"] / (gu_ms / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath):
+    if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168:
         with open(tpath) as f:
-            tr = json.load(f).get(args.workload, {}).get("gemm_gate_up")
-        traffic = tr if tr else None
+            tr = json.load(f).get("gemm_gate_up")
+        if tr:   # ncu DRAM bytes per active group (small R1 case) x this launch's groups
+            traffic = tr["bytes_per_active_group"] * active
 
     e2e = None
     if not args.no_e2e:
