@@ -143,7 +143,8 @@ def test_silu_mul_requant(lib, fp8):
     s = synth.CONFIGS["r1_mini" if fp8 else "bf16_mini"]
     cfg = moe.make_config(s)
     rows, I = 37, s.inter
-    g = (torch.randn(rows, 2 * I, device="cuda") * 3).contiguous()
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    g = (torch.randn(rows, 2 * I, device="cuda", generator=gen) * 3).contiguous()
     g[5] = 0                                        # a zero row
     rows_dev = torch.tensor([30], dtype=torch.int32, device="cuda")
     if fp8:
@@ -174,7 +175,14 @@ def test_silu_mul_requant(lib, fp8):
     else:
         hb = to_np(out.float())
         ref = oquant.bf16_round(h)
-        assert np.all(np.abs(hb[:30] - ref) <= np.abs(ref) * 2.0 ** -8)
+        # fp32 silu on the device against fp64 here: a value may round to the
+        # neighbouring bf16 (one unit in the last place), rarely
+        a = np.abs(ref)
+        _, ex = np.frexp(np.where(a > 0, a, 1.0))
+        ulp = np.where(a > 0, np.ldexp(1.0, ex.astype(np.int64) - 1 - 7), 0.0)
+        diff = hb[:30] != ref
+        assert diff.mean() < 1e-3
+        assert np.all(np.abs(hb[:30] - ref)[diff] <= ulp[diff])
         assert np.all(hb[30:] == 0)
 
 
