@@ -18,7 +18,7 @@ int check_config(const moe_config *c) {
         c->num_shared < 0 || c->max_tokens < 0 || c->num_groups <= 0)
         return MOE_ERR_INVALID_ARG;
     if (c->hidden % 128 || c->inter % 128) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (c->dtype == MOE_DTYPE_FP8_BLOCK128 && (c->hidden > 8192 || c->inter > 8192))
+    if (c->dtype == MOE_DTYPE_FP8_BLOCK128 && (c->hidden > 7168 || c->inter > 7168))
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if (c->num_experts > 1024 || c->num_shared > 4 || c->top_k > 16) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (c->num_groups > 32 || c->num_experts % c->num_groups) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -169,7 +169,7 @@ int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32
     if (c_dtype != MOE_OUT_F32 && c_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
     if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (n_out % 128 || k_dim % (fp8 ? 128 : 64)) return MOE_ERR_UNSUPPORTED_SHAPE;
-    if (fp8 && k_dim > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (fp8 && k_dim > 7168) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)groups * n_out > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return MOE_OK;
     if (!a || !w || !c || !expert_offsets || (fp8 && (!a_scales || !w_scales)))

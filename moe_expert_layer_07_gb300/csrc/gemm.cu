@@ -52,7 +52,7 @@ constexpr int kThreads = 192;
 // 5.5 -> 6.8 TB/s for the gate/up GEMM).
 constexpr int kCtasPerSm = 2;
 constexpr int kBoxRows = 16;   // activation rows per TMA box
-constexpr int kMaxKBlocks = 64; // FP8: K <= 8192
+constexpr int kMaxKBlocks = 56; // FP8: K <= 7168
 
 template <bool FP8, int BN, int STAGES>
 struct GemmShape {
@@ -207,8 +207,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (warp == 0) {
         // ------------------------------ TMA producer
         if (lane == 0) {
-            const uint64_t pol_w = policy_evict_first();   // weights: read once
-            const uint64_t pol_a = policy_evict_last();    // activations: re-read
+            // A weight tile is read once unless its group spans several N
+            // tiles: those run on neighbouring CTAs at about the same time and
+            // share the L2 copy.  Activation rows are re-read by every weight
+            // tile of their group.
+            const uint64_t pol_w_once = policy_evict_first();
+            const uint64_t pol_w_shared = policy_evict_normal();
+            const uint64_t pol_a = policy_evict_last();
             int stage = 0;
             uint32_t phase = 0, issued = 0, parity_bits = 0;
             bool ok = true;
@@ -217,6 +222,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int nbox = (tl.nvalid + kBoxRows - 1) / kBoxRows;
                 const uint32_t bytes = S::kABytes + nbox * kBoxRows * 128;
                 const int wrow = tl.g * args.n_out + tl.mt * kBM;
+                const uint64_t pol_w =
+                    (s_off[tl.g + 1] - s_off[tl.g] > BN) ? pol_w_shared : pol_w_once;
                 for (int kb = 0; kb < KB; ++kb) {
                     if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag,
                                       args.status, MOE_DEV_TIMEOUT)) {
@@ -534,7 +541,11 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     args.c = c;
     args.c_bf16 = c_dtype == MOE_OUT_BF16;
     args.status = status;
-    if (fp8) return launch_impl<true, 32, 4>(args, a, w, s);
+    // Decode-sized groups (a few rows each) stream best with 32-row tiles;
+    // larger groups re-read each weight tile fewer times with 64-row tiles.
+    const bool wide = (int64_t)rows >= 16 * (int64_t)groups;
+    if (fp8) return wide ? launch_impl<true, 64, 3>(args, a, w, s)
+                         : launch_impl<true, 32, 4>(args, a, w, s);
     return launch_impl<false, 32, 4>(args, a, w, s);
 }
 

@@ -12,8 +12,9 @@
 //                      meet in an xor butterfly (16, 8, 4, 2, 1).  A bf16
 //                      product is exact in fp32, so the result is a fixed
 //                      sequence of rounded additions: the routing decision
-//                      is reproducible bit for bit.  A warp computes a tile
-//                      of 4 tokens x 8 experts (32 accumulators per lane).
+//                      is reproducible bit for bit.  A CTA stages a 16-token x
+//                      16-expert tile through shared memory; each warp
+//                      computes 4 tokens x 8 experts (32 accumulators).
 //  route_select_kernel one warp per token: sigmoid (fp64, rounded to fp32)
 //                      or softmax scores, group scores from each group's
 //                      best group_topn, top groups, then top_k experts by
@@ -23,6 +24,7 @@
 
 #include <cfloat>
 #include <climits>
+#include <mutex>
 
 #include "internal.h"
 
@@ -31,7 +33,6 @@ namespace {
 
 constexpr int kTB = 4;   // tokens per warp tile
 constexpr int kEB = 8;   // experts per warp tile
-constexpr int kLogitWarps = 4;
 static_assert(kTB * kEB == 32, "one output per lane");
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
@@ -49,50 +50,80 @@ __device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b, float acc)
     return acc;
 }
 
-__global__ void __launch_bounds__(kLogitWarps * 32)
+// CTA tile of 16 tokens x 16 experts, 8 warps of 4 tokens x 8 experts each.
+// The CTA stages 256 hidden elements of its 32 rows per step in shared
+// memory (cp.async, 4-deep ring), so every row is fetched once per CTA
+// instead of once per warp.  Lane L still reads elements 8L..8L+7 of every
+// 256-element step, i.e. the hidden slice (h/8) mod 32 == L, in increasing h.
+constexpr int kCT = 16, kCE = 16;           // CTA tile
+constexpr int kStepElems = 256;             // hidden elements per stage
+constexpr int kLogitStages = 4;
+constexpr int kStageBytes = (kCT + kCE) * kStepElems * 2;   // 16 KB
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool valid) {
+    // src-size 0 fills the 16 bytes with zeros (rows past T or E, H tail)
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+                 "r"(valid ? 16 : 0)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(256)
     gate_logits_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wg,
                        const float *__restrict__ offset, float *__restrict__ logits, int T,
                        int E, int H) {
-    const int lane = threadIdx.x & 31;
-    const int warp = blockIdx.x * kLogitWarps + (threadIdx.x >> 5);
-    const int e_tiles = (E + kEB - 1) / kEB;
-    const int t0 = (warp / e_tiles) * kTB;
-    const int e0 = (warp % e_tiles) * kEB;
-    if (t0 >= T) return;   // warp-uniform
+    extern __shared__ __align__(16) uint8_t smem[];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t_base = blockIdx.x * kCT, e_base = blockIdx.y * kCE;
+    const int steps = (H + kStepElems - 1) / kStepElems;
+    const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+
+    // stage s: 32 rows (16 tokens then 16 experts) x 32 pieces of 16 bytes
+    auto issue = [&](int step) {
+        const uint32_t buf = sbase + (step % kLogitStages) * kStageBytes;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int p = tid + 256 * i;
+            const int r = p >> 5, piece = p & 31;
+            const int h = step * kStepElems + piece * 8;
+            const bool is_x = r < kCT;
+            const int row = is_x ? t_base + r : e_base + (r - kCT);
+            const bool ok = h < H && (is_x ? row < T : row < E);
+            const uint16_t *src = (is_x ? x : wg) + (ok ? (size_t)row * H + h : 0);
+            cp_async16(buf + r * (kStepElems * 2) + piece * 16, src, ok);
+        }
+    };
 
     float acc[kTB][kEB];
 #pragma unroll
     for (int i = 0; i < kTB; ++i)
 #pragma unroll
         for (int j = 0; j < kEB; ++j) acc[i][j] = 0.0f;
+    const int wt = warp >> 1, we = warp & 1;   // warp tile: tokens 4wt.., experts 8we..
 
-    const int chunks = H / 8;
-    const uint4 zero = make_uint4(0, 0, 0, 0);
-    uint4 xv[kTB], wv[kEB], xn[kTB], wn[kEB];
-    auto load = [&](int c, uint4 (&xd)[kTB], uint4 (&wd)[kEB]) {
+#pragma unroll
+    for (int st = 0; st < kLogitStages - 1; ++st) {
+        if (st < steps) issue(st);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    }
+    for (int step = 0; step < steps; ++step) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kLogitStages - 2) : "memory");
+        __syncthreads();   // stage `step` is visible; stage step-1 is no longer read
+        if (step + kLogitStages - 1 < steps) issue(step + kLogitStages - 1);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        const uint8_t *buf = smem + (step % kLogitStages) * kStageBytes;
+        uint4 xv[kTB], wv[kEB];
 #pragma unroll
         for (int i = 0; i < kTB; ++i)
-            xd[i] = (c < chunks && t0 + i < T)
-                        ? __ldg(reinterpret_cast<const uint4 *>(x + (size_t)(t0 + i) * H) + c)
-                        : zero;
+            xv[i] = *reinterpret_cast<const uint4 *>(buf + (wt * kTB + i) * (kStepElems * 2) + lane * 16);
 #pragma unroll
         for (int j = 0; j < kEB; ++j)
-            wd[j] = (c < chunks && e0 + j < E)
-                        ? __ldg(reinterpret_cast<const uint4 *>(wg + (size_t)(e0 + j) * H) + c)
-                        : zero;
-    };
-    load(lane, xv, wv);
-    for (int c = lane; c < chunks; c += 32) {
-        load(c + 32, xn, wn);   // next chunk's loads overlap this chunk's FMAs
+            wv[j] = *reinterpret_cast<const uint4 *>(buf + (kCT + we * kEB + j) * (kStepElems * 2) + lane * 16);
 #pragma unroll
         for (int i = 0; i < kTB; ++i)
 #pragma unroll
             for (int j = 0; j < kEB; ++j) acc[i][j] = dot8(xv[i], wv[j], acc[i][j]);
-#pragma unroll
-        for (int i = 0; i < kTB; ++i) xv[i] = xn[i];
-#pragma unroll
-        for (int j = 0; j < kEB; ++j) wv[j] = wn[j];
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 
     float mine = 0.0f;
 #pragma unroll
@@ -104,7 +135,7 @@ __global__ void __launch_bounds__(kLogitWarps * 32)
             for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
             if (lane == i * kEB + j) mine = v;
         }
-    const int t = t0 + lane / kEB, e = e0 + lane % kEB;
+    const int t = t_base + wt * kTB + lane / kEB, e = e_base + we * kEB + lane % kEB;
     if (t < T && e < E) logits[(size_t)t * E + e] = offset ? __fadd_rn(mine, offset[e]) : mine;
 }
 
@@ -160,34 +191,81 @@ __global__ void __launch_bounds__(32) route_select_kernel(const SelectArgs a) {
 
     if (a.groups > 1) {
         const int gs = a.E / a.groups;
-        float my_gscore = -FLT_MAX;
-        for (int g = 0; g < a.groups; ++g) {
+        uint32_t gmask = 0;
+        if (gs == 32 && a.topn <= 4) {
+            // Groups of 32: lane L holds expert L of every group (group g is
+            // q == g), so all groups reduce at once; same order, ties and
+            // sums as the general path below.
+            float gsum[PL];
             uint32_t taken = 0;
-            float sum = 0.0f;
             for (int r = 0; r < a.topn; ++r) {
-                float bv = -FLT_MAX;
-                int bi = INT_MAX;
+                float v[PL];
+                int id[PL];
 #pragma unroll
                 for (int q = 0; q < PL; ++q) {
-                    const int e = q * 32 + lane;
-                    if (((valid >> q) & 1u) && !((taken >> q) & 1u) && e >= g * gs &&
-                        e < (g + 1) * gs && (sel[q] > bv || (sel[q] == bv && e < bi))) {
-                        bv = sel[q];
-                        bi = e;
+                    const bool ok = ((valid >> q) & 1u) && !((taken >> q) & 1u);
+                    v[q] = ok ? sel[q] : -FLT_MAX;
+                    id[q] = ok ? q * 32 + lane : INT_MAX;
+                }
+#pragma unroll
+                for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+                    for (int q = 0; q < PL; ++q) {
+                        const float ov = __shfl_xor_sync(0xffffffffu, v[q], o);
+                        const int oi = __shfl_xor_sync(0xffffffffu, id[q], o);
+                        if (ov > v[q] || (ov == v[q] && oi < id[q])) {
+                            v[q] = ov;
+                            id[q] = oi;
+                        }
                     }
                 }
-                warp_argmax(bv, bi);
-                if (bi != INT_MAX && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-                sum = (r == 0) ? bv : __fadd_rn(sum, bv);
+#pragma unroll
+                for (int q = 0; q < PL; ++q) {
+                    if (id[q] != INT_MAX && (id[q] & 31) == lane) taken |= 1u << q;
+                    gsum[q] = (r == 0) ? v[q] : __fadd_rn(gsum[q], v[q]);
+                }
             }
-            if (lane == g) my_gscore = sum;
-        }
-        uint32_t gmask = 0;
-        for (int r = 0; r < a.topk_groups; ++r) {
-            float v = (lane < a.groups && !((gmask >> lane) & 1u)) ? my_gscore : -FLT_MAX;
-            int i = (lane < a.groups && !((gmask >> lane) & 1u)) ? lane : INT_MAX;
-            warp_argmax(v, i);
-            if (i != INT_MAX) gmask |= 1u << i;
+            for (int r = 0; r < a.topk_groups; ++r) {   // group scores are warp-uniform
+                float bv = -FLT_MAX;
+                int bg = INT_MAX;
+#pragma unroll
+                for (int q = 0; q < PL; ++q)
+                    if (q < a.groups && !((gmask >> q) & 1u) &&
+                        (gsum[q] > bv || (gsum[q] == bv && q < bg))) {
+                        bv = gsum[q];
+                        bg = q;
+                    }
+                if (bg != INT_MAX) gmask |= 1u << bg;
+            }
+        } else {
+            float my_gscore = -FLT_MAX;
+            for (int g = 0; g < a.groups; ++g) {
+                uint32_t taken = 0;
+                float sum = 0.0f;
+                for (int r = 0; r < a.topn; ++r) {
+                    float bv = -FLT_MAX;
+                    int bi = INT_MAX;
+#pragma unroll
+                    for (int q = 0; q < PL; ++q) {
+                        const int e = q * 32 + lane;
+                        if (((valid >> q) & 1u) && !((taken >> q) & 1u) && e >= g * gs &&
+                            e < (g + 1) * gs && (sel[q] > bv || (sel[q] == bv && e < bi))) {
+                            bv = sel[q];
+                            bi = e;
+                        }
+                    }
+                    warp_argmax(bv, bi);
+                    if (bi != INT_MAX && (bi & 31) == lane) taken |= 1u << (bi >> 5);
+                    sum = (r == 0) ? bv : __fadd_rn(sum, bv);
+                }
+                if (lane == g) my_gscore = sum;
+            }
+            for (int r = 0; r < a.topk_groups; ++r) {
+                float v = (lane < a.groups && !((gmask >> lane) & 1u)) ? my_gscore : -FLT_MAX;
+                int i = (lane < a.groups && !((gmask >> lane) & 1u)) ? lane : INT_MAX;
+                warp_argmax(v, i);
+                if (i != INT_MAX) gmask |= 1u << i;
+            }
         }
 #pragma unroll
         for (int q = 0; q < PL; ++q) {
@@ -288,10 +366,22 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
                  cudaStream_t s) {
     if (T == 0) return MOE_OK;
     const int E = cfg->num_experts, H = cfg->hidden;
-    const int warps = (int)(ceil_div(T, kTB) * ceil_div(E, kEB));
-    gate_logits_kernel<<<(warps + kLogitWarps - 1) / kLogitWarps, kLogitWarps * 32, 0, s>>>(
-        static_cast<const uint16_t *>(x), static_cast<const uint16_t *>(w_gate), logit_offset,
-        logits, T, E, H);
+    const dim3 grid((unsigned)ceil_div(T, kCT), (unsigned)ceil_div(E, kCE));
+    const int smem = kLogitStages * kStageBytes;
+    static std::once_flag attr_once[64];
+    static int attr_rc[64];
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    std::call_once(attr_once[dev], [&] {
+        attr_rc[dev] = cudaFuncSetAttribute(gate_logits_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
+                               cudaSuccess ? 0 : 1;
+    });
+    if (attr_rc[dev]) return MOE_ERR_CUDA;
+    gate_logits_kernel<<<grid, 256, smem, s>>>(static_cast<const uint16_t *>(x),
+                                               static_cast<const uint16_t *>(w_gate),
+                                               logit_offset, logits, T, E, H);
     MOE_LAUNCH_CHECK();
 
     SelectArgs a;
