@@ -299,7 +299,7 @@ def main():
         dist.barrier()
     import moe_expert_layer_07_gb300 as moe
 
-    inp, layer, log2phys, perm_info = setup(shape, args.seed + rank, device)
+    inp, layer, log2phys, perm_info = setup(shape, replica_seed(args.seed, rank), device)
     T, H = shape.tokens, shape.hidden
     x = inp["x"]
     out = torch.empty((T, H), dtype=torch.float32, device=device)
@@ -324,17 +324,13 @@ def main():
         end.record()
         torch.cuda.synchronize()
         barrier()
-    elapsed_ms = start.elapsed_time(end)
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world, device)
     status = layer.status()
     kms = stepper.kernel_ms()
     offsets = layer.view("expert_offsets", torch.int32, (shape.groups + 1,)).cpu().numpy()
     bytes_per, active, flops = algorithmic_bytes(shape, offsets)
     ms_step = elapsed_ms / args.steps
-    value = T * world * args.steps / (elapsed_ms / 1e3)
+    value = job_tokens_per_s(T, world, args.steps, elapsed_ms)
 
     hbm_peak, bf16_peak, peak_src = load_peaks()
     layer_bytes = sum(bytes_per.values())
@@ -389,6 +385,27 @@ def main():
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def replica_seed(seed, rank):
+    """Each rank's replica draws its own batch (weak scaling: per-GPU work fixed)."""
+    return seed + rank
+
+
+def max_over_ranks(elapsed_ms, world, device=None):
+    """The job's time is the slowest rank's (all_reduce MAX on the default group)."""
+    if world <= 1:
+        return float(elapsed_ms)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(tokens_per_step, world, steps, elapsed_ms):
+    """Whole-job throughput: every rank's tokens over the slowest rank's time."""
+    return tokens_per_step * world * steps / (elapsed_ms / 1e3)
 
 
 def default_cpu_tokens(shape):
