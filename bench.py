@@ -115,24 +115,26 @@ def setup(shape, seed, device):
     import synth
 
     inp = synth.make_inputs(shape, seed=seed, device=device)
+    layer = moe.MoELayer(shape, inp)
     log2phys = None
     info = {}
     if shape.balanced_perm:
-        # calibration: route the batch without a permutation, count rows per
-        # expert from the dispatch offsets, balance, re-lay the weights
-        probe = moe.MoELayer(shape, inp)
+        # calibration with the product path: count rows per expert on the
+        # device over one routed batch, derive the balanced permutation and
+        # re-lay the expert weights on a side stream
+        reb = moe.ExpertRebalancer(layer, shape.num_sets)
         out = torch.empty((shape.tokens, shape.hidden), device=device)
-        probe.forward(inp["x"], out)
-        off = probe.view("expert_offsets", torch.int32, (shape.groups + 1,)).cpu().numpy()
-        counts = np.diff(off)[:shape.num_experts].astype(np.int64)
-        log2phys, phys2log, mom = moe.balance_permutation(counts, shape.num_sets)
-        naive = counts.reshape(shape.num_sets, -1).sum(1)
-        info = {"set_imbalance": round(mom, 4),
-                "set_imbalance_contiguous": round(float(naive.max() / naive.mean()), 4)}
-        del probe
-        inp = synth.relayout_experts(inp, shape, phys2log)
+        layer.forward(inp["x"], out)
+        reb.observe()
+        before, after = reb.rebalance()
+        ms = reb.last_relayout_ms()
+        log2phys = reb.log2phys
+        info = {"set_imbalance": round(after, 4), "set_imbalance_contiguous": round(before, 4),
+                "relayout_ms": round(ms, 3),
+                "relayout_gbs": round(reb.relayout_bytes / (ms * 1e-3) / 1e9, 1)}
+        inp = {k: v for k, v in layer._keep.items() if k != "log2phys"}
+        torch.cuda.synchronize()
         torch.cuda.empty_cache()
-    layer = moe.MoELayer(shape, inp, log2phys=log2phys)
     return inp, layer, log2phys, info
 
 

@@ -198,7 +198,7 @@ MOE_API size_t moe_permute_static_scratch_capacity(void);
  * BF16: A bf16 [rows, K], W bf16 [groups, N, K], scales unused.
  * C: fp32 or bf16 (c_dtype = MOE_OUT_*) [rows, N]; rows outside every group
  *   are not written.  expert_offsets: device int32 [groups + 1].
- * N multiple of 128; K multiple of 128 and at most 8192 (FP8) or multiple
+ * N multiple of 128; K multiple of 128 and at most 7168 (FP8) or multiple
  * of 64 (BF16); groups <= 1024.
  * Tensor cores (tcgen05, accumulators in tensor memory) fed by TMA; weight
  * rows sit on the MMA's M side and the few token rows of an expert on its
@@ -262,6 +262,29 @@ MOE_API int moe_layer_kernel_count(const moe_config *cfg, int32_t T);
  * kernel always returns; nothing traps. */
 MOE_API int moe_selftest_bounded_wait(int32_t *dev_status, int64_t limit_ns, int32_t *dev_result,
                                       void *stream);
+
+/* ---- continuous load balancing ------------------------------------------------
+ * Report, section "Load balancing across GPUs": in serving, activation
+ * frequencies are re-measured periodically and a new expert permutation is
+ * generated from them.
+ * moe_count_expert_rows: counts[p] += expert_offsets[p+1] - expert_offsets[p]
+ *   for every routed expert p (PHYSICAL order), i.e. this batch's rows per
+ *   expert; counts is a device int64 [E] accumulator owned by the caller.
+ *   Exact integer sums: the result does not depend on launch order.
+ * moe_relayout_experts: dst block p = src block src_slot[p] for p < groups,
+ *   each block block_bytes long (a multiple of 16; e.g. one expert's W13,
+ *   W2 or scales).  src_slot is a device int32 [groups] table; an entry
+ *   outside [0, groups) copies nothing and sets MOE_DEV_BAD_EXPERT_ID in
+ *   *dev_status (nullable).  src and dst must not overlap (checked).
+ *   Applying a new permutation: with old/new logical->physical tables,
+ *   src_slot[p] = old_log2phys[new_phys2log[p]] for routed p, and p itself for
+ *   the shared experts; run it on a side stream into second buffers while the
+ *   layer keeps serving, then switch pointers. */
+MOE_API int moe_count_expert_rows(const moe_config *cfg, const int32_t *expert_offsets,
+                                  int64_t *counts, void *stream);
+MOE_API int moe_relayout_experts(const void *src, void *dst, const int32_t *src_slot,
+                                 int32_t groups, int64_t block_bytes, int32_t *dev_status,
+                                 void *stream);
 
 /* ---- host: balanced expert permutation ----------------------------------------------
  * Report, section "Load balancing across GPUs": from measured activation

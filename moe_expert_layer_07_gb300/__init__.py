@@ -17,6 +17,7 @@ __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_
            "permute", "permute_workspace_size", "permute_static_scratch", "grouped_gemm", "combine", "layer_forward",
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
            "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
+           "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
            "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
            "ACT_SILU_MUL"]
 
@@ -73,6 +74,8 @@ _SIGS = {
     "expert_balance_permutation": [_P, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_double)],
     "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
     "moe_permute_static_scratch": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "moe_count_expert_rows": [_CP, _P, _P, _P],
+    "moe_relayout_experts": [_P, _P, _P, _I, ctypes.c_int64, _P, _P],
 }
 
 
@@ -186,6 +189,27 @@ def combine(cfg: Config, T, y, row_of_slot, topk_w, expert_offsets, out, out_dty
            "moe_combine")
 
 
+def count_expert_rows(cfg: Config, expert_offsets, counts, stream=None):
+    """counts[p] += rows of routed expert p (physical) in the batch behind expert_offsets."""
+    _check(lib().moe_count_expert_rows(ctypes.byref(cfg), _ptr(expert_offsets), _ptr(counts),
+                                       _stream(stream)), "moe_count_expert_rows")
+
+
+def relayout_experts(src, dst, src_slot, groups, block_bytes, status=None, stream=None):
+    """dst block p = src block src_slot[p] (device tensors/pointers)."""
+    _check(lib().moe_relayout_experts(_ptr(src), _ptr(dst), _ptr(src_slot), groups, block_bytes,
+                                      _ptr(status), _stream(stream)), "moe_relayout_experts")
+
+
+def source_slots(old_log2phys, new_phys2log, num_experts: int, groups: int):
+    """Re-layout table: new physical slot p takes the block now at
+    old_log2phys[new_phys2log[p]]; shared experts (p >= num_experts) stay."""
+    import numpy as np
+    old = np.asarray(old_log2phys, dtype=np.int64)
+    new = np.asarray(new_phys2log, dtype=np.int64)
+    return np.concatenate([old[new], np.arange(num_experts, groups)]).astype(np.int32)
+
+
 def workspace_size(cfg: Config) -> int:
     n = ctypes.c_size_t()
     _check(lib().moe_workspace_size(ctypes.byref(cfg), ctypes.byref(n)), "moe_workspace_size")
@@ -240,19 +264,26 @@ class MoELayer:
         import torch
         self.cfg = make_config(shape, max_tokens)
         self.shape = shape
-        self._keep = dict(weights)
-        if log2phys is not None:
-            self._keep["log2phys"] = torch.as_tensor(log2phys, dtype=torch.int32,
-                                                     device=weights["w13"].device)
-        k = self._keep
-        self.weights = Weights(w_gate=_ptr(k["wg"]), e_bias=_ptr(k.get("e_bias")),
-                               logit_offset=_ptr(k.get("logit_offset")),
-                               log2phys=_ptr(k.get("log2phys")), w13=_ptr(k["w13"]),
-                               w13_scales=_ptr(k.get("w13_s")), w2=_ptr(k["w2"]),
-                               w2_scales=_ptr(k.get("w2_s")))
+        self.set_weights(weights, log2phys)
         self.ws_bytes = workspace_size(self.cfg)
         self.layout = workspace_layout(self.cfg)
         self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=weights["w13"].device)
+
+    def set_weights(self, weights: dict, log2phys=None):
+        """Point the layer at (new) device weights; keeps references alive."""
+        import torch
+        keep = dict(weights)
+        if log2phys is not None:
+            keep["log2phys"] = torch.as_tensor(log2phys, dtype=torch.int32,
+                                               device=weights["w13"].device)
+        else:
+            keep.pop("log2phys", None)
+        self._keep = keep
+        self.weights = Weights(w_gate=_ptr(keep["wg"]), e_bias=_ptr(keep.get("e_bias")),
+                               logit_offset=_ptr(keep.get("logit_offset")),
+                               log2phys=_ptr(keep.get("log2phys")), w13=_ptr(keep["w13"]),
+                               w13_scales=_ptr(keep.get("w13_s")), w2=_ptr(keep["w2"]),
+                               w2_scales=_ptr(keep.get("w2_s")))
 
     def forward(self, x, out, out_dtype=OUT_F32, T=None, stream=None):
         """x bf16 [T, H] and out [T, H] (fp32 or bf16) device tensors."""
@@ -278,3 +309,89 @@ class MoELayer:
 
     def status(self) -> int:
         return get_device_status(self.ws)
+
+
+class ExpertRebalancer:
+    """Continuous load balancing of one MoELayer: counts each batch's rows per
+    expert on the device, and on request derives a new balanced permutation
+    from the counts and re-lays the expert weights into it on a side stream
+    (report "21K output tokens/s DeepSeek inference on MI300X with Expert
+    Parallelism", section "Load balancing across GPUs").
+
+    The layer's output does not change when its experts move: routing is
+    defined on logical ids and each expert's rows are computed the same way
+    wherever its weights sit.
+    """
+
+    _BLOCKS = ("w13", "w13_s", "w2", "w2_s")
+
+    def __init__(self, layer: MoELayer, num_sets: int):
+        import numpy as np
+        import torch
+        self.layer = layer
+        self.num_sets = num_sets
+        s = layer.shape
+        dev = layer._keep["w13"].device
+        self.counts = torch.zeros(s.num_experts, dtype=torch.int64, device=dev)
+        l2p = layer._keep.get("log2phys")
+        self.log2phys = (np.arange(s.num_experts, dtype=np.int32) if l2p is None
+                         else l2p.cpu().numpy().astype(np.int32))
+        self.side = torch.cuda.Stream(device=dev)
+
+    def observe(self, stream=None):
+        """Add the last forward's rows per expert (enqueued, no host sync)."""
+        lay = self.layer
+        count_expert_rows(lay.cfg, lay.ws.data_ptr() + lay.layout.expert_offsets, self.counts,
+                          stream)
+
+    def logical_counts(self):
+        """Rows per logical expert since the last re-balance (synchronous read)."""
+        return self.counts.cpu().numpy()[self.log2phys]
+
+    def rebalance(self, counts=None):
+        """New permutation from the counts; weights re-laid on a side stream,
+        then the layer switches to them (the current stream waits for the copy).
+        Returns (set imbalance before, after)."""
+        import numpy as np
+        import torch
+        lay, s = self.layer, self.layer.shape
+        c = self.logical_counts() if counts is None else np.asarray(counts, np.int64)
+        m = s.num_experts // self.num_sets
+        loads = np.zeros(self.num_sets, np.int64)
+        for e in range(s.num_experts):
+            loads[self.log2phys[e] // m] += c[e]
+        before = float(loads.max() / loads.mean()) if loads.sum() else 1.0
+        new_l2p, new_p2l, after = balance_permutation(c, self.num_sets)
+        src = torch.as_tensor(source_slots(self.log2phys, new_p2l, s.num_experts, s.groups),
+                              device=self.counts.device)
+        cur = torch.cuda.current_stream(self.counts.device)
+        self.side.wait_stream(cur)
+        new_w = dict(lay._keep)
+        self._events = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+        self.relayout_bytes = 0
+        with torch.cuda.stream(self.side):
+            self._events[0].record(self.side)
+            for key in self._BLOCKS:
+                t = lay._keep.get(key)
+                if t is None:
+                    continue
+                out = torch.empty_like(t)
+                relayout_experts(t, out, src, s.groups, t[0].numel() * t.element_size(),
+                                 stream=self.side)
+                new_w[key] = out
+                self.relayout_bytes += 2 * t.numel() * t.element_size()
+            self._events[1].record(self.side)
+            self.counts.zero_()
+        cur.wait_stream(self.side)
+        for key in self._BLOCKS:   # old buffers stay valid until the copy is done
+            if lay._keep.get(key) is not None:
+                lay._keep[key].record_stream(self.side)
+        new_w.pop("log2phys", None)
+        lay.set_weights(new_w, new_l2p)
+        self.log2phys = new_l2p.astype(np.int32)
+        return before, float(after)
+
+    def last_relayout_ms(self):
+        """Device time of the last re-layout (waits for it)."""
+        self._events[1].synchronize()
+        return self._events[0].elapsed_time(self._events[1])

@@ -151,3 +151,15 @@ def test_balance_rejects_bad_arguments(L):
     c[2] = -1
     assert L.expert_balance_permutation(c.ctypes.data, 10, 5, out.ctypes.data, out.ctypes.data,
                                         None) == -1
+
+
+def test_source_slots_apply_a_new_permutation():
+    rng = np.random.default_rng(21)
+    E, G = 32, 34
+    for _ in range(5):
+        old_p2l = rng.permutation(E)
+        old_l2p = np.argsort(old_p2l)
+        new_p2l = rng.permutation(E)
+        src = moe.source_slots(old_l2p, new_p2l, E, G)
+        blocks_old = np.concatenate([old_p2l, np.arange(E, G)])   # logical id held per slot
+        assert np.array_equal(blocks_old[src], np.concatenate([new_p2l, np.arange(E, G)]))
