@@ -24,6 +24,7 @@ Modules:
   permute  slot -> per-expert row permutation and its offsets
   layer    expert SwiGLU FFN, grouped GEMM, combine, the whole layer
   balance  exhaustive balanced partition (tiny expert counts)
+  affinity co-activation matrix, affinity-aware placement optimum (tiny E)
 """
-from . import balance, layer, permute, quant, routing  # noqa: F401
+from . import affinity, balance, layer, permute, quant, routing  # noqa: F401
 from ._clib import build, num_threads, set_num_threads  # noqa: F401
