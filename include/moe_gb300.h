@@ -282,6 +282,15 @@ MOE_API int moe_selftest_bounded_wait(int32_t *dev_status, int64_t limit_ns, int
  *   layer keeps serving, then switch pointers. */
 MOE_API int moe_count_expert_rows(const moe_config *cfg, const int32_t *expert_offsets,
                                   int64_t *counts, void *stream);
+/* SGLang/H20 article, section "Expert Affinity EPLB": track which experts a
+ * token selects together.  coact[a*E + b] += 1 for every token of the
+ * batch and every two of its k selected experts a != b, as LOGICAL ids
+ * (topk_ids are physical; phys2log, device int32 [E], maps them back;
+ * NULL = identity).  coact: device int64 [E, E] accumulator, symmetric.
+ * Integer atomics: the sums do not depend on order.  Ids out of range are
+ * skipped. */
+MOE_API int moe_count_coactivation(const moe_config *cfg, int32_t T, const int32_t *topk_ids,
+                                   const int32_t *phys2log, int64_t *coact, void *stream);
 MOE_API int moe_relayout_experts(const void *src, void *dst, const int32_t *src_slot,
                                  int32_t groups, int64_t block_bytes, int32_t *dev_status,
                                  void *stream);
@@ -301,6 +310,20 @@ MOE_API int moe_relayout_experts(const void *src, void *dst, const int32_t *src_
  * Pure host code; usable without a GPU. */
 MOE_API int expert_balance_permutation(const int64_t *counts, int32_t num_experts, int32_t num_sets,
                                int32_t *log2phys, int32_t *phys2log, double *max_over_mean);
+
+/* Host: affinity-aware placement (SGLang/H20 article, section "Expert
+ * Affinity EPLB").  From per-expert counts and the symmetric co-activation
+ * matrix coact (host int64 [E, E]), group the experts into num_sets equal
+ * sets that keep as much co-activation inside sets as possible while every
+ * set total stays within max(L*, floor((1 + load_slack) * mean)), L* being
+ * the largest set total of the balanced partition above.  Exact for
+ * E <= 16, otherwise best-improvement swaps from the balanced partition.
+ * Same layout rule and outputs as expert_balance_permutation, plus
+ * *intra_fraction (nullable): co-activation kept inside sets / all of it. */
+MOE_API int expert_affinity_permutation(const int64_t *counts, const int64_t *coact,
+                                        int32_t num_experts, int32_t num_sets, double load_slack,
+                                        int32_t *log2phys, int32_t *phys2log,
+                                        double *max_over_mean, double *intra_fraction);
 
 #ifdef __cplusplus
 }

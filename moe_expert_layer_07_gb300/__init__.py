@@ -18,6 +18,7 @@ __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
            "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
            "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
+           "count_coactivation", "affinity_permutation",
            "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
            "ACT_SILU_MUL"]
 
@@ -75,6 +76,9 @@ _SIGS = {
     "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
     "moe_permute_static_scratch": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_count_expert_rows": [_CP, _P, _P, _P],
+    "moe_count_coactivation": [_CP, _I, _P, _P, _P, _P],
+    "expert_affinity_permutation": [_P, _P, _I, _I, ctypes.c_double, _P, _P,
+                                    ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
     "moe_relayout_experts": [_P, _P, _P, _I, ctypes.c_int64, _P, _P],
 }
 
@@ -193,6 +197,28 @@ def count_expert_rows(cfg: Config, expert_offsets, counts, stream=None):
     """counts[p] += rows of routed expert p (physical) in the batch behind expert_offsets."""
     _check(lib().moe_count_expert_rows(ctypes.byref(cfg), _ptr(expert_offsets), _ptr(counts),
                                        _stream(stream)), "moe_count_expert_rows")
+
+
+def count_coactivation(cfg: Config, T, topk_ids, phys2log, coact, stream=None):
+    """coact[a, b] += tokens selecting both logical experts a and b (device int64 [E, E])."""
+    _check(lib().moe_count_coactivation(ctypes.byref(cfg), T, _ptr(topk_ids), _ptr(phys2log),
+                                        _ptr(coact), _stream(stream)), "moe_count_coactivation")
+
+
+def affinity_permutation(counts, coact, num_sets: int, load_slack: float = 0.05):
+    """Host call: (log2phys, phys2log, max_over_mean, intra_fraction)."""
+    import numpy as np
+    c = np.ascontiguousarray(counts, dtype=np.int64)
+    A = np.ascontiguousarray(coact, dtype=np.int64)
+    E = len(c)
+    l2p = np.empty(E, dtype=np.int32)
+    p2l = np.empty(E, dtype=np.int32)
+    mom, intra = ctypes.c_double(), ctypes.c_double()
+    _check(lib().expert_affinity_permutation(c.ctypes.data, A.ctypes.data, E, num_sets,
+                                             float(load_slack), l2p.ctypes.data, p2l.ctypes.data,
+                                             ctypes.byref(mom), ctypes.byref(intra)),
+           "expert_affinity_permutation")
+    return l2p, p2l, mom.value, intra.value
 
 
 def relayout_experts(src, dst, src_slot, groups, block_bytes, status=None, stream=None):
@@ -325,24 +351,36 @@ class ExpertRebalancer:
 
     _BLOCKS = ("w13", "w13_s", "w2", "w2_s")
 
-    def __init__(self, layer: MoELayer, num_sets: int):
+    def __init__(self, layer: MoELayer, num_sets: int, affinity_slack: float | None = None):
+        """affinity_slack: None for plain balancing; a value (e.g. 0.05) to
+        also track co-activation and place co-selected experts together with
+        set totals allowed up to (1 + slack) x the mean."""
         import numpy as np
         import torch
         self.layer = layer
         self.num_sets = num_sets
+        self.affinity_slack = affinity_slack
         s = layer.shape
         dev = layer._keep["w13"].device
         self.counts = torch.zeros(s.num_experts, dtype=torch.int64, device=dev)
+        self.coact = (torch.zeros((s.num_experts, s.num_experts), dtype=torch.int64, device=dev)
+                      if affinity_slack is not None else None)
         l2p = layer._keep.get("log2phys")
         self.log2phys = (np.arange(s.num_experts, dtype=np.int32) if l2p is None
                          else l2p.cpu().numpy().astype(np.int32))
+        self._p2l = torch.as_tensor(np.argsort(self.log2phys).astype(np.int32), device=dev)
         self.side = torch.cuda.Stream(device=dev)
+        self.last_intra_fraction = None
 
-    def observe(self, stream=None):
-        """Add the last forward's rows per expert (enqueued, no host sync)."""
+    def observe(self, T=None, stream=None):
+        """Add the last forward's rows per expert (and co-activation), enqueued."""
         lay = self.layer
         count_expert_rows(lay.cfg, lay.ws.data_ptr() + lay.layout.expert_offsets, self.counts,
                           stream)
+        if self.coact is not None:
+            count_coactivation(lay.cfg, lay.shape.tokens if T is None else T,
+                               lay.ws.data_ptr() + lay.layout.topk_ids, self._p2l, self.coact,
+                               stream)
 
     def logical_counts(self):
         """Rows per logical expert since the last re-balance (synchronous read)."""
@@ -361,7 +399,11 @@ class ExpertRebalancer:
         for e in range(s.num_experts):
             loads[self.log2phys[e] // m] += c[e]
         before = float(loads.max() / loads.mean()) if loads.sum() else 1.0
-        new_l2p, new_p2l, after = balance_permutation(c, self.num_sets)
+        if self.coact is not None:
+            new_l2p, new_p2l, after, self.last_intra_fraction = affinity_permutation(
+                c, self.coact.cpu().numpy(), self.num_sets, self.affinity_slack)
+        else:
+            new_l2p, new_p2l, after = balance_permutation(c, self.num_sets)
         src = torch.as_tensor(source_slots(self.log2phys, new_p2l, s.num_experts, s.groups),
                               device=self.counts.device)
         cur = torch.cuda.current_stream(self.counts.device)
@@ -382,6 +424,8 @@ class ExpertRebalancer:
                 self.relayout_bytes += 2 * t.numel() * t.element_size()
             self._events[1].record(self.side)
             self.counts.zero_()
+            if self.coact is not None:
+                self.coact.zero_()
         cur.wait_stream(self.side)
         for key in self._BLOCKS:   # old buffers stay valid until the copy is done
             if lay._keep.get(key) is not None:
@@ -389,6 +433,7 @@ class ExpertRebalancer:
         new_w.pop("log2phys", None)
         lay.set_weights(new_w, new_l2p)
         self.log2phys = new_l2p.astype(np.int32)
+        self._p2l = torch.as_tensor(new_p2l.astype(np.int32), device=self.counts.device)
         return before, float(after)
 
     def last_relayout_ms(self):

@@ -12,6 +12,7 @@
 //            other, best swap first, until none lowers the heaviest set.
 // Host-only code.
 #include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <numeric>
 #include <vector>
@@ -122,6 +123,26 @@ struct Exact {
     }
 };
 
+// Sets are numbered by their lowest logical id; inside a set, logical ids
+// ascend; set s holds physical ids [s*m, (s+1)*m).
+void write_layout(const Partition &p, int S, int m, int32_t *log2phys, int32_t *phys2log) {
+    const int E = (int)p.set_of.size();
+    std::vector<int> first(S, E);
+    for (int e = 0; e < E; ++e) first[p.set_of[e]] = std::min(first[p.set_of[e]], e);
+    std::vector<int> set_rank(S);
+    std::iota(set_rank.begin(), set_rank.end(), 0);
+    std::sort(set_rank.begin(), set_rank.end(), [&](int a, int b) { return first[a] < first[b]; });
+    std::vector<int> slot_of_set(S);
+    for (int r = 0; r < S; ++r) slot_of_set[set_rank[r]] = r;
+    std::vector<int> fill(S, 0);
+    for (int e = 0; e < E; ++e) {
+        const int s = slot_of_set[p.set_of[e]];
+        const int phys = s * m + fill[s]++;
+        log2phys[e] = phys;
+        phys2log[phys] = e;
+    }
+}
+
 }  // namespace
 
 extern "C" int expert_balance_permutation(const int64_t *counts, int32_t num_experts,
@@ -145,25 +166,169 @@ extern "C" int expert_balance_permutation(const int64_t *counts, int32_t num_exp
         for (int e = 0; e < E; ++e) p.load[p.set_of[e]] += c[e];
     }
 
-    // Sets are numbered by their lowest logical id; inside a set, logical ids ascend.
-    std::vector<int> first(S, E);
-    for (int e = 0; e < E; ++e) first[p.set_of[e]] = std::min(first[p.set_of[e]], e);
-    std::vector<int> set_rank(S);
-    std::iota(set_rank.begin(), set_rank.end(), 0);
-    std::sort(set_rank.begin(), set_rank.end(), [&](int a, int b) { return first[a] < first[b]; });
-    std::vector<int> slot_of_set(S);
-    for (int r = 0; r < S; ++r) slot_of_set[set_rank[r]] = r;
-    std::vector<int> fill(S, 0);
-    for (int e = 0; e < E; ++e) {
-        const int s = slot_of_set[p.set_of[e]];
-        const int phys = s * m + fill[s]++;
-        log2phys[e] = phys;
-        phys2log[phys] = e;
-    }
+    write_layout(p, S, m, log2phys, phys2log);
     if (max_over_mean) {
         const int64_t total = std::accumulate(c.begin(), c.end(), (int64_t)0);
         const int64_t mx = *std::max_element(p.load.begin(), p.load.end());
         *max_over_mean = total > 0 ? (double)mx * S / (double)total : 1.0;
+    }
+    return MOE_OK;
+}
+
+namespace {
+
+// Co-activation kept inside sets: sum of A[a][b], a < b, same set.
+int64_t intra(const std::vector<int> &set_of, const int64_t *A, int E) {
+    int64_t v = 0;
+    for (int a = 0; a < E; ++a)
+        for (int b = a + 1; b < E; ++b)
+            if (set_of[a] == set_of[b]) v += A[(size_t)a * E + b];
+    return v;
+}
+
+// Exhaustive search (tiny E): the lowest unplaced expert opens a set, which
+// is completed with every combination of the remaining ones under the bound.
+struct AffinityExact {
+    const std::vector<int64_t> &c;
+    const int64_t *A;
+    int E, m;
+    int64_t bound, best = -1;
+    std::vector<int> set_of, best_set_of;
+    int next_set = 0;
+    AffinityExact(const std::vector<int64_t> &counts, const int64_t *aff, int E_, int m_, int64_t b)
+        : c(counts), A(aff), E(E_), m(m_), bound(b), set_of(E_, -1) {}
+    void run(int64_t acc) {
+        int first = -1;
+        for (int e = 0; e < E; ++e)
+            if (set_of[e] < 0) {
+                first = e;
+                break;
+            }
+        if (first < 0) {
+            if (acc > best) {
+                best = acc;
+                best_set_of = set_of;
+            }
+            return;
+        }
+        const int s = next_set++;
+        std::vector<int> members{first};
+        set_of[first] = s;
+        choose(first + 1, members, c[first], acc);
+        set_of[first] = -1;
+        --next_set;
+    }
+    void choose(int from, std::vector<int> &members, int64_t load, int64_t acc) {
+        if ((int)members.size() == m) {
+            int64_t gain = 0;
+            for (size_t i = 0; i < members.size(); ++i)
+                for (size_t j = i + 1; j < members.size(); ++j)
+                    gain += A[(size_t)members[i] * E + members[j]];
+            run(acc + gain);
+            return;
+        }
+        for (int e = from; e < E; ++e) {
+            if (set_of[e] >= 0 || load + c[e] > bound) continue;
+            set_of[e] = set_of[members[0]];
+            members.push_back(e);
+            choose(e + 1, members, load + c[e], acc);
+            members.pop_back();
+            set_of[e] = -1;
+        }
+    }
+};
+
+}  // namespace
+
+// Affinity-aware placement (SGLang/H20 article, section "Expert Affinity
+// EPLB": co-locate experts that are often selected together).  Start from
+// the balanced partition (largest set total L*), then maximise the
+// co-activation kept inside sets while every set total stays within
+// max(L*, floor((1 + slack) * mean)): exhaustively for E <= 16, otherwise by
+// best-improvement swaps between sets.
+extern "C" int expert_affinity_permutation(const int64_t *counts, const int64_t *coact,
+                                           int32_t num_experts, int32_t num_sets,
+                                           double load_slack, int32_t *log2phys,
+                                           int32_t *phys2log, double *max_over_mean,
+                                           double *intra_fraction) {
+    if (!counts || !coact || !log2phys || !phys2log || num_experts <= 0 || num_sets <= 0 ||
+        num_experts % num_sets || !(load_slack >= 0.0))
+        return MOE_ERR_INVALID_ARG;
+    const int E = num_experts, S = num_sets, m = E / S;
+    std::vector<int64_t> c(counts, counts + E);
+    for (int64_t v : c)
+        if (v < 0) return MOE_ERR_INVALID_ARG;
+    for (int a = 0; a < E; ++a)
+        for (int b = 0; b < E; ++b)
+            if (coact[(size_t)a * E + b] < 0 || coact[(size_t)a * E + b] != coact[(size_t)b * E + a])
+                return MOE_ERR_INVALID_ARG;
+
+    Partition p = greedy(c, S, m);
+    improve_by_swaps(c, S, p);
+    if (E <= 16) {
+        Exact ex(c, S, m, p);
+        ex.run(0, 0);
+        p.set_of = ex.best_assign;
+    }
+    p.load.assign(S, 0);
+    for (int e = 0; e < E; ++e) p.load[p.set_of[e]] += c[e];
+    const int64_t balanced_max = *std::max_element(p.load.begin(), p.load.end());
+    const int64_t total = std::accumulate(c.begin(), c.end(), (int64_t)0);
+    const int64_t bound = std::max<int64_t>(
+        balanced_max, (int64_t)std::floor((1.0 + load_slack) * (double)total / S));
+
+    if (E <= 16) {
+        AffinityExact ax(c, coact, E, m, bound);
+        ax.run(0);
+        if (ax.best >= 0) p.set_of = ax.best_set_of;
+    } else {
+        // W[e][s] = co-activation of expert e with the members of set s
+        std::vector<int64_t> W((size_t)E * S, 0);
+        for (int a = 0; a < E; ++a)
+            for (int b = 0; b < E; ++b) W[(size_t)a * S + p.set_of[b]] += coact[(size_t)a * E + b];
+        for (int iter = 0; iter < 100000; ++iter) {
+            int64_t best_gain = 0;
+            int ba = -1, bb = -1;
+            for (int a = 0; a < E; ++a) {
+                const int sa = p.set_of[a];
+                for (int b = a + 1; b < E; ++b) {
+                    const int sb = p.set_of[b];
+                    if (sa == sb) continue;
+                    const int64_t la = p.load[sa] - c[a] + c[b], lb = p.load[sb] - c[b] + c[a];
+                    if (la > bound || lb > bound) continue;
+                    const int64_t ab = coact[(size_t)a * E + b];
+                    const int64_t gain = (W[(size_t)a * S + sb] - ab - W[(size_t)a * S + sa]) +
+                                         (W[(size_t)b * S + sa] - ab - W[(size_t)b * S + sb]);
+                    if (gain > best_gain) {
+                        best_gain = gain;
+                        ba = a;
+                        bb = b;
+                    }
+                }
+            }
+            if (ba < 0) break;
+            const int sa = p.set_of[ba], sb = p.set_of[bb];
+            for (int e = 0; e < E; ++e) {
+                W[(size_t)e * S + sa] += coact[(size_t)e * E + bb] - coact[(size_t)e * E + ba];
+                W[(size_t)e * S + sb] += coact[(size_t)e * E + ba] - coact[(size_t)e * E + bb];
+            }
+            p.load[sa] += c[bb] - c[ba];
+            p.load[sb] += c[ba] - c[bb];
+            std::swap(p.set_of[ba], p.set_of[bb]);
+        }
+    }
+    p.load.assign(S, 0);
+    for (int e = 0; e < E; ++e) p.load[p.set_of[e]] += c[e];
+    write_layout(p, S, m, log2phys, phys2log);
+    if (max_over_mean) {
+        const int64_t mx = *std::max_element(p.load.begin(), p.load.end());
+        *max_over_mean = total > 0 ? (double)mx * S / (double)total : 1.0;
+    }
+    if (intra_fraction) {
+        int64_t all = 0;
+        for (int a = 0; a < E; ++a)
+            for (int b = a + 1; b < E; ++b) all += coact[(size_t)a * E + b];
+        *intra_fraction = all > 0 ? (double)intra(p.set_of, coact, E) / (double)all : 1.0;
     }
     return MOE_OK;
 }

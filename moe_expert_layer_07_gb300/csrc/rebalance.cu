@@ -6,6 +6,9 @@
 //   count_rows_kernel  counts[p] += rows of routed expert p in this batch,
 //                      read from the dispatch offsets (int64, exact: the
 //                      result does not depend on launch order).
+//   coactivation_kernel  A[a][b] += tokens whose top-k holds both a and b
+//                      (logical ids), for affinity-aware placement (SGLang/H20
+//                      article, section "Expert Affinity EPLB").
 //   relayout_kernel    dst block p = src block src_slot[p]: the weight (or
 //                      scale) re-layout that applies a new permutation, with
 //                      16-byte vector copies; run it on a side stream into a
@@ -21,6 +24,26 @@ __global__ void count_rows_kernel(const int32_t *__restrict__ offsets, int64_t *
                                   int E) {
     const int p = blockIdx.x * blockDim.x + threadIdx.x;
     if (p < E) counts[p] += (int64_t)(offsets[p + 1] - offsets[p]);
+}
+
+// One thread per ordered pair (j1 != j2) of a token's top-k: A[a][b] += 1 with
+// a, b the LOGICAL ids; integer atomics, so the sum does not depend on order.
+__global__ void coactivation_kernel(const int32_t *__restrict__ ids,
+                                    const int32_t *__restrict__ phys2log,
+                                    unsigned long long *__restrict__ A, int T, int k, int E) {
+    const long i = (long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long)T * k * k) return;
+    const int t = (int)(i / (k * k)), r = (int)(i % (k * k));
+    const int j1 = r / k, j2 = r % k;
+    if (j1 == j2) return;
+    int a = ids[(long)t * k + j1], b = ids[(long)t * k + j2];
+    if (a < 0 || a >= E || b < 0 || b >= E) return;
+    if (phys2log) {
+        a = phys2log[a];
+        b = phys2log[b];
+        if (a < 0 || a >= E || b < 0 || b >= E) return;
+    }
+    if (a != b) atomicAdd(&A[(long)a * E + b], 1ull);
 }
 
 __global__ void __launch_bounds__(256)
@@ -71,6 +94,22 @@ extern "C" MOE_API int moe_relayout_experts(const void *src, void *dst, const in
     moe::relayout_kernel<<<dim3(gx, groups), 256, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), src_slot, vec, groups,
         dev_status);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+extern "C" MOE_API int moe_count_coactivation(const moe_config *cfg, int32_t T,
+                                              const int32_t *topk_ids, const int32_t *phys2log,
+                                              int64_t *coact, void *stream) {
+    int rc = moe::check_config(cfg);
+    if (rc) return rc;
+    if (T < 0 || (T > 0 && (!topk_ids || !coact))) return MOE_ERR_INVALID_ARG;
+    const long n = (long)T * cfg->top_k * cfg->top_k;
+    if (n == 0) return MOE_OK;
+    moe::coactivation_kernel<<<(unsigned)((n + 255) / 256), 256, 0,
+                               static_cast<cudaStream_t>(stream)>>>(
+        topk_ids, phys2log, reinterpret_cast<unsigned long long *>(coact), T, cfg->top_k,
+        cfg->num_experts);
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

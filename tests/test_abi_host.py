@@ -163,3 +163,63 @@ def test_source_slots_apply_a_new_permutation():
         src = moe.source_slots(old_l2p, new_p2l, E, G)
         blocks_old = np.concatenate([old_p2l, np.arange(E, G)])   # logical id held per slot
         assert np.array_equal(blocks_old[src], np.concatenate([new_p2l, np.arange(E, G)]))
+
+
+from oracle import affinity as oaff   # noqa: E402
+
+
+@pytest.mark.parametrize("E,S", [(6, 2), (8, 2), (8, 4), (12, 3), (12, 4)])
+def test_affinity_placement_is_optimal_on_tiny_inputs(L, E, S):
+    rng = np.random.default_rng(E * 13 + S)
+    for _ in range(3):
+        counts = rng.integers(1, 40, size=E)
+        A = np.triu(rng.integers(0, 12, size=(E, E)), 1)
+        A = A + A.T
+        l2p, p2l, mom, intra = moe.affinity_permutation(counts, A, S, 0.05)
+        assert sorted(l2p.tolist()) == list(range(E)) and np.array_equal(p2l[l2p], np.arange(E))
+        sets = oaff.set_of_logical(l2p, E, S)
+        bound = oaff.load_bound(counts, S, balance.optimum_max_load(counts.tolist(), S), 0.05)
+        assert balance.set_loads(counts, l2p, S).max() <= bound
+        assert oaff.intra_affinity(A, sets) == oaff.optimum_affinity(counts, A, S, bound)
+        assert abs(intra - oaff.intra_affinity(A, sets) / oaff.total_affinity(A)) < 1e-12
+
+
+def test_affinity_placement_recovers_co_selected_clusters(L):
+    rng = np.random.default_rng(3)
+    E, S, k, T = 64, 8, 4, 4000
+    hidden = rng.permutation(E).reshape(S, E // S)      # 8 clusters under a random numbering
+    ids = []
+    for t in range(T):
+        c = hidden[rng.integers(S)]
+        pick = list(rng.choice(c, k - 1, replace=False)) + [int(rng.integers(E))]
+        while len(set(pick)) < k:
+            pick[-1] = int(rng.integers(E))
+        ids.append(pick)
+    ids = np.array(ids)
+    counts = np.bincount(ids.reshape(-1), minlength=E)
+    A = oaff.coactivation_n(ids, E)
+    l2p_b, _, mom_b = moe.balance_permutation(counts, S)
+    l2p_a, _, mom_a, intra = moe.affinity_permutation(counts, A, S, 0.05)
+    sets_contig = np.arange(E) // (E // S)
+    m_contig = oaff.mean_sets_per_token(ids, sets_contig)
+    m_bal = oaff.mean_sets_per_token(ids, oaff.set_of_logical(l2p_b, E, S))
+    m_aff = oaff.mean_sets_per_token(ids, oaff.set_of_logical(l2p_a, E, S))
+    planted = np.zeros(E, np.int64)
+    for s in range(S):
+        planted[hidden[s]] = s
+    m_planted = oaff.mean_sets_per_token(ids, planted)
+    # within 15% of the planted clustering, far below the load-only layouts
+    assert m_aff <= 1.15 * m_planted and m_aff < 0.7 * min(m_contig, m_bal)
+    assert intra >= 0.85 * oaff.intra_affinity(A, planted) / oaff.total_affinity(A)
+    assert mom_a <= max(mom_b, 1.05) + 1e-12
+    assert oaff.intra_affinity(A, oaff.set_of_logical(l2p_a, E, S)) >= \
+        oaff.intra_affinity(A, oaff.set_of_logical(l2p_b, E, S))
+
+
+def test_affinity_placement_rejects_bad_matrices(L):
+    c = np.ones(8, np.int64)
+    A = np.zeros((8, 8), np.int64)
+    A[0, 1] = 3                                          # not symmetric
+    out = np.empty(8, np.int32)
+    assert L.expert_affinity_permutation(c.ctypes.data, A.ctypes.data, 8, 2, ctypes.c_double(0.05),
+                                         out.ctypes.data, out.ctypes.data, None, None) == -1

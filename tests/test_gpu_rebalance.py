@@ -94,3 +94,31 @@ def test_rebalance_moves_experts_without_changing_the_output(lib, name):
     assert np.array_equal(np.sort(reb.log2phys), np.arange(shape.num_experts))
     assert int(reb.counts.sum().item()) == 0          # the window restarts
     print(f"{name}: set imbalance {before:.4f} -> {after:.4f}")
+
+
+def test_coactivation_counts_equal_the_oracle(lib):
+    from oracle import affinity as oaff
+    shape = synth.CONFIGS["r1_mini_zipf"]
+    inp = synth.make_inputs(shape, seed=2, device="cuda")
+    rng = np.random.default_rng(4)
+    p2l = rng.permutation(shape.num_experts)
+    l2p = np.argsort(p2l).astype(np.int32)
+    moved = synth.relayout_experts(inp, shape, p2l)
+    layer = moe.MoELayer(shape, moved, log2phys=l2p)
+    reb = moe.ExpertRebalancer(layer, shape.num_sets, affinity_slack=0.05)
+    out = torch.empty((shape.tokens, shape.hidden), device="cuda")
+    want = np.zeros((shape.num_experts, shape.num_experts), np.int64)
+    for b in range(2):
+        x = synth.make_inputs(shape, seed=20 + b, device="cuda")["x"]
+        layer.forward(x, out)
+        reb.observe()
+        _, logical = _oracle_phys_ids(shape, inp, x)
+        want += oaff.coactivation_n(logical, shape.num_experts)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(reb.coact), want)
+    before, after = reb.rebalance()
+    out_b = torch.empty_like(out)
+    layer.forward(x, out_b)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_b) and layer.status() == 0
+    assert 0.0 <= reb.last_intra_fraction <= 1.0
