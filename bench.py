@@ -141,7 +141,7 @@ def setup(shape, seed, device):
 class Stepper:
     """The hot path as its C-ABI steps on one stream, CUDA events around each."""
 
-    NAMES = ["route", "quant_x", "permute", "gemm_gate_up", "silu_requant", "gemm_down", "combine"]
+    NAMES = ["route", "quant_x", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
 
     def __init__(self, layer, x, out):
         import torch
@@ -157,6 +157,8 @@ class Stepper:
                    "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "gate_up",
                    "h", "h_scales", "y")}
         self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
+        rows = s.tokens * (s.top_k + s.num_shared)
+        self.wide = self.fp8 and rows >= 16 * s.groups   # as moe_layer_forward decides
         ws[L.status:L.status + 4].zero_()   # the device status word starts clear
         self.k = {}
         self.events = []
@@ -186,12 +188,16 @@ class Stepper:
                     p["row_of_slot"], p["xp"], p["xp_scales"] if self.fp8 else None,
                     p["perm_scratch"], self.perm_bytes, p["status"])
         mark()
-        moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"] if self.fp8 else None,
-                         p["expert_offsets"], w["w13"], w.get("w13_s"), p["gate_up"],
-                         moe.OUT_F32, p["status"])
-        mark()
-        moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, p["gate_up"], p["h"],
-                        p["h_scales"] if self.fp8 else None, rows_dev=p["expert_offsets"] + 4 * G)
+        if self.wide:   # the layer's two-kernel path for wide batches
+            moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"], p["expert_offsets"],
+                             w["w13"], w.get("w13_s"), p["gate_up"], moe.OUT_F32, p["status"])
+            moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, p["gate_up"], p["h"], p["h_scales"],
+                            rows_dev=p["expert_offsets"] + 4 * G)
+        else:
+            moe.grouped_gemm_swiglu(cfg, G, I, H, rows, p["xp"],
+                                    p["xp_scales"] if self.fp8 else None, p["expert_offsets"],
+                                    w["w13"], w.get("w13_s"), p["h"],
+                                    p["h_scales"] if self.fp8 else None, p["status"])
         mark()
         moe.grouped_gemm(cfg, G, H, I, rows, p["h"], p["h_scales"] if self.fp8 else None,
                          p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_F32,
@@ -230,8 +236,10 @@ def algorithmic_bytes(shape, offsets):
     b["route"] = 2 * T * H + 2 * E * H + 4 * T * E * 2 + 8 * T * k
     b["quant_x"] = (2 * T * H + T * H + T * sc_h) if fp8 else 0
     b["permute"] = 4 * T * k * 3 + rows * (H * eb + sc_h) * 2
-    b["gemm_gate_up"] = active * w13 + rows * (H * eb + sc_h) + rows * 2 * I * 4
-    b["silu_requant"] = rows * 2 * I * 4 + rows * (I * eb + sc_i)
+    wide = fp8 and rows >= 16 * (E + S)
+    # gate/up with SwiGLU; wide batches also write and re-read fp32 gate/up rows
+    b["gemm_gate_up_swiglu"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i) + \
+        (2 * rows * 2 * I * 4 if wide else 0)
     b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4
     b["combine"] = T * (k + S) * H * 4 + 8 * T * k + T * H * 4
     flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)
@@ -336,13 +344,14 @@ def main():
 
     hbm_peak, bf16_peak, peak_src = load_peaks()
     layer_bytes = sum(bytes_per.values())
-    gu_ms = kms["gemm_gate_up"]
-    achieved = bytes_per["gemm_gate_up"] / (gu_ms / 1e3) / 1e9
+    gu_ms = kms["gemm_gate_up_swiglu"]
+    achieved = bytes_per["gemm_gate_up_swiglu"] / (gu_ms / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168:
+    if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168 and \
+            not stepper.wide:
         with open(tpath) as f:
-            tr = json.load(f).get("gemm_gate_up")
+            tr = json.load(f).get("gemm_gate_up_swiglu")
         if tr:   # ncu DRAM bytes per active group (small R1 case) x this launch's groups
             traffic = tr["bytes_per_active_group"] * active
 
@@ -372,7 +381,7 @@ def main():
         "layer_roofline_frac": (layer_bytes / (hbm_peak * 1e9)) / (ms_step / 1e3),
         "active_experts": active,
         "kernels_ms": {k: round(v, 5) for k, v in kms.items()},
-        "roofline": {"bound": "hbm", "kernel": "grouped_gemm gate/up", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": "grouped_gemm gate/up + SwiGLU", "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)"},
         "tensor_pipe_frac_of_bf16x2": (flops / (ms_step / 1e3)) / (2 * bf16_peak * 1e12),

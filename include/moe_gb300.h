@@ -210,6 +210,25 @@ MOE_API int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_ou
                      const int32_t *expert_offsets, const void *w, const float *w_scales,
                      void *c, int32_t c_dtype, int32_t *dev_status, void *stream);
 
+/* Grouped GEMM with the SwiGLU epilogue (gate/up GEMM and SiLU-mul fused):
+ * for the rows r of group g, with W13[g] = [W_gate; W_up] ([2*inter, K]),
+ *   g = A[r] W_gate^T, u = A[r] W_up^T (fp32, FP8 block scales as in
+ *   moe_grouped_gemm), h = silu(g) * u (fp32), and
+ *   FP8 layers: h quantised per row and 128-feature group as in
+ *     moe_act_requant -> h e4m3 [rows, inter], h_scales fp32 [rows, inter/128];
+ *   BF16 layers: h rounded to bf16 -> h bf16 [rows, inter] (h_scales unused).
+ * Gives the same bits as moe_grouped_gemm (fp32 C) followed by
+ * moe_act_requant(SILU_MUL), without writing the fp32 gate/up rows.  A tile
+ * takes 128 gate rows and the matching 128 up rows, which share one
+ * activation tile (the report's "horizontal fusion" of an expert's GEMMs,
+ * section "Library optimisation").  inter multiple of 128; K as in
+ * moe_grouped_gemm. */
+MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter,
+                                    int32_t k_dim, int32_t rows, const void *a,
+                                    const float *a_scales, const int32_t *expert_offsets,
+                                    const void *w13, const float *w13_scales, void *h,
+                                    float *h_scales, int32_t *dev_status, void *stream);
+
 /* ---- combine -------------------------------------------------------------------
  * out[t, :] = sum_s Y[expert_offsets[E+s] + t, :]
  *           + sum_j topk_w[t, j] * Y[row_of_slot[t, j], :]    (fp32, shared
@@ -223,9 +242,12 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
                 int32_t out_dtype, void *stream);
 
 /* ---- the whole layer -------------------------------------------------------------
- * route -> (FP8: quantise x) -> permute -> grouped GEMM gate/up ->
- * SiLU-mul (+ FP8 requantisation) -> grouped GEMM down (fp32 expert
- * outputs) -> combine, all on
+ * route -> (FP8: quantise x) -> permute -> grouped GEMM gate/up with the
+ * SwiGLU epilogue (+ FP8 requantisation of h) -> grouped GEMM down (fp32
+ * expert outputs) -> combine, all on
+ * `stream`; FP8 batches whose groups average 16 rows or more run the
+ * gate/up GEMM (64-row tiles, fp32 rows) and SiLU-mul as two kernels
+ * instead, with the same result bits; also
  * `stream`, all intermediates inside `ws` (size from moe_workspace_size for
  * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..
  * max_tokens.  The workspace's device status word is cleared at the start

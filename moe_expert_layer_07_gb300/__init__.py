@@ -18,7 +18,7 @@ __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
            "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
            "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
-           "count_coactivation", "affinity_permutation",
+           "count_coactivation", "affinity_permutation", "grouped_gemm_swiglu",
            "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
            "ACT_SILU_MUL"]
 
@@ -76,6 +76,7 @@ _SIGS = {
     "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
     "moe_permute_static_scratch": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_count_expert_rows": [_CP, _P, _P, _P],
+    "moe_grouped_gemm_swiglu": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_count_coactivation": [_CP, _I, _P, _P, _P, _P],
     "expert_affinity_permutation": [_P, _P, _I, _I, ctypes.c_double, _P, _P,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
@@ -185,6 +186,14 @@ def grouped_gemm(cfg: Config, groups, n_out, k_dim, rows, a, a_scales, expert_of
                                   _ptr(a_scales), _ptr(expert_offsets), _ptr(w), _ptr(w_scales),
                                   _ptr(c), c_dtype, _ptr(status), _stream(stream)),
            "moe_grouped_gemm")
+
+
+def grouped_gemm_swiglu(cfg: Config, groups, inter, k_dim, rows, a, a_scales, expert_offsets,
+                        w13, w13_scales, h, h_scales, status=None, stream=None):
+    _check(lib().moe_grouped_gemm_swiglu(ctypes.byref(cfg), groups, inter, k_dim, rows, _ptr(a),
+                                         _ptr(a_scales), _ptr(expert_offsets), _ptr(w13),
+                                         _ptr(w13_scales), _ptr(h), _ptr(h_scales), _ptr(status),
+                                         _stream(stream)), "moe_grouped_gemm_swiglu")
 
 
 def combine(cfg: Config, T, y, row_of_slot, topk_w, expert_offsets, out, out_dtype, stream=None):

@@ -51,6 +51,14 @@ namespace {
 
 bool al16(const void *p) { return p == nullptr || aligned16(p); }
 
+// Groups averaging 16 rows or more: the gate/up GEMM with 64-row tiles and a
+// separate SiLU-mul kernel beats the fused SwiGLU epilogue (whose two fp32
+// accumulators keep it at 32-row tiles); decode batches take the fused path.
+bool wide_rows(const moe_config *cfg, int64_t T) {
+    return cfg->dtype == MOE_DTYPE_FP8_BLOCK128 &&
+           total_rows(cfg, T) >= 16 * (int64_t)groups_of(cfg);
+}
+
 int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
     const int64_t E = cfg->num_experts, k = cfg->top_k, H = cfg->hidden, I = cfg->inter;
     const int64_t G = groups_of(cfg), Rt = total_rows(cfg, Tm);
@@ -73,7 +81,9 @@ int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
     L->perm_scratch = take((int64_t)permute_scratch_bytes(cfg, (int)Tm));
     L->xp = take(Rt * H * (fp8 ? 1 : 2));
     L->xp_scales = take(fp8 ? 4 * Rt * (H / 128) : 0);
-    L->gate_up = take(4 * Rt * 2 * I);
+    // fp32 gate/up rows exist only for batches wide enough to take the
+    // two-kernel path (see moe_layer_forward)
+    L->gate_up = take(wide_rows(cfg, Tm) ? 4 * Rt * 2 * I : 0);
     L->h = take(Rt * I * (fp8 ? 1 : 2));
     L->h_scales = take(fp8 ? 4 * Rt * (I / 128) : 0);
     L->y = take(4 * Rt * H);
@@ -179,6 +189,28 @@ int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32
                                w_scales, c, c_dtype, dev_status, static_cast<cudaStream_t>(stream));
 }
 
+int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter, int32_t k_dim,
+                            int32_t rows, const void *a, const float *a_scales,
+                            const int32_t *expert_offsets, const void *w13,
+                            const float *w13_scales, void *h, float *h_scales,
+                            int32_t *dev_status, void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    if (groups <= 0 || rows < 0 || inter <= 0 || k_dim <= 0) return MOE_ERR_INVALID_ARG;
+    if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (inter % 128 || k_dim % (fp8 ? 128 : 64)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (fp8 && k_dim > 7168) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)groups * 2 * inter > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!a || !w13 || !h || !expert_offsets || (fp8 && (!a_scales || !w13_scales || !h_scales)))
+        return MOE_ERR_INVALID_ARG;
+    if (!al16(a) || !al16(w13) || !al16(h)) return MOE_ERR_INVALID_ARG;
+    return launch_grouped_gemm_swiglu(fp8, groups, inter, k_dim, rows, a, a_scales,
+                                      expert_offsets, w13, w13_scales, h, h_scales, dev_status,
+                                      static_cast<cudaStream_t>(stream));
+}
+
 int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
                 const float *topk_w, const int32_t *expert_offsets, void *out, int32_t out_dtype,
                 void *stream) {
@@ -211,8 +243,10 @@ int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
 int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
     if (check_config(cfg) || T <= 0) return 0;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
-    // route, (quantise x), permute, gemm, act, gemm, combine
-    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count() + 1 + 1 + 1 + 1;
+    // route, (quantise x), permute, gate/up GEMM with SwiGLU (or GEMM + SiLU-mul
+    // for wide batches), down GEMM, combine
+    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count() +
+           (wide_rows(cfg, T) ? 2 : 1) + 1 + 1;
 }
 
 int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, const void *x,
@@ -265,12 +299,19 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
                         reinterpret_cast<float *>(base + L.xp_scales), base + L.perm_scratch,
                         status, s);
     if (rc) return rc;
-    rc = launch_grouped_gemm(fp8, G, 2 * I, H, rows, base + L.xp,
-                             reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
-                             w->w13_scales, base + L.gate_up, MOE_OUT_F32, status, s);
-    if (rc) return rc;
-    rc = launch_act_requant(cfg, MOE_ACT_SILU_MUL, rows, offsets + G, base + L.gate_up,
-                            base + L.h, reinterpret_cast<float *>(base + L.h_scales), s);
+    if (wide_rows(cfg, T)) {
+        rc = launch_grouped_gemm(fp8, G, 2 * I, H, rows, base + L.xp,
+                                 reinterpret_cast<const float *>(base + L.xp_scales), offsets,
+                                 w->w13, w->w13_scales, base + L.gate_up, MOE_OUT_F32, status, s);
+        if (rc) return rc;
+        rc = launch_act_requant(cfg, MOE_ACT_SILU_MUL, rows, offsets + G, base + L.gate_up,
+                                base + L.h, reinterpret_cast<float *>(base + L.h_scales), s);
+    } else {
+        rc = launch_grouped_gemm_swiglu(fp8, G, I, H, rows, base + L.xp,
+                                        reinterpret_cast<const float *>(base + L.xp_scales),
+                                        offsets, w->w13, w->w13_scales, base + L.h,
+                                        reinterpret_cast<float *>(base + L.h_scales), status, s);
+    }
     if (rc) return rc;
     rc = launch_grouped_gemm(fp8, G, H, I, rows, base + L.h,
                              reinterpret_cast<const float *>(base + L.h_scales), offsets, w->w2,

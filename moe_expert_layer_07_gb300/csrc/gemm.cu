@@ -34,6 +34,7 @@
 // and MMAs, frees its tensor memory and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -54,21 +55,28 @@ constexpr int kCtasPerSm = 2;
 constexpr int kBoxRows = 16;   // activation rows per TMA box
 constexpr int kMaxKBlocks = 56; // FP8: K <= 7168
 
-template <bool FP8, int BN, int STAGES>
+// SW (SwiGLU epilogue): a tile covers 128 gate rows and the matching 128 up
+// rows of W13 (two A tiles per stage sharing one activation tile) and writes
+// h = silu(gate) * up instead of C.
+template <bool FP8, int BN, int STAGES, bool SW>
 struct GemmShape {
-    static constexpr int kABytes = kBM * 128;
+    static constexpr int kNA = SW ? 2 : 1;               // weight tiles per stage
+    static constexpr int kABytes = kBM * 128;            // one weight tile
     static constexpr int kBBytes = BN * 128;
-    static constexpr int kStageBytes = kABytes + kBBytes;
+    static constexpr int kStageBytes = kNA * kABytes + kBBytes;
     static constexpr int kSmemBytes = STAGES * kStageBytes + 1024;
     static constexpr int kAccBufs = 4;                   // TMEM accumulators in flight
-    static constexpr int kTmemCols = kAccBufs * BN;
+    static constexpr int kAccCols = kNA * BN;
+    static constexpr int kTmemCols = kAccBufs * kAccCols;
     static constexpr int kKPerStage = FP8 ? 128 : 64;   // elements of K per stage
     static constexpr int kXsElems = FP8 ? BN * kMaxKBlocks : 1;
-    static constexpr int kWsElems = FP8 ? kMaxKBlocks : 1;
+    static constexpr int kWsElems = FP8 ? kNA * kMaxKBlocks : 1;
+    static constexpr int kAmaxElems = (SW && FP8) ? 4 * BN : 1;
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 64, "BN");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols * kCtasPerSm <= 512,
                   "TMEM columns");
-    static_assert((kSmemBytes + 8 * kXsElems + 8 * kWsElems + 8 * 1024 + 1024) * kCtasPerSm <=
+    static_assert((kSmemBytes + 8 * kXsElems + 8 * kWsElems + 8 * kAmaxElems + 8 * 1024 + 1024) *
+                          kCtasPerSm <=
                       228 * 1024,
                   "shared memory");
 };
@@ -78,10 +86,15 @@ struct GemmArgs {
     const int32_t *offsets;
     const float *a_scales;
     const float *w_scales;
-    void *c;
+    void *c;          // C [rows, n_out]; SwiGLU: h [rows, n_out/2] (e4m3 or bf16)
+    float *h_scales;  // SwiGLU + FP8: [rows, n_out/256]
     int c_bf16;
     int32_t *status;
 };
+
+__device__ __forceinline__ float silu_mul(float g, float u) {
+    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
+}
 
 struct Tile {
     int g, mt, row0, nvalid;
@@ -107,11 +120,11 @@ __device__ __forceinline__ Tile decode_tile(int t, int G, const int *s_tiles, co
     return tl;
 }
 
-template <bool FP8, int BN, int STAGES>
+template <bool FP8, int BN, int STAGES, bool SW>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmA, const GemmArgs args) {
-    using S = GemmShape<FP8, BN, STAGES>;
+    using S = GemmShape<FP8, BN, STAGES, SW>;
     constexpr int NB = S::kAccBufs;
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -120,6 +133,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __shared__ __align__(8) uint64_t acc_empty[NB];
     __shared__ __align__(8) uint64_t scale_full[2];
     __shared__ __align__(8) uint64_t scale_empty[2];
+    __shared__ __align__(8) uint64_t amax_bar[2];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_abort, s_bad;
@@ -130,12 +144,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // out [kb][n] so that lanes read consecutive words.
     __shared__ float s_ws[2][S::kWsElems];
     __shared__ float s_xs[2][S::kXsElems];
+    // SwiGLU + FP8: per tile, each epilogue warp's |h| maximum of every row n
+    __shared__ float s_amax[2][S::kAmaxElems];
 
     using namespace ptx;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t smem_base = (smem_u32(dsmem) + 1023u) & ~1023u;
     const int G = args.groups;
-    const int MT = args.n_out / kBM;
+    const int MTW = args.n_out / kBM;            // 128-row blocks of W per group
+    const int MT = SW ? MTW / 2 : MTW;           // weight tiles per group
     const int KB = args.k_dim / S::kKPerStage;
     volatile int *abort_flag = &s_abort;
 
@@ -151,6 +168,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(&scale_full[b]), 128);   // every epilogue thread's copies
             mbar_init(smem_u32(&scale_empty[b]), 4);    // every epilogue warp done reading
+            mbar_init(smem_u32(&amax_bar[b]), 4);       // every epilogue warp's row maxima
         }
         mbar_init(smem_u32(&drain_bar), 1);
         s_abort = 0;
@@ -220,8 +238,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
                 const int nbox = (tl.nvalid + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = S::kABytes + nbox * kBoxRows * 128;
-                const int wrow = tl.g * args.n_out + tl.mt * kBM;
+                const uint32_t bytes = S::kNA * S::kABytes + nbox * kBoxRows * 128;
+                const int wrow = tl.g * args.n_out + tl.mt * kBM;   // SwiGLU: gate rows
+                const int wrow_up = wrow + args.n_out / 2;          // SwiGLU: up rows
                 const uint64_t pol_w =
                     (s_off[tl.g + 1] - s_off[tl.g] > BN) ? pol_w_shared : pol_w_once;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -231,10 +250,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         break;
                     }
                     const uint32_t sa = smem_base + stage * S::kStageBytes;
-                    const uint32_t sb = sa + S::kABytes;
+                    const uint32_t sb = sa + S::kNA * S::kABytes;
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     tma_load_2d(sa, &tmW, kb * S::kKPerStage, wrow, fb, pol_w);
+                    if (SW) tma_load_2d(sa + S::kABytes, &tmW, kb * S::kKPerStage, wrow_up, fb, pol_w);
                     for (int b = 0; b < nbox; ++b)
                         tma_load_2d(sb + b * kBoxRows * 128, &tmA, kb * S::kKPerStage,
                                     tl.row0 + b * kBoxRows, fb, pol_a);
@@ -280,13 +300,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     tc_fence_after();
                     const uint32_t sa = smem_base + stage * S::kStageBytes;
                     const uint64_t da = sdesc_k_sw128(sa);
-                    const uint64_t db = sdesc_k_sw128(sa + S::kABytes);
-                    const uint32_t d = tmem_base + (uint32_t)(ab * BN);
+                    const uint64_t da_up = sdesc_k_sw128(sa + S::kABytes);
+                    const uint64_t db = sdesc_k_sw128(sa + S::kNA * S::kABytes);
+                    const uint32_t d = tmem_base + (uint32_t)(ab * S::kAccCols);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K
                         const uint32_t acc = FP8 ? (kk > 0) : (kb > 0 || kk > 0);
                         if (FP8) mma_f8f6f4(d, da + 2 * kk, db + 2 * kk, idesc, acc);
                         else mma_f16(d, da + 2 * kk, db + 2 * kk, idesc, acc);
+                        if (SW) {   // up rows into the next BN columns
+                            if (FP8) mma_f8f6f4(d + BN, da_up + 2 * kk, db + 2 * kk, idesc, acc);
+                            else mma_f16(d + BN, da_up + 2 * kk, db + 2 * kk, idesc, acc);
+                        }
                     }
                     mma_commit(smem_u32(&empty_bar[stage]));
                     if (FP8 || kb == KB - 1) {
@@ -313,6 +338,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int etid = threadIdx.x - 64;         // 0..127
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         const int m_local = q * 32 + lane;
+        const int n_h = args.n_out / 2;            // SwiGLU: width of h
         int ab = 0;
         uint32_t aphase = 0;
         bool ok = true;
@@ -321,9 +347,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // buffer's scale_full barrier completes when all 128 threads' copies land.
         auto stage_scales = [&](int t, int b) {
             const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
-            const float *wsp = args.w_scales + ((size_t)tl.g * MT + tl.mt) * KB;
+            const float *wsp = args.w_scales + ((size_t)tl.g * MTW + tl.mt) * KB;
             const float *xsp = args.a_scales + (size_t)tl.row0 * KB;
             for (int i = etid; i < KB; i += 128) cp_async4(smem_u32(&s_ws[b][i]), wsp + i);
+            if (SW) {   // up rows' block scales
+                const float *wup = wsp + (size_t)(MTW / 2) * KB;
+                for (int i = etid; i < KB; i += 128) cp_async4(smem_u32(&s_ws[b][KB + i]), wup + i);
+            }
             const int n_el = tl.nvalid * KB;
             for (int i = etid; i < n_el; i += 128) {
                 const int n = i / KB, kb = i - n * KB;
@@ -359,28 +389,62 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     break;
                 }
                 float acc[BN];
+                float accu[SW ? BN : 1];
 #pragma unroll
                 for (int n = 0; n < BN; ++n) acc[n] = 0.0f;
+#pragma unroll
+                for (int n = 0; n < (SW ? BN : 1); ++n) accu[n] = 0.0f;
                 for (int kb = 0; kb < KB; ++kb) {
                     const float sw = s_ws[b][kb];
-                    float sx[BN / 32];
+                    const float swu = SW ? s_ws[b][KB + kb] : 0.0f;
+                    float xs[BN / 32];
 #pragma unroll
                     for (int h = 0; h < BN / 32; ++h)
-                        sx[h] = (h * 32 + lane < tl.nvalid) ? s_xs[b][kb * BN + h * 32 + lane] * sw
-                                                            : 0.0f;
+                        xs[h] = (h * 32 + lane < tl.nvalid) ? s_xs[b][kb * BN + h * 32 + lane] : 0.0f;
                     if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
                                       MOE_DEV_TIMEOUT)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const uint32_t col = (uint32_t)(ab * S::kAccCols);
                     uint32_t v[BN / 16][16];
 #pragma unroll
                     for (int c = 0; c < BN / 16; ++c)
-                        if (c < nchunks) tmem_ld16(lane_base + (uint32_t)(ab * BN + c * 16), v[c]);
+                        if (c < nchunks) tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
 #pragma unroll
                     for (int c = 0; c < BN / 16; ++c)
                         if (c < nchunks) tmem_wait_ld(v[c]);
+#pragma unroll
+                    for (int c = 0; c < BN / 16; ++c)
+                        if (c < nchunks) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) {
+                                const int n = c * 16 + j;
+                                const float sx = __fmul_rn(__shfl_sync(0xffffffffu, xs[n / 32], n & 31), sw);
+                                acc[n] = fmaf(__uint_as_float(v[c][j]), sx, acc[n]);
+                            }
+                        }
+                    if (SW) {   // up rows: same activation scales, their own block scale
+#pragma unroll
+                        for (int c = 0; c < BN / 16; ++c)
+                            if (c < nchunks)
+                                tmem_ld16(lane_base + col + (uint32_t)(BN + c * 16), v[c]);
+#pragma unroll
+                        for (int c = 0; c < BN / 16; ++c)
+                            if (c < nchunks) tmem_wait_ld(v[c]);
+#pragma unroll
+                        for (int c = 0; c < BN / 16; ++c)
+                            if (c < nchunks) {
+#pragma unroll
+                                for (int j = 0; j < 16; ++j) {
+                                    const int n = c * 16 + j;
+                                    const float sx =
+                                        __fmul_rn(__shfl_sync(0xffffffffu, xs[n / 32], n & 31), swu);
+                                    accu[SW ? n : 0] = fmaf(__uint_as_float(v[c][j]), sx, accu[SW ? n : 0]);
+                                }
+                            }
+                    }
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
@@ -388,21 +452,48 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         ab = 0;
                         aphase ^= 1u;
                     }
-#pragma unroll
-                    for (int c = 0; c < BN / 16; ++c)
-                        if (c < nchunks) {
-#pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int n = c * 16 + j;
-                                const float scale = __shfl_sync(0xffffffffu, sx[n / 32], n & 31);
-                                acc[n] = fmaf(__uint_as_float(v[c][j]), scale, acc[n]);
-                            }
-                        }
                 }
                 if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&scale_empty[b]));
-                if (args.c_bf16) {
+                if (SW) {
+                    // h = silu(gate) * up; each row n is quantised over the
+                    // tile's 128 features (one per thread): warp maxima, then
+                    // the four warps' maxima through shared memory.
+#pragma unroll
+                    for (int n = 0; n < BN; ++n) acc[n] = silu_mul(acc[n], accu[SW ? n : 0]);
+                    float mine = 0.0f;
+#pragma unroll
+                    for (int n = 0; n < BN; ++n) {
+                        float m = fabsf(acc[n]);
+#pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if ((n & 31) == lane) mine = m;
+                        if ((n & 31) == 31 || n == BN - 1) {   // lanes hold rows [n & ~31, ...)
+                            const int base = n & ~31;
+                            if (lane <= n - base) s_amax[b][q * BN + base + lane] = mine;
+                        }
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&amax_bar[b]));
+                    if (!wait_bounded(smem_u32(&amax_bar[b]), ((uint32_t)it >> 1) & 1u, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *H8 = static_cast<uint8_t *>(args.c);
+#pragma unroll
+                    for (int n = 0; n < BN; ++n)
+                        if (n < tl.nvalid) {
+                            const float amax = fmaxf(fmaxf(s_amax[b][n], s_amax[b][BN + n]),
+                                                     fmaxf(s_amax[b][2 * BN + n], s_amax[b][3 * BN + n]));
+                            const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+                            const size_t row = (size_t)(tl.row0 + n);
+                            H8[row * n_h + tl.mt * kBM + m_local] = (uint8_t)__nv_cvt_float_to_fp8(
+                                __fdiv_rn(acc[n], sc), __NV_SATFINITE, __NV_E4M3);
+                            if (m_local == 0) args.h_scales[row * (n_h / 128) + tl.mt] = sc;
+                        }
+                } else if (args.c_bf16) {
                     __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(args.c);
 #pragma unroll
                     for (int n = 0; n < BN; ++n)
@@ -421,22 +512,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     break;
                 }
                 tc_fence_after();
+                const uint32_t col = (uint32_t)(ab * S::kAccCols);
 #pragma unroll
                 for (int c = 0; c < BN / 16; ++c)
                     if (c < nchunks) {
-                        uint32_t v[16];
-                        tmem_ld16(lane_base + (uint32_t)(ab * BN + c * 16), v);
+                        uint32_t v[16], vu[16];
+                        tmem_ld16(lane_base + col + (uint32_t)(c * 16), v);
                         tmem_wait_ld(v);
+                        if (SW) {
+                            tmem_ld16(lane_base + col + (uint32_t)(BN + c * 16), vu);
+                            tmem_wait_ld(vu);
+                        }
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const int n = c * 16 + j;
                             if (n < tl.nvalid) {
-                                const size_t idx = (size_t)(tl.row0 + n) * args.n_out + m_glob;
-                                if (args.c_bf16)
-                                    static_cast<__nv_bfloat16 *>(args.c)[idx] =
-                                        __float2bfloat16_rn(__uint_as_float(v[j]));
-                                else
-                                    static_cast<float *>(args.c)[idx] = __uint_as_float(v[j]);
+                                if (SW) {
+                                    const size_t idx = (size_t)(tl.row0 + n) * n_h + tl.mt * kBM + m_local;
+                                    static_cast<__nv_bfloat16 *>(args.c)[idx] = __float2bfloat16_rn(
+                                        silu_mul(__uint_as_float(v[j]), __uint_as_float(vu[j])));
+                                } else {
+                                    const size_t idx = (size_t)(tl.row0 + n) * args.n_out + m_glob;
+                                    if (args.c_bf16)
+                                        static_cast<__nv_bfloat16 *>(args.c)[idx] =
+                                            __float2bfloat16_rn(__uint_as_float(v[j]));
+                                    else
+                                        static_cast<float *>(args.c)[idx] = __uint_as_float(v[j]);
+                                }
                             }
                         }
                     }
@@ -493,10 +595,10 @@ bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint6
     return r == CUDA_SUCCESS;
 }
 
-template <bool FP8, int BN, int STAGES>
+template <bool FP8, int BN, int STAGES, bool SW = false>
 int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t s) {
-    using Sh = GemmShape<FP8, BN, STAGES>;
-    auto kern = grouped_gemm_kernel<FP8, BN, STAGES>;
+    using Sh = GemmShape<FP8, BN, STAGES, SW>;
+    auto kern = grouped_gemm_kernel<FP8, BN, STAGES, SW>;
     static std::once_flag attr_once[64];
     static int attr_rc[64];
     int dev = 0;
@@ -515,7 +617,7 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
     if (!encode_2d(&tmA, a, FP8, (uint64_t)args.k_dim, (uint64_t)args.rows, kBoxRows))
         return MOE_ERR_CUDA;
     const int64_t tiles_bound =
-        (int64_t)(args.n_out / kBM) * (args.groups + ceil_div(args.rows, BN));
+        (int64_t)(args.n_out / kBM / (SW ? 2 : 1)) * (args.groups + ceil_div(args.rows, BN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, tiles_bound);
     if (grid <= 0) return MOE_OK;
     kern<<<grid, kThreads, Sh::kSmemBytes, s>>>(tmW, tmA, args);
@@ -539,6 +641,7 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     args.a_scales = a_scales;
     args.w_scales = w_scales;
     args.c = c;
+    args.h_scales = nullptr;
     args.c_bf16 = c_dtype == MOE_OUT_BF16;
     args.status = status;
     // Decode-sized groups (a few rows each) stream best with 32-row tiles;
@@ -547,6 +650,27 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     if (fp8) return wide ? launch_impl<true, 64, 3>(args, a, w, s)
                          : launch_impl<true, 32, 4>(args, a, w, s);
     return launch_impl<false, 32, 4>(args, a, w, s);
+}
+
+int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int rows,
+                               const void *a, const float *a_scales, const int32_t *offsets,
+                               const void *w13, const float *w13_scales, void *h,
+                               float *h_scales, int32_t *status, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    GemmArgs args;
+    args.groups = groups;
+    args.n_out = 2 * inter;
+    args.k_dim = k_dim;
+    args.rows = rows;
+    args.offsets = offsets;
+    args.a_scales = a_scales;
+    args.w_scales = w13_scales;
+    args.c = h;
+    args.h_scales = h_scales;
+    args.c_bf16 = !fp8;
+    args.status = status;
+    if (fp8) return launch_impl<true, 32, 2, true>(args, a, w13, s);
+    return launch_impl<false, 32, 2, true>(args, a, w13, s);
 }
 
 }  // namespace moe

@@ -44,6 +44,10 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
                         const float *a_scales, const int32_t *offsets, const void *w,
                         const float *w_scales, void *c, int c_dtype, int32_t *status,
                         cudaStream_t s);
+int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int rows,
+                               const void *a, const float *a_scales, const int32_t *offsets,
+                               const void *w13, const float *w13_scales, void *h,
+                               float *h_scales, int32_t *status, cudaStream_t s);
 int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *row_of_slot,
                    const float *topk_w, const int32_t *offsets, void *out, int out_dtype,
                    cudaStream_t s);

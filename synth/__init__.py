@@ -96,7 +96,13 @@ CONFIGS = {
                           num_experts=8, num_shared=2, top_k=3,
                           scoring="softmax", norm_topk=True),
     # R1 hidden/intermediate sizes with 32 experts: a few GB on the device,
-    # the case kernel profiles are captured on.
+    # the cases kernel profiles are captured on (16 tokens: decode-sized
+    # groups of a few rows, as in the 128-token, 256-expert layer).
+    "r1_e32_t16": MoEShape("r1_e32_t16", tokens=16, hidden=7168, inter=2048,
+                           num_experts=32, num_shared=1, top_k=8, num_groups=8,
+                           topk_groups=4, group_topn=2, scoring="sigmoid",
+                           norm_topk=True, routed_scaling=2.5, dtype="fp8",
+                           bias_std=0.01),
     "r1_e32_t128": MoEShape("r1_e32_t128", tokens=128, hidden=7168, inter=2048,
                             num_experts=32, num_shared=1, top_k=8, num_groups=8,
                             topk_groups=4, group_topn=2, scoring="sigmoid",

@@ -459,3 +459,52 @@ def test_bounded_wait_reports_timeout_and_context_survives(lib):
     wl = workload("bf16_mini")
     _, out = run_layer(wl)
     check_close(to_np(out), oracle_layer(wl)["out"], BF16_TOL)
+
+
+@pytest.mark.parametrize("fp8,inter,K,counts", [
+    (True, 384, 1024, GEMM_ROWS), (True, 2048, 7168, [3, 0, 17, 40, 128, 1]),
+    (False, 384, 512, GEMM_ROWS)])
+def test_swiglu_epilogue_equals_gemm_then_silu_requant(lib, fp8, inter, K, counts):
+    """The fused gate/up + SwiGLU kernel gives the bits of the two-kernel path."""
+    s = synth.CONFIGS["r1_mini" if fp8 else "bf16_mini"]
+    cfg = moe.make_config(s)
+    counts = np.array(counts)
+    G = len(counts)
+    off_np = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    rows = int(off_np[-1])
+    off = torch.as_tensor(off_np, device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(9)
+    a32 = torch.randn(rows, K, device="cuda", generator=g)
+    w32 = torch.randn(G, 2 * inter, K, device="cuda", generator=g) * 0.05
+    if fp8:
+        a = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+        asc = torch.empty((rows, K // 128), device="cuda")
+        cfg_q = moe.make_config(synth.MoEShape("q", rows, K, 128, 1, 0, 1, dtype="fp8"))
+        moe.act_requant(cfg_q, moe.ACT_IDENTITY, rows, a32.to(torch.bfloat16), a, asc)
+        w, wsc = synth.block_quantize_e4m3(w32)
+        h_ref = torch.empty((rows, inter), dtype=torch.uint8, device="cuda")
+        hs_ref = torch.empty((rows, inter // 128), device="cuda")
+        h = torch.full_like(h_ref, 0x55)
+        hs = torch.full_like(hs_ref, -1.0)
+    else:
+        a, asc = a32.to(torch.bfloat16), None
+        w, wsc = w32.to(torch.bfloat16), None
+        h_ref = torch.empty((rows, inter), dtype=torch.bfloat16, device="cuda")
+        h = torch.zeros_like(h_ref)
+        hs_ref = hs = None
+    cfg_i = moe.make_config(dataclasses_replace(s, inter=inter, hidden=K))
+    gu = torch.empty((rows, 2 * inter), device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.grouped_gemm(cfg, G, 2 * inter, K, rows, a, asc, off, w, wsc, gu, moe.OUT_F32, st)
+    moe.act_requant(cfg_i, moe.ACT_SILU_MUL, rows, gu, h_ref, hs_ref)
+    moe.grouped_gemm_swiglu(cfg, G, inter, K, rows, a, asc, off, w, wsc, h, hs, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(h, h_ref)
+    if fp8:
+        assert torch.equal(hs, hs_ref)
+
+
+def dataclasses_replace(shape, **kw):
+    import dataclasses
+    return dataclasses.replace(shape, **kw)
