@@ -162,30 +162,44 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i) {
     }
 }
 
-// One warp (one CTA) per token: the fp64 sigmoid runs on the SMs' narrow
-// FP64 pipes, so tokens are spread over as many SMs as possible.
-template <int PL>   // experts per lane: expert e = q*32 + lane, q < PL
-__global__ void __launch_bounds__(32) route_select_kernel(const SelectArgs a) {
+// One CTA per token. The fp64 sigmoid runs on the SMs' narrow FP64 pipes, so
+// all four warps of the CTA (one per SM sub-partition) evaluate the scores
+// into shared memory; warp 0 then does the selection alone, holding expert
+// e = q*32 + lane in its registers.
+constexpr int kSelThreads = 128;
+
+template <int PL>   // experts per lane of warp 0: e = q*32 + lane, q < PL
+__global__ void __launch_bounds__(kSelThreads) route_select_kernel(const SelectArgs a) {
+    __shared__ float sh_l[PL * 32], sh_s[PL * 32], sh_sel[PL * 32];
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x;
-    if (t >= a.T) return;   // warp-uniform
+    if (t >= a.T) return;   // block-uniform
     const float *lrow = a.logits + (size_t)t * a.E;
+
+    for (int e = threadIdx.x; e < PL * 32; e += kSelThreads) {
+        const bool ok = e < a.E;
+        const float lv = ok ? lrow[e] : 0.0f;
+        float sv = lv, selv = lv;
+        if (a.sigmoid) {
+            sv = (float)(1.0 / (1.0 + exp(-(double)lv)));
+            selv = (ok && a.bias) ? __fadd_rn(sv, a.bias[e]) : sv;
+        }
+        sh_l[e] = lv;
+        sh_s[e] = sv;
+        sh_sel[e] = selv;
+    }
+    __syncthreads();
+    if (threadIdx.x >= 32) return;   // warp-uniform
 
     float l[PL], s[PL], sel[PL];
     uint32_t valid = 0;
 #pragma unroll
     for (int q = 0; q < PL; ++q) {
         const int e = q * 32 + lane;
-        const bool ok = e < a.E;
-        l[q] = ok ? lrow[e] : 0.0f;
-        if (a.sigmoid) {
-            s[q] = (float)(1.0 / (1.0 + exp(-(double)l[q])));
-            sel[q] = (ok && a.bias) ? __fadd_rn(s[q], a.bias[e]) : s[q];
-        } else {
-            s[q] = l[q];
-            sel[q] = l[q];
-        }
-        if (ok) valid |= 1u << q;
+        l[q] = sh_l[e];
+        s[q] = sh_s[e];
+        sel[q] = sh_sel[e];
+        if (e < a.E) valid |= 1u << q;
     }
     uint32_t allowed = valid;
 
@@ -353,7 +367,7 @@ __global__ void __launch_bounds__(32) route_select_kernel(const SelectArgs a) {
 
 template <int PL>
 void launch_select(const SelectArgs &a, cudaStream_t s) {
-    route_select_kernel<PL><<<a.T, 32, 0, s>>>(a);
+    route_select_kernel<PL><<<a.T, kSelThreads, 0, s>>>(a);
 }
 
 }  // namespace
