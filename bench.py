@@ -141,7 +141,8 @@ def setup(shape, seed, device):
 class Stepper:
     """The hot path as its C-ABI steps on one stream, CUDA events around each."""
 
-    NAMES = ["route", "quant_x", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
+    NAMES_FUSED = ["route", "quant_x", "permute", "expert_ffn", "combine"]
+    NAMES_SPLIT = ["route", "quant_x", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
 
     def __init__(self, layer, x, out):
         import torch
@@ -155,10 +156,13 @@ class Stepper:
         self.p = {n: base + getattr(L, n) for n in
                   ("status", "logits", "topk_ids", "topk_w", "xq", "xs", "expert_offsets",
                    "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "gate_up",
-                   "h", "h_scales", "y")}
+                   "h", "h_scales", "y", "ffn_sched")}
         self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
         rows = s.tokens * (s.top_k + s.num_shared)
         self.wide = self.fp8 and rows >= 16 * s.groups   # as moe_layer_forward decides
+        self.fused = self.fp8 and not self.wide and s.inter % 256 == 0
+        self.NAMES = self.NAMES_FUSED if self.fused else self.NAMES_SPLIT
+        self.sched_bytes = moe.expert_ffn_sched_bytes(s.groups, rows)
         ws[L.status:L.status + 4].zero_()   # the device status word starts clear
         self.k = {}
         self.events = []
@@ -188,6 +192,17 @@ class Stepper:
                     p["row_of_slot"], p["xp"], p["xp_scales"] if self.fp8 else None,
                     p["perm_scratch"], self.perm_bytes, p["status"])
         mark()
+        if self.fused:   # decode batches: both expert GEMMs in one persistent kernel
+            moe.expert_ffn(cfg, G, rows, p["xp"], p["xp_scales"], p["expert_offsets"], w["w13"],
+                           w["w13_s"], w["w2"], w["w2_s"], p["h"], p["h_scales"], p["y"],
+                           p["ffn_sched"], self.sched_bytes, p["status"])
+            mark()
+            moe.combine(cfg, T, p["y"], p["row_of_slot"], p["topk_w"], p["expert_offsets"],
+                        self.out, moe.OUT_F32)
+            mark()
+            if record:
+                self.events.append(ev)
+            return
         if self.wide:   # the layer's two-kernel path for wide batches
             moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"], p["expert_offsets"],
                              w["w13"], w.get("w13_s"), p["gate_up"], moe.OUT_F32, p["status"])
@@ -241,6 +256,8 @@ def algorithmic_bytes(shape, offsets):
     b["gemm_gate_up_swiglu"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i) + \
         (2 * rows * 2 * I * 4 if wide else 0)
     b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4
+    if fp8 and not wide and I % 256 == 0:   # one kernel holds both GEMMs
+        b["expert_ffn"] = b.pop("gemm_gate_up_swiglu") + b.pop("gemm_down")
     b["combine"] = T * (k + S) * H * 4 + 8 * T * k + T * H * 4
     flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)
     return b, active, flops
@@ -344,14 +361,16 @@ def main():
 
     hbm_peak, bf16_peak, peak_src = load_peaks()
     layer_bytes = sum(bytes_per.values())
-    gu_ms = kms["gemm_gate_up_swiglu"]
-    achieved = bytes_per["gemm_gate_up_swiglu"] / (gu_ms / 1e3) / 1e9
+    top = "expert_ffn" if stepper.fused else "gemm_gate_up_swiglu"
+    top_label = ("expert_ffn (gate/up + SwiGLU + down, one kernel)" if stepper.fused
+                 else "grouped_gemm gate/up + SwiGLU")
+    achieved = bytes_per[top] / (kms[top] / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168 and \
             not stepper.wide:
         with open(tpath) as f:
-            tr = json.load(f).get("gemm_gate_up_swiglu")
+            tr = json.load(f).get(top)
         if tr:   # ncu DRAM bytes per active group (small R1 case) x this launch's groups
             traffic = tr["bytes_per_active_group"] * active
 
@@ -381,7 +400,7 @@ def main():
         "layer_roofline_frac": (layer_bytes / (hbm_peak * 1e9)) / (ms_step / 1e3),
         "active_experts": active,
         "kernels_ms": {k: round(v, 5) for k, v in kms.items()},
-        "roofline": {"bound": "hbm", "kernel": "grouped_gemm gate/up + SwiGLU", "achieved": achieved,
+        "roofline": {"bound": "hbm", "kernel": top_label, "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)"},
         "tensor_pipe_frac_of_bf16x2": (flops / (ms_step / 1e3)) / (2 * bf16_peak * 1e12),

@@ -229,6 +229,36 @@ MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32
                                     const void *w13, const float *w13_scales, void *h,
                                     float *h_scales, int32_t *dev_status, void *stream);
 
+/* ---- the experts' FFN in one kernel (FP8 layers) ------------------------------
+ * For the rows r of every group g (offsets as in moe_grouped_gemm):
+ *   g, u = A[r] W13[g]^T     (W13 e4m3 [groups, 2*inter, hidden], block scales
+ *                             w13_scales fp32 [groups, 2*inter/128, hidden/128],
+ *                             A e4m3 [rows, hidden], a_scales fp32 [rows, hidden/128]),
+ *   h    = silu(g) * u, quantised per row and 128-feature group
+ *          -> h e4m3 [rows, inter], h_scales fp32 [rows, inter/128],
+ *   y[r] = h[r] W2[g]^T      (W2 e4m3 [groups, hidden, inter], w2_scales fp32
+ *                             [groups, hidden/128, inter/128]) -> y fp32 [rows, hidden].
+ * The same bits as moe_grouped_gemm_swiglu followed by moe_grouped_gemm
+ * (fp32 C), in one persistent launch: the report's fused MoE kernel
+ * (section "Library optimisation") runs an expert's FFN as one kernel.
+ * CTAs claim the gate/up tiles, then the down tiles, from a counter; a down
+ * tile waits (bounded, about a second, else MOE_DEV_TIMEOUT) until the h
+ * rows of its 32-row activation tile are complete, so no wave of either
+ * GEMM ends with most of the GPU idle.
+ *   sched: device scratch of at least moe_expert_ffn_sched_bytes(groups,
+ *   rows) bytes, owned by the caller, cleared by the call on `stream`; one
+ *   call at a time per buffer (else MOE_ERR_WORKSPACE_TOO_SMALL if short).
+ * cfg supplies hidden and inter; cfg->dtype must be FP8_BLOCK128 and inter a
+ * multiple of 256 (else MOE_ERR_UNSUPPORTED_SHAPE); groups <= 1024; a, w13,
+ * w2, h and y 16-byte aligned. */
+MOE_API size_t moe_expert_ffn_sched_bytes(int32_t groups, int32_t rows);
+MOE_API int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const void *a,
+                           const float *a_scales, const int32_t *expert_offsets,
+                           const void *w13, const float *w13_scales, const void *w2,
+                           const float *w2_scales, void *h, float *h_scales, float *y,
+                           int32_t *sched, size_t sched_bytes, int32_t *dev_status,
+                           void *stream);
+
 /* ---- combine -------------------------------------------------------------------
  * out[t, :] = sum_s Y[expert_offsets[E+s] + t, :]
  *           + sum_j topk_w[t, j] * Y[row_of_slot[t, j], :]    (fp32, shared
@@ -242,13 +272,16 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
                 int32_t out_dtype, void *stream);
 
 /* ---- the whole layer -------------------------------------------------------------
- * route -> (FP8: quantise x) -> permute -> grouped GEMM gate/up with the
- * SwiGLU epilogue (+ FP8 requantisation of h) -> grouped GEMM down (fp32
- * expert outputs) -> combine, all on
- * `stream`; FP8 batches whose groups average 16 rows or more run the
- * gate/up GEMM (64-row tiles, fp32 rows) and SiLU-mul as two kernels
- * instead, with the same result bits; also
- * `stream`, all intermediates inside `ws` (size from moe_workspace_size for
+ * route -> (FP8: quantise x) -> permute -> the experts' FFN -> combine, all
+ * on `stream`.  The experts' FFN is
+ *   FP8, groups averaging fewer than 16 rows (decode), inter % 256 == 0:
+ *     moe_expert_ffn (one persistent kernel);
+ *   FP8, groups averaging 16 rows or more: grouped GEMM gate/up (64-row
+ *     tiles, fp32 rows), SiLU-mul + requantisation, grouped GEMM down;
+ *   otherwise: grouped GEMM gate/up with the SwiGLU epilogue, grouped GEMM
+ *     down;
+ * all with the same result bits (fp32 expert outputs), and
+ * all intermediates inside `ws` (size from moe_workspace_size for
  * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..
  * max_tokens.  The workspace's device status word is cleared at the start
  * of every call; read it with moe_get_device_status after the stream has
@@ -261,7 +294,7 @@ MOE_API int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32
  * callers that want to read routing results or rows per expert. */
 typedef struct moe_ws_layout {
     size_t status, logits, topk_ids, topk_w, xq, xs, expert_offsets, src_of_row,
-        row_of_slot, perm_scratch, xp, xp_scales, gate_up, h, h_scales, y, total;
+        row_of_slot, perm_scratch, xp, xp_scales, gate_up, h, h_scales, y, ffn_sched, total;
 } moe_ws_layout;
 MOE_API int moe_workspace_layout(const moe_config *cfg, moe_ws_layout *layout /* host */);
 

@@ -19,6 +19,7 @@ __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_
            "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
            "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
            "count_coactivation", "affinity_permutation", "grouped_gemm_swiglu",
+           "expert_ffn", "expert_ffn_sched_bytes",
            "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
            "ACT_SILU_MUL"]
 
@@ -52,7 +53,7 @@ class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "logits", "topk_ids", "topk_w", "xq", "xs", "expert_offsets",
                  "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "gate_up",
-                 "h", "h_scales", "y", "total")]
+                 "h", "h_scales", "y", "ffn_sched", "total")]
 
 
 _lib = None
@@ -81,6 +82,8 @@ _SIGS = {
     "expert_affinity_permutation": [_P, _P, _I, _I, ctypes.c_double, _P, _P,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
     "moe_relayout_experts": [_P, _P, _P, _I, ctypes.c_int64, _P, _P],
+    "moe_expert_ffn": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
+                       _P, _P],
 }
 
 
@@ -98,6 +101,8 @@ def lib():
             fn.restype = ctypes.c_int
         L.moe_permute_static_scratch_capacity.argtypes = []
         L.moe_permute_static_scratch_capacity.restype = ctypes.c_size_t
+        L.moe_expert_ffn_sched_bytes.argtypes = [_I, _I]
+        L.moe_expert_ffn_sched_bytes.restype = ctypes.c_size_t
         L.moe_status_string.argtypes = [ctypes.c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
         _lib = L
@@ -194,6 +199,20 @@ def grouped_gemm_swiglu(cfg: Config, groups, inter, k_dim, rows, a, a_scales, ex
                                          _ptr(a_scales), _ptr(expert_offsets), _ptr(w13),
                                          _ptr(w13_scales), _ptr(h), _ptr(h_scales), _ptr(status),
                                          _stream(stream)), "moe_grouped_gemm_swiglu")
+
+
+def expert_ffn_sched_bytes(groups, rows) -> int:
+    """Bytes of the scheduler scratch moe_expert_ffn needs."""
+    return int(lib().moe_expert_ffn_sched_bytes(groups, rows))
+
+
+def expert_ffn(cfg: Config, groups, rows, a, a_scales, expert_offsets, w13, w13_scales, w2,
+               w2_scales, h, h_scales, y, sched, sched_bytes, status=None, stream=None):
+    """Both expert GEMMs with SwiGLU between them, one persistent kernel (FP8)."""
+    _check(lib().moe_expert_ffn(ctypes.byref(cfg), groups, rows, _ptr(a), _ptr(a_scales),
+                                _ptr(expert_offsets), _ptr(w13), _ptr(w13_scales), _ptr(w2),
+                                _ptr(w2_scales), _ptr(h), _ptr(h_scales), _ptr(y), _ptr(sched),
+                                sched_bytes, _ptr(status), _stream(stream)), "moe_expert_ffn")
 
 
 def combine(cfg: Config, T, y, row_of_slot, topk_w, expert_offsets, out, out_dtype, stream=None):

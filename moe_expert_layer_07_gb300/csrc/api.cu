@@ -59,6 +59,12 @@ bool wide_rows(const moe_config *cfg, int64_t T) {
            total_rows(cfg, T) >= 16 * (int64_t)groups_of(cfg);
 }
 
+// FP8 decode batches run both expert GEMMs in one persistent kernel (its
+// down stages hold two 128-wide K blocks, hence inter % 256).
+bool fused_ffn(const moe_config *cfg, int64_t T) {
+    return cfg->dtype == MOE_DTYPE_FP8_BLOCK128 && !wide_rows(cfg, T) && cfg->inter % 256 == 0;
+}
+
 int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
     const int64_t E = cfg->num_experts, k = cfg->top_k, H = cfg->hidden, I = cfg->inter;
     const int64_t G = groups_of(cfg), Rt = total_rows(cfg, Tm);
@@ -70,6 +76,10 @@ int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
         return o;
     };
     L->status = take(4);
+    // the fused FFN's unit counter and per-tile h counters; sits right after
+    // the status word so that one memset clears both
+    L->ffn_sched = take(fp8 && cfg->inter % 256 == 0
+                            ? (int64_t)ffn_sched_bytes((int)G, (int)Rt) : 0);
     L->logits = take(4 * Tm * E);
     L->topk_ids = take(4 * Tm * k);
     L->topk_w = take(4 * Tm * k);
@@ -211,6 +221,34 @@ int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter
                                       static_cast<cudaStream_t>(stream));
 }
 
+size_t moe_expert_ffn_sched_bytes(int32_t groups, int32_t rows) {
+    if (groups <= 0 || rows < 0) return 0;
+    return ffn_sched_bytes(groups, rows);
+}
+
+int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const void *a,
+                   const float *a_scales, const int32_t *expert_offsets, const void *w13,
+                   const float *w13_scales, const void *w2, const float *w2_scales, void *h,
+                   float *h_scales, float *y, int32_t *sched, size_t sched_bytes,
+                   int32_t *dev_status, void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (groups <= 0 || rows < 0) return MOE_ERR_INVALID_ARG;
+    if (cfg->dtype != MOE_DTYPE_FP8_BLOCK128 || cfg->inter % 256 || groups > 1024)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)groups * 2 * cfg->inter > INT32_MAX || (int64_t)groups * cfg->hidden > INT32_MAX)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!a || !a_scales || !expert_offsets || !w13 || !w13_scales || !w2 || !w2_scales || !h ||
+        !h_scales || !y || !sched)
+        return MOE_ERR_INVALID_ARG;
+    if (!al16(a) || !al16(w13) || !al16(w2) || !al16(h) || !al16(y)) return MOE_ERR_INVALID_ARG;
+    if (sched_bytes < ffn_sched_bytes(groups, rows)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return launch_expert_ffn(groups, cfg->hidden, cfg->inter, rows, a, a_scales, expert_offsets,
+                             w13, w13_scales, w2, w2_scales, h, h_scales, y, sched, false,
+                             dev_status, static_cast<cudaStream_t>(stream));
+}
+
 int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
                 const float *topk_w, const int32_t *expert_offsets, void *out, int32_t out_dtype,
                 void *stream) {
@@ -243,10 +281,11 @@ int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
 int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
     if (check_config(cfg) || T <= 0) return 0;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
-    // route, (quantise x), permute, gate/up GEMM with SwiGLU (or GEMM + SiLU-mul
-    // for wide batches), down GEMM, combine
-    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count() +
-           (wide_rows(cfg, T) ? 2 : 1) + 1 + 1;
+    // route, (quantise x), permute, the experts' FFN (one fused kernel; or
+    // gate/up GEMM with SwiGLU + down GEMM; or, for wide batches, GEMM +
+    // SiLU-mul + down GEMM), combine
+    const int ffn = fused_ffn(cfg, T) ? 1 : (wide_rows(cfg, T) ? 3 : 2);
+    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count() + ffn + 1;
 }
 
 int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, const void *x,
@@ -270,11 +309,15 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint8_t *base = static_cast<uint8_t *>(ws);
     int32_t *status = reinterpret_cast<int32_t *>(base + L.status);
-    MOE_CUDA_TRY(cudaMemsetAsync(status, 0, sizeof(int32_t), s));
+    const bool fused = T > 0 && fused_ffn(cfg, T);
+    const int rows = (int)total_rows(cfg, T);
+    // status word (and, for the fused FFN, its scheduler counters) cleared
+    const size_t clear = fused ? L.ffn_sched + ffn_sched_bytes(groups_of(cfg), rows)
+                               : sizeof(int32_t);
+    MOE_CUDA_TRY(cudaMemsetAsync(status, 0, clear, s));
     if (T == 0) return MOE_OK;
 
     const int E = cfg->num_experts, G = groups_of(cfg), H = cfg->hidden, I = cfg->inter;
-    const int rows = (int)total_rows(cfg, T);
     float *logits = reinterpret_cast<float *>(base + L.logits);
     int32_t *ids = reinterpret_cast<int32_t *>(base + L.topk_ids);
     float *tw = reinterpret_cast<float *>(base + L.topk_w);
@@ -299,6 +342,16 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
                         reinterpret_cast<float *>(base + L.xp_scales), base + L.perm_scratch,
                         status, s);
     if (rc) return rc;
+    if (fused) {
+        rc = launch_expert_ffn(G, H, I, rows, base + L.xp,
+                               reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
+                               w->w13_scales, w->w2, w->w2_scales, base + L.h,
+                               reinterpret_cast<float *>(base + L.h_scales),
+                               reinterpret_cast<float *>(base + L.y),
+                               reinterpret_cast<int32_t *>(base + L.ffn_sched), true, status, s);
+        if (rc) return rc;
+        return launch_combine(cfg, T, base + L.y, ros, tw, offsets, out, out_dtype, s);
+    }
     if (wide_rows(cfg, T)) {
         rc = launch_grouped_gemm(fp8, G, 2 * I, H, rows, base + L.xp,
                                  reinterpret_cast<const float *>(base + L.xp_scales), offsets,

@@ -1,0 +1,618 @@
+// The experts' FFN in one persistent kernel (FP8 layers):
+//
+//   for every group g and its rows r:
+//     g, u = Xp[r] W13[g]^T            (gate and up, FP8 128x128 block scales)
+//     h    = silu(g) * u  -> e4m3 + one fp32 scale per 128 features
+//     Y[r] = h W2[g]^T                 (fp32)
+//
+// Moreh report "21K output tokens/s DeepSeek inference on MI300X with Expert
+// Parallelism", section "Library optimisation": its fused MoE kernel runs an
+// expert's FFN as one kernel.  Here one launch holds both grouped GEMMs.
+// The work units are the gate/up tiles (128 gate + 128 up weight rows x 32
+// activation rows, SwiGLU and requantisation in the epilogue, as in the
+// stand-alone SwiGLU GEMM) followed by the down tiles (128 rows of W2 x the
+// same 32 activation rows).  CTAs claim units from a global counter, so a
+// CTA that runs out of gate/up work moves on to down tiles while others
+// finish theirs: the last wave of large gate/up tiles no longer idles most
+// of the GPU, and the two GEMMs need no launch boundary between them.
+//
+// A down tile of (group g, activation tile j) reads h rows that the gate/up
+// tiles of (g, j) write.  Each finished gate/up tile adds one to a per-j
+// counter (release, after a proxy fence); the producer of a down tile waits
+// (bounded) until the counter reaches the number of gate/up tiles of j,
+// then issues its TMA loads of h, and the epilogue threads acquire the same
+// count before they read h's scales.  Every gate/up unit is claimed before any down
+// unit and a producer issues all loads of a unit before it claims the next,
+// so a unit that is waited on is always in some running CTA's pipeline: no
+// wait can be circular.
+//
+// Per CTA (two per SM), 6 warps:
+//   warp 0     scheduler + TMA producer: a 2-deep ring of 40 KB stages; a
+//              gate/up stage holds one 128-wide K block (gate box, up box,
+//              activation rows), a down stage two K blocks (two W2 boxes,
+//              two h boxes).
+//   warp 1     MMA issuer: tcgen05.mma kind::f8f6f4, one TMEM accumulator
+//              per K block (four rotate), tcgen05.commit to mbarriers.
+//   warps 2-5  epilogue: per K block the partial product times
+//              x_scale[r, kb] * w_scale[g, m/128, kb] is added to fp32
+//              registers (thread = weight row, 32 activation rows), then
+//              gate/up: SiLU-mul, row maxima across the four warps, e4m3
+//              codes and scales of h; down: Y rows (fp32).
+// The activation scales are read straight from global memory one K block
+// ahead (the tile's 32 rows x K/128 floats stay in L1), which frees the
+// shared memory that a second stage-sized buffer would need.
+//
+// Every wait is bounded (about a second): on expiry the CTA records
+// MOE_DEV_TIMEOUT, raises its abort flag so that its other warps stop,
+// lets its copies and MMAs drain, frees its tensor memory and exits.
+#include <cuda.h>
+#include <cuda_fp8.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "internal.h"
+#include "numerics.cuh"
+#include "ptx.cuh"
+#include "tma_host.h"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;                // weight rows per tile (MMA M)
+constexpr int kBN = 32;                 // activation rows per tile (MMA N)
+constexpr int kBoxRows = 16;            // activation rows per TMA box
+constexpr int kThreads = 192;
+constexpr int kCtasPerSm = 2;
+constexpr int kStages = 2;
+constexpr int kABytes = kBM * 128;                         // 16 KB weight box
+constexpr int kBBytes = kBN * 128;                         // 4 KB: one K block of rows
+constexpr int kStageBytes = 2 * kABytes + 2 * kBBytes;     // 40 KB
+constexpr int kSmemBytes = kStages * kStageBytes + 1024;   // + 1024-byte alignment slack
+constexpr int kAccBufs = 4;
+constexpr int kAccCols = 2 * kBN;                          // gate | up
+constexpr int kTmemCols = kAccBufs * kAccCols;             // 256
+constexpr int kRing = 4;                                   // claimed units in flight
+constexpr int kMaxGroups = 1024;
+static_assert(kBN == 32, "one activation row per lane");
+static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte swizzle alignment");
+static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM columns");
+static_assert(kSmemBytes + 2 * 4 * (kMaxGroups + 1) + 2 * 4 * 4 * kBN + 1024 <=
+                  228 * 1024 / kCtasPerSm - 1024,
+              "shared memory for two CTAs per SM");
+
+struct FfnArgs {
+    int groups, hidden, inter, rows;
+    const int32_t *offsets;
+    const float *x_scales;     // [rows, hidden/128]
+    const float *w13_scales;   // [groups, 2*inter/128, hidden/128]
+    const float *w2_scales;    // [groups, hidden/128, inter/128]
+    uint8_t *h;                // [rows, inter] e4m3
+    float *h_scales;           // [rows, inter/128]
+    float *y;                  // [rows, hidden]
+    int32_t *sched;            // [0] next unit; [1 + j] finished gate/up tiles of activation tile j
+    int32_t *status;
+};
+
+struct Unit {
+    bool down;
+    int g, mt, j, row0, nvalid;
+};
+
+// Units: the gate/up tiles of all groups (group-major, then weight tile,
+// then activation tile), then the down tiles in the same order.  s_nt is the
+// prefix count of activation tiles over groups.
+__device__ __forceinline__ Unit decode_unit(int t, int n_gu, int MT1, int MT2, int G,
+                                            const int *s_nt, const int *s_off) {
+    Unit u;
+    u.down = t >= n_gu;
+    const int MT = u.down ? MT2 : MT1;
+    const int local0 = u.down ? t - n_gu : t;
+    const int q = local0 / MT;   // s_nt[g] <= q < s_nt[g + 1] for the unit's group g
+    int lo = 0, hi = G;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_nt[mid] <= q) lo = mid;
+        else hi = mid;
+    }
+    u.g = lo;
+    const int ntn = s_nt[lo + 1] - s_nt[lo];
+    const int local = local0 - MT * s_nt[lo];
+    u.mt = local / ntn;
+    const int nt = local - u.mt * ntn;
+    u.j = s_nt[lo] + nt;
+    u.row0 = s_off[lo] + nt * kBN;
+    u.nvalid = min(kBN, s_off[lo + 1] - u.row0);
+    return u;
+}
+
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    expert_ffn_kernel(const __grid_constant__ CUtensorMap tmW13,
+                      const __grid_constant__ CUtensorMap tmX,
+                      const __grid_constant__ CUtensorMap tmW2,
+                      const __grid_constant__ CUtensorMap tmH, const FfnArgs args) {
+    extern __shared__ uint8_t dsmem[];
+    __shared__ __align__(8) uint64_t full_bar[kStages];
+    __shared__ __align__(8) uint64_t empty_bar[kStages];
+    __shared__ __align__(8) uint64_t acc_full[kAccBufs];
+    __shared__ __align__(8) uint64_t acc_empty[kAccBufs];
+    __shared__ __align__(8) uint64_t unit_full[kRing];
+    __shared__ __align__(8) uint64_t unit_empty[kRing];
+    __shared__ __align__(8) uint64_t amax_bar[2];
+    __shared__ __align__(8) uint64_t hdone_bar[2];
+    __shared__ __align__(8) uint64_t drain_bar;
+    __shared__ uint32_t tmem_slot;
+    __shared__ int s_abort, s_bad;
+    __shared__ int s_ring[kRing];
+    __shared__ int s_off[kMaxGroups + 1];
+    __shared__ int s_nt[kMaxGroups + 1];
+    __shared__ float s_amax[2][4 * kBN];   // per gate/up tile: each epilogue warp's row maxima
+
+    using namespace ptx;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t smem_base = (smem_u32(dsmem) + 1023u) & ~1023u;
+    const int G = args.groups, H = args.hidden, I = args.inter;
+    const int MT1 = I / kBM;    // gate/up tiles per activation tile
+    const int MT2 = H / kBM;    // down tiles per activation tile
+    const int KB1 = H / 128;    // K blocks of the gate/up GEMM
+    const int KB2 = I / 128;    // K blocks of the down GEMM (even)
+    volatile int *abort_flag = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(smem_u32(&full_bar[s]), 1);
+            mbar_init(smem_u32(&empty_bar[s]), 1);
+        }
+        for (int b = 0; b < kAccBufs; ++b) {
+            mbar_init(smem_u32(&acc_full[b]), 1);
+            mbar_init(smem_u32(&acc_empty[b]), 4);
+        }
+        for (int r = 0; r < kRing; ++r) {
+            mbar_init(smem_u32(&unit_full[r]), 1);
+            mbar_init(smem_u32(&unit_empty[r]), 5);   // the MMA thread + four epilogue warps
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(smem_u32(&amax_bar[b]), 4);
+            mbar_init(smem_u32(&hdone_bar[b]), 4);
+        }
+        mbar_init(smem_u32(&drain_bar), 1);
+        s_abort = 0;
+        s_bad = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmW13);
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmW2);
+        tma_prefetch_desc(&tmH);
+    }
+    for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = args.offsets[i];
+    __syncthreads();
+    for (int g = threadIdx.x; g < G; g += kThreads) {
+        const int a = s_off[g], b = s_off[g + 1];
+        if (a < 0 || b < a || b > args.rows) s_bad = 1;
+    }
+    __syncthreads();
+    if (warp == 0) {   // activation-tile prefix over groups: lane L owns a contiguous run
+        const int per = (G + 31) / 32;
+        const int g0 = lane * per;
+        int local = 0;
+        for (int q = 0; q < per; ++q) {
+            const int g = g0 + q;
+            if (g < G) local += (s_off[g + 1] - s_off[g] + kBN - 1) / kBN;
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        int run = incl - local;
+        for (int q = 0; q < per; ++q) {
+            const int g = g0 + q;
+            if (g < G) {
+                s_nt[g] = run;
+                run += (s_off[g + 1] - s_off[g] + kBN - 1) / kBN;
+            }
+        }
+        if (lane == 31) s_nt[G] = incl;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = tmem_slot;
+    const int NT = s_nt[G];
+    const int n_gu = MT1 * NT;
+    const int total = s_bad ? 0 : n_gu + MT2 * NT;
+    if (s_bad && threadIdx.x == 0 && blockIdx.x == 0 && args.status)
+        atomicOr(args.status, MOE_DEV_BAD_OFFSETS);
+
+    if (warp == 0) {
+        // ------------------------------ scheduler + TMA producer
+        if (lane == 0) {
+            // Weight boxes are read once unless their group spans several
+            // activation tiles (then neighbouring units share the L2 copy);
+            // activation and h rows are re-read by every weight tile.
+            const uint64_t pol_w_once = policy_evict_first();
+            const uint64_t pol_w_shared = policy_evict_normal();
+            const uint64_t pol_a = policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0, issued = 0, parity_bits = 0;
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int slot = i % kRing;
+                if (!wait_bounded(smem_u32(&unit_empty[slot]), ((uint32_t)(i / kRing) & 1u) ^ 1u,
+                                  abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                const int t = atomicAdd(args.sched, 1);
+                s_ring[slot] = t;
+                mbar_arrive(smem_u32(&unit_full[slot]));
+                if (t >= total) break;
+                const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
+                if (u.down) {   // h rows of activation tile j complete?
+                    if (!wait_flag_geq(args.sched + 1 + u.j, MT1, abort_flag, args.status,
+                                       MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    fence_proxy_async_global();
+                }
+                const int nbox = (u.nvalid + kBoxRows - 1) / kBoxRows;
+                const int nsteps = u.down ? KB2 / 2 : KB1;
+                const uint32_t bytes =
+                    2 * kABytes + (u.down ? 2 : 1) * nbox * kBoxRows * 128;
+                const uint64_t pol_w =
+                    (s_off[u.g + 1] - s_off[u.g] > kBN) ? pol_w_shared : pol_w_once;
+                const int wrow = u.down ? u.g * H + u.mt * kBM : u.g * 2 * I + u.mt * kBM;
+                for (int ks = 0; ks < nsteps; ++ks) {
+                    if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_base + stage * kStageBytes;
+                    const uint32_t sb = sa + 2 * kABytes;
+                    const uint32_t fb = smem_u32(&full_bar[stage]);
+                    mbar_arrive_expect_tx(fb, bytes);
+                    if (!u.down) {
+                        tma_load_2d(sa, &tmW13, ks * 128, wrow, fb, pol_w);            // gate rows
+                        tma_load_2d(sa + kABytes, &tmW13, ks * 128, wrow + I, fb, pol_w);   // up rows
+                        for (int b = 0; b < nbox; ++b)
+                            tma_load_2d(sb + b * kBoxRows * 128, &tmX, ks * 128,
+                                        u.row0 + b * kBoxRows, fb, pol_a);
+                    } else {
+#pragma unroll
+                        for (int hk = 0; hk < 2; ++hk) {
+                            const int k0 = (2 * ks + hk) * 128;
+                            tma_load_2d(sa + hk * kABytes, &tmW2, k0, wrow, fb, pol_w);
+                            for (int b = 0; b < nbox; ++b)
+                                tma_load_2d(sb + hk * kBBytes + b * kBoxRows * 128, &tmH, k0,
+                                            u.row0 + b * kBoxRows, fb, pol_a);
+                        }
+                    }
+                    issued |= 1u << stage;
+                    parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {   // let every copy in flight land before the CTA exits
+                for (int s = 0; s < kStages; ++s)
+                    if ((issued >> s) & 1u)
+                        wait_drain(smem_u32(&full_bar[s]), (parity_bits >> s) & 1u);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------ MMA issuer
+        if (lane == 0) {
+            int stage = 0, ab = 0;
+            uint32_t phase = 0, aphase = 0;
+            bool ok = true;
+            for (int i = 0; ok; ++i) {
+                const int slot = i % kRing;
+                if (!wait_bounded(smem_u32(&unit_full[slot]), (uint32_t)(i / kRing) & 1u,
+                                  abort_flag, args.status, MOE_DEV_TIMEOUT)) {
+                    ok = false;
+                    break;
+                }
+                const int t = s_ring[slot];
+                mbar_arrive(smem_u32(&unit_empty[slot]));
+                if (t >= total) break;
+                const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
+                const int nmma = ((u.nvalid + 15) / 16) * 16;
+                const uint32_t idesc = idesc_e4m3(kBM, nmma);
+                const int nsteps = u.down ? KB2 / 2 : KB1;
+                for (int ks = 0; ks < nsteps && ok; ++ks) {
+                    if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, args.status,
+                                      MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_base + stage * kStageBytes;
+                    const uint32_t sb = sa + 2 * kABytes;
+                    const int nacc = u.down ? 2 : 1;
+                    for (int hk = 0; hk < nacc; ++hk) {
+                        if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
+                                          args.status, MOE_DEV_TIMEOUT)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d = tmem_base + (uint32_t)(ab * kAccCols);
+                        if (!u.down) {
+                            const uint64_t dg = sdesc_k_sw128(sa);
+                            const uint64_t du = sdesc_k_sw128(sa + kABytes);
+                            const uint64_t db = sdesc_k_sw128(sb);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K
+                                mma_f8f6f4(d, dg + 2 * kk, db + 2 * kk, idesc, kk > 0);
+                                mma_f8f6f4(d + kBN, du + 2 * kk, db + 2 * kk, idesc, kk > 0);
+                            }
+                        } else {
+                            const uint64_t da = sdesc_k_sw128(sa + hk * kABytes);
+                            const uint64_t db = sdesc_k_sw128(sb + hk * kBBytes);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_f8f6f4(d, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
+                        }
+                        mma_commit(smem_u32(&acc_full[ab]));
+                        if (++ab == kAccBufs) {
+                            ab = 0;
+                            aphase ^= 1u;
+                        }
+                    }
+                    if (!ok) break;
+                    mma_commit(smem_u32(&empty_bar[stage]));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // every MMA issued by this thread completes before teardown
+            mma_commit(smem_u32(&drain_bar));
+            wait_drain(smem_u32(&drain_bar), 0);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;                    // TMEM lanes [32q, 32q + 32)
+        const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
+        const int m_local = q * 32 + lane;
+        // a wait's outcome is made warp-uniform: the tcgen05.ld that follow
+        // are warp-collective
+        auto wwait = [&](uint64_t *bar, uint32_t parity) {
+            const bool r = wait_bounded(smem_u32(bar), parity, abort_flag, args.status,
+                                        MOE_DEV_TIMEOUT);
+            return __all_sync(0xffffffffu, r) != 0;
+        };
+        int ab = 0, n_done_gu = 0;
+        uint32_t aphase = 0;
+        bool ok = true;
+        for (int i = 0; ok; ++i) {
+            const int slot = i % kRing;
+            if (!wwait(&unit_full[slot], (uint32_t)(i / kRing) & 1u)) break;
+            const int t = s_ring[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&unit_empty[slot]));
+            if (t >= total) break;
+            const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
+            const int nchunks = (u.nvalid + 15) / 16;
+            const bool row_ok = lane < u.nvalid;   // lane n holds activation row n's scale
+            float acc[kBN], accu[kBN];
+#pragma unroll
+            for (int n = 0; n < kBN; ++n) {
+                acc[n] = 0.0f;
+                accu[n] = 0.0f;
+            }
+            const int KB = u.down ? KB2 : KB1;
+            const float *wsp, *wup = nullptr, *xsp;
+            if (!u.down) {
+                wsp = args.w13_scales + ((size_t)u.g * (2 * MT1) + u.mt) * KB1;
+                wup = wsp + (size_t)MT1 * KB1;
+                xsp = args.x_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB1;
+            } else {
+                // h and its scales are written by gate/up units of this launch:
+                // the unit id is published before its producer has seen them
+                // complete, so every thread acquires the completion count
+                // itself before it reads a scale
+                const bool dep = wait_flag_geq(args.sched + 1 + u.j, MT1, abort_flag,
+                                               args.status, MOE_DEV_TIMEOUT);
+                if (!__all_sync(0xffffffffu, dep)) {
+                    ok = false;
+                    break;
+                }
+                wsp = args.w2_scales + ((size_t)u.g * MT2 + u.mt) * KB2;
+                xsp = args.h_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB2;
+            }
+            // scales of K block kb + 1 are fetched while block kb is reduced;
+            // h_scales (written during this launch) take coherent loads, the
+            // rest the read-only path
+            auto xs_at = [&](int kb) {
+                if (!row_ok) return 0.0f;
+                return u.down ? ld_relaxed_gpu_f32(xsp + kb) : __ldg(xsp + kb);
+            };
+            float xs_n = xs_at(0), sw_n = __ldg(wsp), su_n = u.down ? 0.0f : __ldg(wup);
+            for (int kb = 0; kb < KB; ++kb) {
+                const float xs = xs_n, sw = sw_n, su = su_n;
+                if (kb + 1 < KB) {
+                    xs_n = xs_at(kb + 1);
+                    sw_n = __ldg(wsp + kb + 1);
+                    if (!u.down) su_n = __ldg(wup + kb + 1);
+                }
+                if (!wwait(&acc_full[ab], aphase)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t col = (uint32_t)(ab * kAccCols);
+                uint32_t v[kBN / 16][16];
+#pragma unroll
+                for (int c = 0; c < kBN / 16; ++c)
+                    if (c < nchunks) tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
+#pragma unroll
+                for (int c = 0; c < kBN / 16; ++c)
+                    if (c < nchunks) tmem_wait_ld(v[c]);
+#pragma unroll
+                for (int c = 0; c < kBN / 16; ++c)
+                    if (c < nchunks) {
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            const int n = c * 16 + jj;
+                            const float sx = __fmul_rn(__shfl_sync(0xffffffffu, xs, n), sw);
+                            acc[n] = fmaf(__uint_as_float(v[c][jj]), sx, acc[n]);
+                        }
+                    }
+                if (!u.down) {   // up rows: same activation scales, their own block scale
+#pragma unroll
+                    for (int c = 0; c < kBN / 16; ++c)
+                        if (c < nchunks)
+                            tmem_ld16(lane_base + col + (uint32_t)(kBN + c * 16), v[c]);
+#pragma unroll
+                    for (int c = 0; c < kBN / 16; ++c)
+                        if (c < nchunks) tmem_wait_ld(v[c]);
+#pragma unroll
+                    for (int c = 0; c < kBN / 16; ++c)
+                        if (c < nchunks) {
+#pragma unroll
+                            for (int jj = 0; jj < 16; ++jj) {
+                                const int n = c * 16 + jj;
+                                const float sx = __fmul_rn(__shfl_sync(0xffffffffu, xs, n), su);
+                                accu[n] = fmaf(__uint_as_float(v[c][jj]), sx, accu[n]);
+                            }
+                        }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+                if (++ab == kAccBufs) {
+                    ab = 0;
+                    aphase ^= 1u;
+                }
+            }
+            if (!ok) break;
+
+            if (!u.down) {
+                // h = silu(gate) * up; row n is quantised over the tile's 128
+                // features (one per thread): warp maxima, then the four warps'
+                // maxima through shared memory
+                const int b = n_done_gu & 1;
+                const uint32_t par = (uint32_t)(n_done_gu >> 1) & 1u;
+#pragma unroll
+                for (int n = 0; n < kBN; ++n) acc[n] = silu_mul(acc[n], accu[n]);
+                float mine = 0.0f;
+#pragma unroll
+                for (int n = 0; n < kBN; ++n) {
+                    float m = fabsf(acc[n]);
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (n == lane) mine = m;
+                }
+                s_amax[b][q * kBN + lane] = mine;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&amax_bar[b]));
+                if (!wwait(&amax_bar[b], par)) break;
+#pragma unroll
+                for (int n = 0; n < kBN; ++n)
+                    if (n < u.nvalid) {
+                        const float amax = fmaxf(fmaxf(s_amax[b][n], s_amax[b][kBN + n]),
+                                                 fmaxf(s_amax[b][2 * kBN + n], s_amax[b][3 * kBN + n]));
+                        const float sc = fp8_group_scale(amax);
+                        const size_t row = (size_t)(u.row0 + n);
+                        args.h[row * I + u.mt * kBM + m_local] = fp8_code(acc[n], sc);
+                        if (m_local == 0) args.h_scales[row * KB2 + u.mt] = sc;
+                    }
+                // publish: every epilogue warp's h stores, then one release
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&hdone_bar[b]));
+                if (q == 2) {   // warp 2 publishes
+                    if (!wwait(&hdone_bar[b], par)) break;
+                    if (lane == 0) {
+                        __threadfence();
+                        fence_proxy_async_global();
+                        red_release_gpu_add(args.sched + 1 + u.j, 1);
+                    }
+                    __syncwarp();
+                }
+                ++n_done_gu;
+            } else {
+#pragma unroll
+                for (int n = 0; n < kBN; ++n)
+                    if (n < u.nvalid)
+                        args.y[(size_t)(u.row0 + n) * H + u.mt * kBM + m_local] = acc[n];
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+size_t ffn_sched_bytes(int groups, int rows) {
+    return (size_t)4 * (1 + (size_t)groups + (size_t)ceil_div(rows, kBN));
+}
+
+int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *xp,
+                      const float *xp_scales, const int32_t *offsets, const void *w13,
+                      const float *w13_scales, const void *w2, const float *w2_scales, void *h,
+                      float *h_scales, float *y, int32_t *sched, bool sched_zeroed,
+                      int32_t *status, cudaStream_t s) {
+    if (rows == 0) return MOE_OK;
+    static std::once_flag attr_once[64];
+    static int attr_rc[64];
+    int dev = 0;
+    MOE_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    std::call_once(attr_once[dev], [&] {
+        attr_rc[dev] = cudaFuncSetAttribute(expert_ffn_kernel,
+                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            kSmemBytes) == cudaSuccess ? 0 : 1;
+    });
+    if (attr_rc[dev]) return MOE_ERR_CUDA;
+    CUtensorMap tmW13, tmX, tmW2, tmH;
+    if (!encode_2d(&tmW13, w13, true, (uint64_t)hidden, (uint64_t)groups * 2 * inter, kBM) ||
+        !encode_2d(&tmX, xp, true, (uint64_t)hidden, (uint64_t)rows, kBoxRows) ||
+        !encode_2d(&tmW2, w2, true, (uint64_t)inter, (uint64_t)groups * hidden, kBM) ||
+        !encode_2d(&tmH, h, true, (uint64_t)inter, (uint64_t)rows, kBoxRows))
+        return MOE_ERR_CUDA;
+    if (!sched_zeroed) MOE_CUDA_TRY(cudaMemsetAsync(sched, 0, ffn_sched_bytes(groups, rows), s));
+    FfnArgs a;
+    a.groups = groups;
+    a.hidden = hidden;
+    a.inter = inter;
+    a.rows = rows;
+    a.offsets = offsets;
+    a.x_scales = xp_scales;
+    a.w13_scales = w13_scales;
+    a.w2_scales = w2_scales;
+    a.h = static_cast<uint8_t *>(h);
+    a.h_scales = h_scales;
+    a.y = y;
+    a.sched = sched;
+    a.status = status;
+    const int64_t units_bound =
+        (int64_t)(inter / kBM + hidden / kBM) * (groups + ceil_div(rows, kBN));
+    const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, units_bound);
+    expert_ffn_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW13, tmX, tmW2, tmH, a);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}
+
+}  // namespace moe

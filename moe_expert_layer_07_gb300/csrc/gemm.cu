@@ -40,7 +40,9 @@
 #include <mutex>
 
 #include "internal.h"
+#include "numerics.cuh"
 #include "ptx.cuh"
+#include "tma_host.h"
 
 namespace moe {
 namespace {
@@ -91,10 +93,6 @@ struct GemmArgs {
     int c_bf16;
     int32_t *status;
 };
-
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
-}
 
 struct Tile {
     int g, mt, row0, nvalid;
@@ -487,10 +485,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         if (n < tl.nvalid) {
                             const float amax = fmaxf(fmaxf(s_amax[b][n], s_amax[b][BN + n]),
                                                      fmaxf(s_amax[b][2 * BN + n], s_amax[b][3 * BN + n]));
-                            const float sc = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+                            const float sc = fp8_group_scale(amax);
                             const size_t row = (size_t)(tl.row0 + n);
-                            H8[row * n_h + tl.mt * kBM + m_local] = (uint8_t)__nv_cvt_float_to_fp8(
-                                __fdiv_rn(acc[n], sc), __NV_SATFINITE, __NV_E4M3);
+                            H8[row * n_h + tl.mt * kBM + m_local] = fp8_code(acc[n], sc);
                             if (m_local == 0) args.h_scales[row * (n_h / 128) + tl.mt] = sc;
                         }
                 } else if (args.c_bf16) {
@@ -562,9 +559,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
+}  // namespace
+
 // ---- host side ---------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -594,6 +593,8 @@ bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint6
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
+
+namespace {
 
 template <bool FP8, int BN, int STAGES, bool SW = false>
 int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t s) {

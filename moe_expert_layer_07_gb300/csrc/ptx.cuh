@@ -79,6 +79,45 @@ __device__ __forceinline__ bool wait_drain(uint32_t bar, uint32_t parity) {
     return true;
 }
 
+// ---- flags between CTAs (global memory, GPU scope) ------------------------------
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t *p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float ld_relaxed_gpu_f32(const float *p) {
+    float v;
+    asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void red_release_gpu_add(int32_t *p, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy global accesses with async-proxy (TMA)
+// accesses to global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits until *flag >= target (acquire); bounded like wait_bounded.
+__device__ __forceinline__ bool wait_flag_geq(const int32_t *flag, int target,
+                                              volatile int *abort_flag, int32_t *status,
+                                              int32_t timeout_bit) {
+    if (ld_acquire_gpu(flag) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        __nanosleep(64);
+        if (ld_acquire_gpu(flag) >= target) return true;
+        if (*abort_flag) return false;
+        if (globaltimer() - t0 > kWaitLimitNs || it >= kWaitMaxPolls) {
+            if (ld_acquire_gpu(flag) >= target) return true;
+            *abort_flag = 1;
+            if (status) atomicOr(status, timeout_bit);
+            return false;
+        }
+    }
+}
+
 // ---- cp.async (4-byte global -> shared) ------------------------------------
 __device__ __forceinline__ void cp_async4(uint32_t dst, const void *src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst),

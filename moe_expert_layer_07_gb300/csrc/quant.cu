@@ -10,6 +10,7 @@
 #include <cuda_fp8.h>
 
 #include "internal.h"
+#include "numerics.cuh"
 
 namespace moe {
 namespace {
@@ -20,10 +21,6 @@ __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 
 // two fp32 -> two e4m3 codes (round to nearest even, saturate to +-448)
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
-}
-
-__device__ __forceinline__ float group_scale(float amax) {
-    return amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
 }
 
 // One warp per (row, 256-column segment): lanes 0-15 quantise group 2s,
@@ -49,7 +46,7 @@ __global__ void __launch_bounds__(256)
     for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
 #pragma unroll
     for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sc = group_scale(amax);
+    const float sc = fp8_group_scale(amax);
     if (!active) return;
     uint2 q;
     q.x = (uint32_t)e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
@@ -58,10 +55,6 @@ __global__ void __launch_bounds__(256)
           ((uint32_t)e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
     *reinterpret_cast<uint2 *>(out + row * H + col) = q;
     if ((lane & 15) == 0) scales[row * (H / 128) + col / 128] = sc;
-}
-
-__device__ __forceinline__ float silu_mul(float g, float u) {
-    return __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, expf(-g))), u);
 }
 
 // One warp per (row, 128-wide group of h); each lane 4 consecutive values.
@@ -85,7 +78,7 @@ __global__ void __launch_bounds__(256)
         float amax = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float sc = group_scale(amax);
+        const float sc = fp8_group_scale(amax);
         const uint32_t q = (uint32_t)e4m3x2(__fdiv_rn(h[0], sc), __fdiv_rn(h[1], sc)) |
                            ((uint32_t)e4m3x2(__fdiv_rn(h[2], sc), __fdiv_rn(h[3], sc)) << 16);
         *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(out) + row * I + col) = q;

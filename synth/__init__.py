@@ -92,6 +92,14 @@ CONFIGS = {
                              norm_topk=True, routed_scaling=2.5, dtype="fp8",
                              bias_std=0.01, zipf_s=1.0, balanced_perm=True,
                              num_sets=4),
+    # as r1_mini with a 512-wide intermediate (the size the one-kernel expert
+    # FFN takes) and Zipf-skewed routing, so hot experts span several 32-row
+    # activation tiles
+    "r1_mini_i512": MoEShape("r1_mini_i512", tokens=53, hidden=1024, inter=512,
+                             num_experts=32, num_shared=1, top_k=8, num_groups=8,
+                             topk_groups=4, group_topn=2, scoring="sigmoid",
+                             norm_topk=True, routed_scaling=2.5, dtype="fp8",
+                             bias_std=0.01, zipf_s=1.0),
     "bf16_mini": MoEShape("bf16_mini", tokens=29, hidden=512, inter=384,
                           num_experts=8, num_shared=2, top_k=3,
                           scoring="softmax", norm_topk=True),

@@ -59,6 +59,22 @@ def test_workspace_size_r1_decode(L):
             lay.src_of_row, lay.row_of_slot, lay.perm_scratch, lay.xp, lay.xp_scales, lay.gate_up,
             lay.h, lay.h_scales, lay.y]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    # the one-kernel FFN's scheduler counters follow the status word, so one
+    # memset clears both
+    assert lay.ffn_sched == 256
+    assert lay.logits - lay.ffn_sched >= moe.expert_ffn_sched_bytes(257, rows)
+
+
+def test_layer_kernel_counts(L):
+    # route (2) + quantise x + permute (3) + experts' FFN + combine
+    r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
+    assert moe.layer_kernel_count(r1, 128) == 8        # one-kernel FFN
+    assert moe.layer_kernel_count(r1, 4096) == 10      # wide: GEMM, SiLU-mul, GEMM
+    mini = moe.make_config(synth.CONFIGS["r1_mini"])   # inter 384: two GEMM kernels
+    assert moe.layer_kernel_count(mini, 37) == 9
+    b16 = moe.make_config(synth.CONFIGS["bf16_mini"])
+    assert moe.layer_kernel_count(b16, 29) == 8
+    assert moe.layer_kernel_count(r1, 0) == 0
 
 
 def test_bad_arguments_are_rejected_before_launch(L):
@@ -105,6 +121,22 @@ def test_bad_arguments_are_rejected_before_launch(L):
                                1 << 40, None) == -1
     assert L.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 4, fake, fake, 0, fake,
                                16, None) == -3
+    # the one-kernel expert FFN: FP8 with inter % 256 == 0 only, enough scratch
+    r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
+    ffn = lambda c, groups, rows, nbytes: L.moe_expert_ffn(
+        ctypes.byref(c), groups, rows, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
+        fake, nbytes, None, None)
+    need = moe.expert_ffn_sched_bytes(257, 1152)
+    assert need == 4 * (1 + 257 + 36)
+    assert ffn(b16, 9, 10, 1 << 20) == -2
+    assert ffn(cfg, 33, 10, 1 << 20) == -2           # inter 384
+    assert ffn(r1, 257, 1152, need - 4) == -3
+    assert ffn(r1, 0, 10, need) == -1
+    assert ffn(r1, 2000, 10, 1 << 20) == -2
+    assert L.moe_expert_ffn(ctypes.byref(r1), 257, 1152, P(0x1001), fake, fake, fake, fake, fake,
+                            fake, fake, fake, fake, fake, need, None, None) == -1
+    assert L.moe_expert_ffn(ctypes.byref(r1), 257, 0, None, None, None, None, None, None, None,
+                            None, None, None, None, 0, None, None) == 0
     # zero tokens enqueue nothing and succeed
     assert L.moe_route(ctypes.byref(cfg), 0, None, None, None, None, None, None, None, None,
                        None, None) == 0

@@ -24,7 +24,7 @@ from _gpu_common import (BF16_TOL, FP8_TOL, W_RTOL, Workload, build_library, che
 
 pytestmark = pytest.mark.gpu
 
-SMALL = ["tiny_bf16", "v2lite_bf16", "r1_mini", "r1_mini_zipf", "bf16_mini"]
+SMALL = ["tiny_bf16", "v2lite_bf16", "r1_mini", "r1_mini_zipf", "r1_mini_i512", "bf16_mini"]
 FULL = ["r1_decode_t128", "r1_zipf_t1024", "r1_prefill_t4096"]
 SAMPLE = {"r1_decode_t128": 16, "r1_zipf_t1024": 16, "r1_prefill_t4096": 16}
 
@@ -426,8 +426,9 @@ def test_layer_all_tokens_on_few_experts(lib):
     check_close(to_np(out), ref["out"], FP8_TOL)
 
 
-def test_layer_deterministic_and_graph_capturable(lib):
-    wl = workload("r1_mini")
+@pytest.mark.parametrize("name", ["r1_mini", "r1_mini_i512"])
+def test_layer_deterministic_and_graph_capturable(lib, name):
+    wl = workload(name)
     layer, out1 = run_layer(wl)
     _, out2 = run_layer(wl, layer=layer)
     assert torch.equal(out1, out2)
