@@ -11,6 +11,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -18,14 +19,19 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kMaxK = 16;
 constexpr int kMaxShared = 4;
+constexpr int kMaxRows = kMaxShared + kMaxK;
 
-// grid: (T, column blocks); each thread handles 8 consecutive columns
+// grid: (T, column blocks); each thread handles 4 consecutive columns.  All
+// rows of the token are loaded before the first addition, so their memory
+// latencies overlap; the additions then run in the fixed order.
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(const float *__restrict__ y, const int32_t *__restrict__ row_of_slot,
                    const float *__restrict__ topk_w, const int32_t *__restrict__ offsets,
                    void *__restrict__ out, int out_bf16, int T, int H, int E, int S, int k) {
-    __shared__ long rows[kMaxShared + kMaxK];
-    __shared__ float wts[kMaxShared + kMaxK];
+    __shared__ long rows[kMaxRows];
+    __shared__ float wts[kMaxRows];
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // expert outputs of the previous kernel
     const int t = blockIdx.x;
     if (threadIdx.x < S) {
         rows[threadIdx.x] = (long)offsets[E + threadIdx.x] + t;
@@ -36,37 +42,38 @@ __global__ void __launch_bounds__(kThreads)
         wts[threadIdx.x] = topk_w[(long)t * k + j];
     }
     __syncthreads();
-    const int v = blockIdx.y * kThreads + threadIdx.x;   // 8-column vector index
-    if (v * 8 >= H) return;
-    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int r = 0; r < S + k; ++r) {
-        const long row = rows[r];
-        if (row < 0) continue;
-        const float4 *src = reinterpret_cast<const float4 *>(y + row * H) + 2 * v;
-        const float4 a = __ldg(src), b = __ldg(src + 1);
-        const float val[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    const int v = blockIdx.y * kThreads + threadIdx.x;   // 4-column vector index
+    if (v * 4 >= H) return;
+    const int n = S + k;
+    float4 val[kMaxRows];
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r)
+        if (r < n && rows[r] >= 0)
+            val[r] = __ldg(reinterpret_cast<const float4 *>(y + rows[r] * H) + v);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+    for (int r = 0; r < kMaxRows; ++r) {
+        if (r >= n || rows[r] < 0) continue;
+        const float x[4] = {val[r].x, val[r].y, val[r].z, val[r].w};
         if (r < S) {
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], val[q]);
+            for (int q = 0; q < 4; ++q) acc[q] = __fadd_rn(acc[q], x[q]);
         } else {
             const float w = wts[r];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) acc[q] = fmaf(w, val[q], acc[q]);
+            for (int q = 0; q < 4; ++q) acc[q] = fmaf(w, x[q], acc[q]);
         }
     }
     if (out_bf16) {
-        uint4 o;
-        uint32_t *p = reinterpret_cast<uint32_t *>(&o);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[2 * q], acc[2 * q + 1]);
-            p[q] = *reinterpret_cast<uint32_t *>(&b2);
-        }
-        reinterpret_cast<uint4 *>(static_cast<uint16_t *>(out) + (long)t * H)[v] = o;
+        __nv_bfloat162 b0 = __floats2bfloat162_rn(acc[0], acc[1]);
+        __nv_bfloat162 b1 = __floats2bfloat162_rn(acc[2], acc[3]);
+        uint2 o;
+        o.x = *reinterpret_cast<uint32_t *>(&b0);
+        o.y = *reinterpret_cast<uint32_t *>(&b1);
+        reinterpret_cast<uint2 *>(static_cast<uint16_t *>(out) + (long)t * H)[v] = o;
     } else {
-        float4 *o = reinterpret_cast<float4 *>(static_cast<float *>(out) + (long)t * H) + 2 * v;
-        o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
-        o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        reinterpret_cast<float4 *>(static_cast<float *>(out) + (long)t * H)[v] =
+            make_float4(acc[0], acc[1], acc[2], acc[3]);
     }
 }
 
@@ -77,10 +84,12 @@ int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *r
                    cudaStream_t s) {
     if (T == 0) return MOE_OK;
     const int H = cfg->hidden;
-    dim3 grid(T, (unsigned)ceil_div(H / 8, kThreads));
-    combine_kernel<<<grid, kThreads, 0, s>>>(static_cast<const float *>(y), row_of_slot, topk_w,
-                                             offsets, out, out_dtype == MOE_OUT_BF16, T, H,
-                                             cfg->num_experts, cfg->num_shared, cfg->top_k);
+    if (cfg->num_shared + cfg->top_k > kMaxRows) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const dim3 grid(T, (unsigned)ceil_div(H / 4, kThreads));
+    if (launch_dependent(combine_kernel, grid, dim3(kThreads), 0, s, static_cast<const float *>(y),
+                         row_of_slot, topk_w, offsets, out, (int)(out_dtype == MOE_OUT_BF16), T,
+                         H, cfg->num_experts, cfg->num_shared, cfg->top_k))
+        return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

@@ -190,6 +190,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tma_prefetch_desc(&tmW2);
         tma_prefetch_desc(&tmH);
     }
+    pdl_wait();   // the set-up above overlaps the previous kernel's tail
     for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = args.offsets[i];
     __syncthreads();
     for (int g = threadIdx.x; g < G; g += kThreads) {
@@ -253,7 +254,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int t = atomicAdd(args.sched, 1);
                 s_ring[slot] = t;
                 mbar_arrive(smem_u32(&unit_full[slot]));
-                if (t >= total) break;
+                if (t >= total) {
+                    pdl_launch_dependents();   // nothing left to claim
+                    break;
+                }
                 const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
                 if (u.down) {   // h rows of activation tile j complete?
                     if (!wait_flag_geq(args.sched + 1 + u.j, MT1, abort_flag, args.status,
@@ -424,14 +428,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             } else {
                 // h and its scales are written by gate/up units of this launch:
                 // the unit id is published before its producer has seen them
-                // complete, so every thread acquires the completion count
-                // itself before it reads a scale
-                const bool dep = wait_flag_geq(args.sched + 1 + u.j, MT1, abort_flag,
-                                               args.status, MOE_DEV_TIMEOUT);
-                if (!__all_sync(0xffffffffu, dep)) {
+                // complete, so the epilogue acquires the completion count too
+                // before it reads a scale (lane 0 polls; after the warp
+                // barrier every lane's own acquire load reads the final count)
+                bool dep = true;
+                if (lane == 0)
+                    dep = wait_flag_geq(args.sched + 1 + u.j, MT1, abort_flag, args.status,
+                                        MOE_DEV_TIMEOUT);
+                if (!__shfl_sync(0xffffffffu, dep, 0)) {
                     ok = false;
                     break;
                 }
+                __syncwarp();
+                (void)ld_acquire_gpu(args.sched + 1 + u.j);
                 wsp = args.w2_scales + ((size_t)u.g * MT2 + u.mt) * KB2;
                 xsp = args.h_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB2;
             }
@@ -610,7 +619,9 @@ int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *x
     const int64_t units_bound =
         (int64_t)(inter / kBM + hidden / kBM) * (groups + ceil_div(rows, kBN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, units_bound);
-    expert_ffn_kernel<<<grid, kThreads, kSmemBytes, s>>>(tmW13, tmX, tmW2, tmH, a);
+    if (launch_dependent(expert_ffn_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, tmW13, tmX,
+                         tmW2, tmH, a))
+        return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

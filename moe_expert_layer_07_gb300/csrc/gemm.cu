@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmA);
     }
+    pdl_wait();   // the set-up above overlaps the previous kernel's tail
     for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = args.offsets[i];
     __syncthreads();
     for (int g = threadIdx.x; g < G; g += kThreads) {
@@ -621,7 +622,8 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
         (int64_t)(args.n_out / kBM / (SW ? 2 : 1)) * (args.groups + ceil_div(args.rows, BN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, tiles_bound);
     if (grid <= 0) return MOE_OK;
-    kern<<<grid, kThreads, Sh::kSmemBytes, s>>>(tmW, tmA, args);
+    if (launch_dependent(kern, dim3(grid), dim3(kThreads), Sh::kSmemBytes, s, tmW, tmA, args))
+        return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

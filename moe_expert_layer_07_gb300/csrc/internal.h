@@ -61,6 +61,26 @@ int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *r
                    const float *topk_w, const int32_t *offsets, void *out, int out_dtype,
                    cudaStream_t s);
 
+// Programmatic dependent launch: `kernel` may start while the previous
+// kernel in the stream drains.  Every CTA of such a kernel executes
+// pdl_wait() (griddepcontrol.wait) before it reads data that an earlier
+// kernel wrote and before it exits, so stream order stays transitive.
+template <typename... KArgs, typename... Args>
+int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t c = {};
+    c.gridDim = grid;
+    c.blockDim = block;
+    c.dynamicSmemBytes = smem;
+    c.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    c.attrs = at;
+    c.numAttrs = 1;
+    return cudaLaunchKernelEx(&c, kernel, args...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 // Kernel launches per call, for the layer's launch count.
 int route_kernel_count();
 int permute_kernel_count();

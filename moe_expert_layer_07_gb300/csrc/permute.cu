@@ -18,6 +18,7 @@
 //   permute_scatter  one warp per row: writes row_of_slot / src_of_row and
 //                    copies the row (16-byte vectors) and its scales.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -40,6 +41,8 @@ struct PermArgs {
 
 __global__ void __launch_bounds__(kChunk) permute_count_kernel(const PermArgs a) {
     extern __shared__ int32_t wc[];   // [32 warps][E]
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // routing ids
     const int R = a.T * a.k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int i = blockIdx.x * kChunk + tid;
@@ -100,6 +103,8 @@ __device__ int block_exclusive_scan(int v, int *total, int *sh) {
 
 __global__ void __launch_bounds__(1024) permute_scan_kernel(const PermArgs a, int chunks) {
     __shared__ int sh[33];
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // per-chunk counts
     const int G = a.E + a.S;
     const int per = (G + 1023) / 1024;   // consecutive groups per thread
     const int g0 = threadIdx.x * per;
@@ -134,6 +139,8 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const PermArgs a, in
 }
 
 __global__ void __launch_bounds__(256) permute_scatter_kernel(const PermArgs a) {
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // offsets and ranks
     const int lane = threadIdx.x & 31;
     const long w = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const long R = (long)a.T * a.k;
@@ -214,14 +221,18 @@ int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const 
             MOE_CUDA_TRY(cudaFuncSetAttribute(permute_count_kernel,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
                                               (int)smem));
-        permute_count_kernel<<<chunks, kChunk, smem, s>>>(a);
+        if (launch_dependent(permute_count_kernel, dim3(chunks), dim3(kChunk), smem, s, a))
+            return MOE_ERR_CUDA;
         MOE_LAUNCH_CHECK();
     }
-    permute_scan_kernel<<<1, 1024, 0, s>>>(a, chunks);
+    if (launch_dependent(permute_scan_kernel, dim3(1), dim3(1024), 0, s, a, chunks))
+        return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
     const int64_t rows = total_rows(cfg, T);
     if (rows > 0) {
-        permute_scatter_kernel<<<(unsigned)ceil_div(rows, 8), 256, 0, s>>>(a);
+        if (launch_dependent(permute_scatter_kernel, dim3((unsigned)ceil_div(rows, 8)), dim3(256),
+                             0, s, a))
+            return MOE_ERR_CUDA;
         MOE_LAUNCH_CHECK();
     }
     return MOE_OK;

@@ -17,6 +17,16 @@ __device__ __forceinline__ uint64_t globaltimer() {
     return t;
 }
 
+// ---- programmatic dependent launch ------------------------------------------
+// Waits until the previous kernel in the stream has completed and its
+// memory is visible (a no-op for a kernel launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel in the stream be scheduled once every CTA of this
+// grid has executed this (or exited); it still waits for completion.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- mbarrier ------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -11,6 +11,7 @@
 
 #include "internal.h"
 #include "numerics.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -28,6 +29,8 @@ __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
 __global__ void __launch_bounds__(256)
     quant_rows_kernel(const uint16_t *__restrict__ in, uint8_t *__restrict__ out,
                       float *__restrict__ scales, int rows, const int32_t *rows_dev, int H) {
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();
     const int lane = threadIdx.x & 31;
     const long warp = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int segs = (H + 255) / 256;
@@ -62,6 +65,8 @@ template <bool FP8>
 __global__ void __launch_bounds__(256)
     silu_mul_kernel(const float *__restrict__ in, void *__restrict__ out,
                     float *__restrict__ scales, int rows, const int32_t *rows_dev, int I) {
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // the gate/up rows (and their count) of the previous kernel
     const int lane = threadIdx.x & 31;
     const long warp = (long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int groups = I / 128;
@@ -99,22 +104,25 @@ int launch_act_requant(const moe_config *cfg, int mode, int rows, const int32_t 
                        const void *in, void *out, float *out_scales, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    int rc;
     if (mode == MOE_ACT_IDENTITY) {
         const int H = cfg->hidden;
         const long warps = (long)rows * ((H + 255) / 256);
-        quant_rows_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
-            static_cast<const uint16_t *>(in), static_cast<uint8_t *>(out), out_scales, rows,
-            rows_dev, H);
+        rc = launch_dependent(quant_rows_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, s,
+                              static_cast<const uint16_t *>(in), static_cast<uint8_t *>(out),
+                              out_scales, rows, rows_dev, H);
     } else {
         const int I = cfg->inter;
         const long warps = (long)rows * (I / 128);
-        if (fp8)
-            silu_mul_kernel<true><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
-                static_cast<const float *>(in), out, out_scales, rows, rows_dev, I);
-        else
-            silu_mul_kernel<false><<<(unsigned)((warps + 7) / 8), 256, 0, s>>>(
-                static_cast<const float *>(in), out, out_scales, rows, rows_dev, I);
+        const dim3 grid((unsigned)((warps + 7) / 8));
+        rc = fp8 ? launch_dependent(silu_mul_kernel<true>, grid, dim3(256), 0, s,
+                                    static_cast<const float *>(in), out, out_scales, rows,
+                                    rows_dev, I)
+                 : launch_dependent(silu_mul_kernel<false>, grid, dim3(256), 0, s,
+                                    static_cast<const float *>(in), out, out_scales, rows,
+                                    rows_dev, I);
     }
+    if (rc) return rc;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }

@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace moe {
 namespace {
@@ -72,6 +73,7 @@ __global__ void __launch_bounds__(256)
                        const float *__restrict__ offset, float *__restrict__ logits, int T,
                        int E, int H) {
     extern __shared__ __align__(16) uint8_t smem[];
+    ptx::pdl_launch_dependents();   // the selection kernel may take its SM slots now
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t_base = blockIdx.x * kCT, e_base = blockIdx.y * kCE;
     const int steps = (H + kStepElems - 1) / kStepElems;
@@ -171,6 +173,8 @@ constexpr int kSelThreads = 128;
 template <int PL>   // experts per lane of warp 0: e = q*32 + lane, q < PL
 __global__ void __launch_bounds__(kSelThreads) route_select_kernel(const SelectArgs a) {
     __shared__ float sh_l[PL * 32], sh_s[PL * 32], sh_sel[PL * 32];
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // logits of the previous kernel
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x;
     if (t >= a.T) return;   // block-uniform
@@ -366,8 +370,8 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(const SelectA
 }
 
 template <int PL>
-void launch_select(const SelectArgs &a, cudaStream_t s) {
-    route_select_kernel<PL><<<a.T, kSelThreads, 0, s>>>(a);
+int launch_select(const SelectArgs &a, cudaStream_t s) {
+    return launch_dependent(route_select_kernel<PL>, dim3(a.T), dim3(kSelThreads), 0, s, a);
 }
 
 }  // namespace
@@ -415,12 +419,14 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
     a.w = topk_w;
     a.status = status;
     const int pl = (int)ceil_div(E, 32);
-    if (pl <= 1) launch_select<1>(a, s);
-    else if (pl <= 2) launch_select<2>(a, s);
-    else if (pl <= 4) launch_select<4>(a, s);
-    else if (pl <= 8) launch_select<8>(a, s);
-    else if (pl <= 16) launch_select<16>(a, s);
-    else launch_select<32>(a, s);
+    int rc;
+    if (pl <= 1) rc = launch_select<1>(a, s);
+    else if (pl <= 2) rc = launch_select<2>(a, s);
+    else if (pl <= 4) rc = launch_select<4>(a, s);
+    else if (pl <= 8) rc = launch_select<8>(a, s);
+    else if (pl <= 16) rc = launch_select<16>(a, s);
+    else rc = launch_select<32>(a, s);
+    if (rc) return rc;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
 }
