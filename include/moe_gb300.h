@@ -318,6 +318,20 @@ MOE_API int moe_layer_kernel_count(const moe_config *cfg, int32_t T);
 MOE_API int moe_selftest_bounded_wait(int32_t *dev_status, int64_t limit_ns, int32_t *dev_result,
                                       void *stream);
 
+/* Self-test of moe_expert_ffn's inter-CTA wait (no counterpart on the pages:
+ * a robustness check of this library).  Runs the one-kernel FFN on a tiny
+ * problem (hidden 128, inter 256, one group, one row) whose scheduler
+ * counter starts past the gate/up units, so the down unit waits for h rows
+ * that no CTA will write: its bounded wait gives up after about a second,
+ * sets MOE_DEV_TIMEOUT in *dev_status, and every CTA drains its copies and
+ * MMAs, frees its tensor memory and exits; nothing traps and the context
+ * stays usable.  scratch: device, 16-byte aligned, at least
+ * moe_selftest_ffn_flag_timeout_scratch_bytes() bytes, owned by the caller
+ * (cleared by the call). */
+MOE_API size_t moe_selftest_ffn_flag_timeout_scratch_bytes(void);
+MOE_API int moe_selftest_ffn_flag_timeout(void *scratch, size_t scratch_bytes,
+                                          int32_t *dev_status, void *stream);
+
 /* ---- continuous load balancing ------------------------------------------------
  * Report, section "Load balancing across GPUs": in serving, activation
  * frequencies are re-measured periodically and a new expert permutation is

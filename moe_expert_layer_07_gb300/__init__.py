@@ -82,6 +82,7 @@ _SIGS = {
     "expert_affinity_permutation": [_P, _P, _I, _I, ctypes.c_double, _P, _P,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
     "moe_relayout_experts": [_P, _P, _P, _I, ctypes.c_int64, _P, _P],
+    "moe_selftest_ffn_flag_timeout": [_P, ctypes.c_size_t, _P, _P],
     "moe_expert_ffn": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
                        _P, _P],
 }
@@ -103,6 +104,8 @@ def lib():
         L.moe_permute_static_scratch_capacity.restype = ctypes.c_size_t
         L.moe_expert_ffn_sched_bytes.argtypes = [_I, _I]
         L.moe_expert_ffn_sched_bytes.restype = ctypes.c_size_t
+        L.moe_selftest_ffn_flag_timeout_scratch_bytes.argtypes = []
+        L.moe_selftest_ffn_flag_timeout_scratch_bytes.restype = ctypes.c_size_t
         L.moe_status_string.argtypes = [ctypes.c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
         _lib = L

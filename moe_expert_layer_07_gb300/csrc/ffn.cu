@@ -627,3 +627,73 @@ int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *x
 }
 
 }  // namespace moe
+
+// ---- self-test of the inter-CTA flag wait ------------------------------------
+namespace moe {
+namespace {
+
+constexpr int kSelftestH = 128, kSelftestI = 256;
+
+__global__ void ffn_selftest_init_kernel(int32_t *offsets, int32_t *sched, int n_gu) {
+    if (threadIdx.x == 0) {
+        offsets[0] = 0;
+        offsets[1] = 1;
+        sched[0] = n_gu;   // every gate/up unit counts as claimed; none will finish
+    }
+}
+
+struct SelftestLayout {
+    size_t xp, xs, off, w13, w13s, w2, w2s, h, hs, y, sched, total;
+};
+
+SelftestLayout selftest_layout() {
+    SelftestLayout L;
+    size_t o = 0;
+    auto take = [&](size_t b) {
+        const size_t r = o;
+        o = align_up(o + b);
+        return r;
+    };
+    L.xp = take(kSelftestH);
+    L.xs = take(4 * (kSelftestH / 128));
+    L.off = take(8);
+    L.w13 = take((size_t)2 * kSelftestI * kSelftestH);
+    L.w13s = take(4 * (2 * kSelftestI / 128) * (kSelftestH / 128));
+    L.w2 = take((size_t)kSelftestH * kSelftestI);
+    L.w2s = take(4 * (kSelftestH / 128) * (kSelftestI / 128));
+    L.h = take(kSelftestI);
+    L.hs = take(4 * (kSelftestI / 128));
+    L.y = take(4 * kSelftestH);
+    L.sched = take(ffn_sched_bytes(1, 1));
+    L.total = o;
+    return L;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" MOE_API size_t moe_selftest_ffn_flag_timeout_scratch_bytes(void) {
+    return moe::selftest_layout().total;
+}
+
+extern "C" MOE_API int moe_selftest_ffn_flag_timeout(void *scratch, size_t scratch_bytes,
+                                                     int32_t *dev_status, void *stream) {
+    using namespace moe;
+    const SelftestLayout L = selftest_layout();
+    if (!scratch || !dev_status || !aligned16(scratch) || scratch_bytes < L.total)
+        return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *b = static_cast<uint8_t *>(scratch);
+    MOE_CUDA_TRY(cudaMemsetAsync(b, 0, L.total, s));
+    int32_t *off = reinterpret_cast<int32_t *>(b + L.off);
+    int32_t *sched = reinterpret_cast<int32_t *>(b + L.sched);
+    const int n_gu = kSelftestI / 128;   // gate/up units of the one 32-row activation tile
+    ffn_selftest_init_kernel<<<1, 32, 0, s>>>(off, sched, n_gu);
+    MOE_LAUNCH_CHECK();
+    return launch_expert_ffn(1, kSelftestH, kSelftestI, 1, b + L.xp,
+                             reinterpret_cast<const float *>(b + L.xs), off, b + L.w13,
+                             reinterpret_cast<const float *>(b + L.w13s), b + L.w2,
+                             reinterpret_cast<const float *>(b + L.w2s), b + L.h,
+                             reinterpret_cast<float *>(b + L.hs), reinterpret_cast<float *>(b + L.y),
+                             sched, true, dev_status, s);
+}

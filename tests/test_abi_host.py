@@ -137,6 +137,12 @@ def test_bad_arguments_are_rejected_before_launch(L):
                             fake, fake, fake, fake, fake, need, None, None) == -1
     assert L.moe_expert_ffn(ctypes.byref(r1), 257, 0, None, None, None, None, None, None, None,
                             None, None, None, None, 0, None, None) == 0
+    # the FFN flag self-test needs its scratch
+    n = L.moe_selftest_ffn_flag_timeout_scratch_bytes()
+    assert 0 < n < (1 << 20)
+    assert L.moe_selftest_ffn_flag_timeout(fake, n - 1, fake, None) == -1
+    assert L.moe_selftest_ffn_flag_timeout(None, n, fake, None) == -1
+    assert L.moe_selftest_ffn_flag_timeout(fake, n, None, None) == -1
     # zero tokens enqueue nothing and succeed
     assert L.moe_route(ctypes.byref(cfg), 0, None, None, None, None, None, None, None, None,
                        None, None) == 0

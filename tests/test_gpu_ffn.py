@@ -139,3 +139,23 @@ def test_expert_ffn_no_rows_and_bad_offsets(lib):
     h, hs, y, stv, _ = _fused(cfg, G, rows, H, I, *args)
     assert stv & moe.DEV_BAD_OFFSETS
     assert bool(torch.isnan(y).all())
+
+
+def test_flag_wait_gives_up_and_context_survives(lib):
+    """A down unit whose h rows nobody writes: the bounded wait expires, the
+    device status says so, and the next launches run normally."""
+    n = moe.lib().moe_selftest_ffn_flag_timeout_scratch_bytes()
+    scratch = torch.empty(n, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = moe.lib().moe_selftest_ffn_flag_timeout(scratch.data_ptr(), n, st.data_ptr(),
+                                                 torch.cuda.current_stream().cuda_stream)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(st.item()) & moe.DEV_TIMEOUT
+    H, I, counts = 1024, 512, [3, 0, 17, 40, 128, 1]
+    cfg = _cfg(H, I)
+    p = _problem(H, I, counts, seed=3)
+    G, rows = p[0], p[1]
+    h_ref, hs_ref, y_ref = _two_kernels(cfg, G, rows, H, I, *p[2:])
+    h, hs, y, stv, _ = _fused(cfg, G, rows, H, I, *p[2:])
+    assert stv == 0 and torch.equal(y, y_ref) and torch.equal(h, h_ref)
