@@ -77,7 +77,7 @@ constexpr int kMaxGroups = 1024;
 static_assert(kBN == 32, "one activation row per lane");
 static_assert(kStageBytes % 1024 == 0, "stages keep 1024-byte swizzle alignment");
 static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM columns");
-static_assert(kSmemBytes + 2 * 4 * (kMaxGroups + 1) + 2 * 4 * 4 * kBN + 1024 <=
+static_assert(kSmemBytes + 2 * 4 * (kMaxGroups + 1) + 2 * 4 * 4 * kBN + 4 * 4 * 2 * 2 * kBN + 1024 <=
                   228 * 1024 / kCtasPerSm - 1024,
               "shared memory for two CTAs per SM");
 
@@ -147,6 +147,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __shared__ int s_off[kMaxGroups + 1];
     __shared__ int s_nt[kMaxGroups + 1];
     __shared__ float s_amax[2][4 * kBN];   // per gate/up tile: each epilogue warp's row maxima
+    // per epilogue warp and K-block parity: every column's promotion factor
+    // x_scale[n, kb] * w_scale[kb] (gate, then up), read as 16-byte broadcasts
+    __shared__ __align__(16) float s_sx[4][2][2 * kBN];
 
     using namespace ptx;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -459,6 +462,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     sw_n = __ldg(wsp + kb + 1);
                     if (!u.down) su_n = __ldg(wup + kb + 1);
                 }
+                float *sxw = s_sx[q][kb & 1];
+                sxw[lane] = __fmul_rn(xs, sw);   // lane n holds row n's activation scale
+                if (!u.down) sxw[kBN + lane] = __fmul_rn(xs, su);
+                __syncwarp();
                 if (!wwait(&acc_full[ab], aphase)) {
                     ok = false;
                     break;
@@ -476,10 +483,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int c = 0; c < kBN / 16; ++c)
                     if (c < nchunks) {
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            const int n = c * 16 + jj;
-                            const float sx = __fmul_rn(__shfl_sync(0xffffffffu, xs, n), sw);
-                            acc[n] = fmaf(__uint_as_float(v[c][jj]), sx, acc[n]);
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const float4 f = reinterpret_cast<const float4 *>(sxw)[c * 4 + j4];
+                            const int n = c * 16 + j4 * 4;
+                            acc[n] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, acc[n]);
+                            acc[n + 1] = fmaf(__uint_as_float(v[c][j4 * 4 + 1]), f.y, acc[n + 1]);
+                            acc[n + 2] = fmaf(__uint_as_float(v[c][j4 * 4 + 2]), f.z, acc[n + 2]);
+                            acc[n + 3] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, acc[n + 3]);
                         }
                     }
                 if (!u.down) {   // up rows: same activation scales, their own block scale
@@ -494,10 +504,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     for (int c = 0; c < kBN / 16; ++c)
                         if (c < nchunks) {
 #pragma unroll
-                            for (int jj = 0; jj < 16; ++jj) {
-                                const int n = c * 16 + jj;
-                                const float sx = __fmul_rn(__shfl_sync(0xffffffffu, xs, n), su);
-                                accu[n] = fmaf(__uint_as_float(v[c][jj]), sx, accu[n]);
+                            for (int j4 = 0; j4 < 4; ++j4) {
+                                const float4 f =
+                                    reinterpret_cast<const float4 *>(sxw + kBN)[c * 4 + j4];
+                                const int n = c * 16 + j4 * 4;
+                                accu[n] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, accu[n]);
+                                accu[n + 1] = fmaf(__uint_as_float(v[c][j4 * 4 + 1]), f.y, accu[n + 1]);
+                                accu[n + 2] = fmaf(__uint_as_float(v[c][j4 * 4 + 2]), f.z, accu[n + 2]);
+                                accu[n + 3] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, accu[n + 3]);
                             }
                         }
                 }

@@ -77,7 +77,9 @@ struct GemmShape {
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 64, "BN");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols * kCtasPerSm <= 512,
                   "TMEM columns");
-    static_assert((kSmemBytes + 8 * kXsElems + 8 * kWsElems + 8 * kAmaxElems + 8 * 1024 + 1024) *
+    static constexpr int kSxElems = FP8 ? 4 * 2 * kNA * BN : 1;   // per warp, per K-block parity
+    static_assert((kSmemBytes + 8 * kXsElems + 8 * kWsElems + 8 * kAmaxElems + 4 * kSxElems +
+                   8 * 1024 + 1024) *
                           kCtasPerSm <=
                       228 * 1024,
                   "shared memory");
@@ -144,6 +146,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __shared__ float s_xs[2][S::kXsElems];
     // SwiGLU + FP8: per tile, each epilogue warp's |h| maximum of every row n
     __shared__ float s_amax[2][S::kAmaxElems];
+    // FP8: per epilogue warp, the K block's promotion factor of every column
+    // n, x_scale[n, kb] * w_scale[kb] (gate, then up), read back as 16-byte
+    // broadcasts instead of a shuffle per column
+    __shared__ __align__(16) float s_sx[S::kSxElems];
 
     using namespace ptx;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -396,10 +402,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 for (int kb = 0; kb < KB; ++kb) {
                     const float sw = s_ws[b][kb];
                     const float swu = SW ? s_ws[b][KB + kb] : 0.0f;
-                    float xs[BN / 32];
+                    float *sxw = s_sx + (q * 2 + (kb & 1)) * (S::kNA * BN);
 #pragma unroll
-                    for (int h = 0; h < BN / 32; ++h)
-                        xs[h] = (h * 32 + lane < tl.nvalid) ? s_xs[b][kb * BN + h * 32 + lane] : 0.0f;
+                    for (int h = 0; h < BN / 32; ++h) {
+                        const int n = h * 32 + lane;
+                        const float xv = n < tl.nvalid ? s_xs[b][kb * BN + n] : 0.0f;
+                        sxw[n] = __fmul_rn(xv, sw);
+                        if (SW) sxw[BN + n] = __fmul_rn(xv, swu);
+                    }
+                    __syncwarp();
                     if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
                                       MOE_DEV_TIMEOUT)) {
                         ok = false;
@@ -418,10 +429,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     for (int c = 0; c < BN / 16; ++c)
                         if (c < nchunks) {
 #pragma unroll
-                            for (int j = 0; j < 16; ++j) {
-                                const int n = c * 16 + j;
-                                const float sx = __fmul_rn(__shfl_sync(0xffffffffu, xs[n / 32], n & 31), sw);
-                                acc[n] = fmaf(__uint_as_float(v[c][j]), sx, acc[n]);
+                            for (int j4 = 0; j4 < 4; ++j4) {
+                                const float4 f = reinterpret_cast<const float4 *>(sxw)[c * 4 + j4];
+                                const int n = c * 16 + j4 * 4;
+                                acc[n] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, acc[n]);
+                                acc[n + 1] = fmaf(__uint_as_float(v[c][j4 * 4 + 1]), f.y, acc[n + 1]);
+                                acc[n + 2] = fmaf(__uint_as_float(v[c][j4 * 4 + 2]), f.z, acc[n + 2]);
+                                acc[n + 3] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, acc[n + 3]);
                             }
                         }
                     if (SW) {   // up rows: same activation scales, their own block scale
@@ -436,11 +450,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         for (int c = 0; c < BN / 16; ++c)
                             if (c < nchunks) {
 #pragma unroll
-                                for (int j = 0; j < 16; ++j) {
-                                    const int n = c * 16 + j;
-                                    const float sx =
-                                        __fmul_rn(__shfl_sync(0xffffffffu, xs[n / 32], n & 31), swu);
-                                    accu[SW ? n : 0] = fmaf(__uint_as_float(v[c][j]), sx, accu[SW ? n : 0]);
+                                for (int j4 = 0; j4 < 4; ++j4) {
+                                    const float4 f =
+                                        reinterpret_cast<const float4 *>(sxw + BN)[c * 4 + j4];
+                                    const int n = c * 16 + j4 * 4;
+                                    float *au = accu + (SW ? n : 0);
+                                    au[0] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, au[0]);
+                                    au[SW ? 1 : 0] = fmaf(__uint_as_float(v[c][j4 * 4 + 1]), f.y, au[SW ? 1 : 0]);
+                                    au[SW ? 2 : 0] = fmaf(__uint_as_float(v[c][j4 * 4 + 2]), f.z, au[SW ? 2 : 0]);
+                                    au[SW ? 3 : 0] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, au[SW ? 3 : 0]);
                                 }
                             }
                     }
