@@ -111,6 +111,12 @@ CONFIGS = {
                            topk_groups=4, group_topn=2, scoring="sigmoid",
                            norm_topk=True, routed_scaling=2.5, dtype="fp8",
                            bias_std=0.01),
+    # about 128 rows per routed expert, as in the 4096-token, 256-expert layer
+    "r1_e32_t512": MoEShape("r1_e32_t512", tokens=512, hidden=7168, inter=2048,
+                            num_experts=32, num_shared=1, top_k=8, num_groups=8,
+                            topk_groups=4, group_topn=2, scoring="sigmoid",
+                            norm_topk=True, routed_scaling=2.5, dtype="fp8",
+                            bias_std=0.01),
     "r1_e32_t128": MoEShape("r1_e32_t128", tokens=128, hidden=7168, inter=2048,
                             num_experts=32, num_shared=1, top_k=8, num_groups=8,
                             topk_groups=4, group_topn=2, scoring="sigmoid",
