@@ -39,16 +39,10 @@ static_assert(kTB * kEB == 32, "one output per lane");
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
-__device__ __forceinline__ float dot8(const uint4 &a, const uint4 &b, float acc) {
-    acc = fmaf(bf_lo(a.x), bf_lo(b.x), acc);
-    acc = fmaf(bf_hi(a.x), bf_hi(b.x), acc);
-    acc = fmaf(bf_lo(a.y), bf_lo(b.y), acc);
-    acc = fmaf(bf_hi(a.y), bf_hi(b.y), acc);
-    acc = fmaf(bf_lo(a.z), bf_lo(b.z), acc);
-    acc = fmaf(bf_hi(a.z), bf_hi(b.z), acc);
-    acc = fmaf(bf_lo(a.w), bf_lo(b.w), acc);
-    acc = fmaf(bf_hi(a.w), bf_hi(b.w), acc);
-    return acc;
+// element e (0..7, increasing h) of 8 packed bf16 values, widened to fp32
+__device__ __forceinline__ float bf_elem(const uint4 &a, int e) {
+    const uint32_t w = e < 2 ? a.x : e < 4 ? a.y : e < 6 ? a.z : a.w;
+    return (e & 1) ? bf_hi(w) : bf_lo(w);
 }
 
 // CTA tile of 16 tokens x 16 experts, 8 warps of 4 tokens x 8 experts each.
@@ -120,10 +114,21 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int j = 0; j < kEB; ++j)
             wv[j] = *reinterpret_cast<const uint4 *>(buf + (kCT + we * kEB + j) * (kStepElems * 2) + lane * 16);
+        // outer products over the chunk's 8 elements: each bf16 value is
+        // widened once per step, and every accumulator still takes its 8
+        // products in increasing h
 #pragma unroll
-        for (int i = 0; i < kTB; ++i)
+        for (int e = 0; e < 8; ++e) {
+            float xf[kTB], wf[kEB];
 #pragma unroll
-            for (int j = 0; j < kEB; ++j) acc[i][j] = dot8(xv[i], wv[j], acc[i][j]);
+            for (int i = 0; i < kTB; ++i) xf[i] = bf_elem(xv[i], e);
+#pragma unroll
+            for (int j = 0; j < kEB; ++j) wf[j] = bf_elem(wv[j], e);
+#pragma unroll
+            for (int i = 0; i < kTB; ++i)
+#pragma unroll
+                for (int j = 0; j < kEB; ++j) acc[i][j] = fmaf(xf[i], wf[j], acc[i][j]);
+        }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
 
