@@ -298,6 +298,47 @@ def test_grouped_gemm(lib, fp8, N, K, out_bf16):
     assert np.all(np.isnan(got[inside:]))
 
 
+WIDE_ROWS = [0, 1, 127, 128, 129, 0, 255, 64, 300, 17]
+
+
+def test_grouped_gemm_tile_variants_agree(lib):
+    """The 32- and 64-row activation tiles (chosen by rows per group) promote
+    per K block in the same order: the same bits, within the oracle's
+    tolerance.  Empty groups appended to the same problem move it between
+    the variants."""
+    s = synth.CONFIGS["r1_mini"]
+    cfg = moe.make_config(s)
+    N, K = 384, 1024
+    counts = np.array(WIDE_ROWS)
+    rows = int(counts.sum())
+    g = torch.Generator(device="cuda").manual_seed(11)
+    a32 = torch.randn(rows, K, device="cuda", generator=g)
+    a = torch.empty((rows, K), dtype=torch.uint8, device="cuda")
+    asc = torch.empty((rows, K // 128), device="cuda")
+    cfg_q = moe.make_config(synth.MoEShape("q", rows, K, 128, 1, 0, 1, dtype="fp8"))
+    moe.act_requant(cfg_q, moe.ACT_IDENTITY, rows, a32.to(torch.bfloat16), a, asc)
+    w, wsc = synth.block_quantize_e4m3(
+        torch.randn(len(counts), N, K, device="cuda", generator=g) * 0.05)
+    outs = []
+    for extra in (0, 40, 70):   # 102, 20 and 13 rows per group: 64, 64 and 32-row tiles
+        G = len(counts) + extra
+        off = np.concatenate([[0], np.cumsum(np.concatenate([counts, np.zeros(extra, int)]))])
+        wpad = torch.cat([w, torch.zeros((extra, N, K), dtype=w.dtype, device="cuda")])
+        spad = torch.cat([wsc, torch.ones((extra,) + tuple(wsc.shape[1:]), device="cuda")])
+        c = torch.full((rows, N), float("nan"), device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        moe.grouped_gemm(cfg, G, N, K, rows, a, asc,
+                         torch.as_tensor(off.astype(np.int32), device="cuda"), wpad, spad, c,
+                         moe.OUT_F32, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        outs.append(c)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    ref = olayer.grouped_gemm(s, off, to_np(a), to_np(w), to_np(asc), to_np(wsc))
+    check_close(to_np(outs[0]), ref, 1e-3)
+
+
 def test_grouped_gemm_rejects_inconsistent_offsets(lib):
     s = synth.CONFIGS["r1_mini"]
     cfg = moe.make_config(s)
