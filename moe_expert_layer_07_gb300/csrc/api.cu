@@ -326,8 +326,21 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     int32_t *ros = reinterpret_cast<int32_t *>(base + L.row_of_slot);
     (void)E;
 
+    // The one-kernel FFN claims gate/up units 0, 1, ... first (group-major);
+    // at decode every group has one 32-row activation tile, so unit u is
+    // (expert u / (inter/128), weight tile u % (inter/128)).  Their first K
+    // blocks go to L2 while routing leaves HBM idle (about 80 MB at R1).
+    L2Prefetch pf;
+    if (fused) {
+        pf.w13 = static_cast<const uint8_t *>(w->w13);
+        pf.hidden = H;
+        pf.inter = I;
+        pf.groups = G;
+        pf.units = 2 * sm_count();
+        pf.bytes = H < 1024 ? H : 1024;
+    }
     rc = launch_route(cfg, T, x, w->w_gate, w->e_bias, w->logit_offset, w->log2phys, logits, ids,
-                      tw, status, s);
+                      tw, status, s, fused ? &pf : nullptr);
     if (rc) return rc;
     const void *rows_src = x;
     const float *rows_scales = nullptr;

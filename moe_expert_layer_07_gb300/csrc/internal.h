@@ -29,10 +29,18 @@ inline int groups_of(const moe_config *cfg) { return cfg->num_experts + cfg->num
 int sm_count();
 
 // ---- launchers (validated arguments; return MOE_OK or MOE_ERR_CUDA) ----
+// Weight rows the expert FFN will read first, for the gate-logit kernel to
+// prefetch into L2 while routing keeps HBM idle: the first `bytes` of every
+// gate and up row of the first `units` gate/up units, taking unit u as
+// (expert u / (inter/128), weight tile u % (inter/128)).
+struct L2Prefetch {
+    const uint8_t *w13 = nullptr;   // e4m3 [groups, 2*inter, hidden]
+    int hidden = 0, inter = 0, groups = 0, units = 0, bytes = 0;
+};
 int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate,
                  const float *e_bias, const float *logit_offset, const int32_t *log2phys,
                  float *logits, int32_t *topk_ids, float *topk_w, int32_t *status,
-                 cudaStream_t s);
+                 cudaStream_t s, const L2Prefetch *pf = nullptr);
 int launch_act_requant(const moe_config *cfg, int mode, int rows, const int32_t *rows_dev,
                        const void *in, void *out, float *out_scales, cudaStream_t s);
 size_t permute_scratch_bytes(const moe_config *cfg, int T);

@@ -65,9 +65,22 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
 __global__ void __launch_bounds__(256)
     gate_logits_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wg,
                        const float *__restrict__ offset, float *__restrict__ logits, int T,
-                       int E, int H) {
+                       int E, int H, const L2Prefetch pf) {
     extern __shared__ __align__(16) uint8_t smem[];
     ptx::pdl_launch_dependents();   // the selection kernel may take its SM slots now
+    if (pf.units > 0) {   // L2 prefetch of the expert FFN's first weight rows (a hint)
+        const int mt1 = pf.inter / 128;
+        const long jobs = (long)pf.units * 256;
+        const long nthreads = (long)gridDim.x * gridDim.y * blockDim.x;
+        for (long j = ((long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+             j < jobs; j += nthreads) {
+            const int u = (int)(j >> 8), r = (int)(j & 255);
+            const int g = u / mt1, mt = u - g * mt1;
+            if (g >= pf.groups) break;
+            const long row = (long)g * 2 * pf.inter + (r < 128 ? 0 : pf.inter) + mt * 128 + (r & 127);
+            ptx::prefetch_l2(pf.w13 + row * pf.hidden, (uint32_t)pf.bytes);
+        }
+    }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t_base = blockIdx.x * kCT, e_base = blockIdx.y * kCE;
     const int steps = (H + kStepElems - 1) / kStepElems;
@@ -386,7 +399,7 @@ int route_kernel_count() { return 2; }
 int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate,
                  const float *e_bias, const float *logit_offset, const int32_t *log2phys,
                  float *logits, int32_t *topk_ids, float *topk_w, int32_t *status,
-                 cudaStream_t s) {
+                 cudaStream_t s, const L2Prefetch *pf) {
     if (T == 0) return MOE_OK;
     const int E = cfg->num_experts, H = cfg->hidden;
     const dim3 grid((unsigned)ceil_div(T, kCT), (unsigned)ceil_div(E, kCE));
@@ -402,9 +415,10 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
                                cudaSuccess ? 0 : 1;
     });
     if (attr_rc[dev]) return MOE_ERR_CUDA;
+    const L2Prefetch none;
     gate_logits_kernel<<<grid, 256, smem, s>>>(static_cast<const uint16_t *>(x),
                                                static_cast<const uint16_t *>(w_gate),
-                                               logit_offset, logits, T, E, H);
+                                               logit_offset, logits, T, E, H, pf ? *pf : none);
     MOE_LAUNCH_CHECK();
 
     SelectArgs a;
