@@ -132,7 +132,9 @@ def setup(shape, seed, device):
         info = {"set_imbalance": round(after, 4), "set_imbalance_contiguous": round(before, 4),
                 "relayout_ms": round(ms, 3),
                 "relayout_gbs": round(reb.relayout_bytes / (ms * 1e-3) / 1e9, 1)}
-        inp = {k: v for k, v in layer._keep.items() if k != "log2phys"}
+        # the oracle's view: row-major weights in the same physical order (the
+        # layer holds its own tile-packed copy)
+        inp = synth.relayout_experts(inp, shape, np.argsort(log2phys))
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
     return inp, layer, log2phys, info
@@ -175,7 +177,7 @@ class Stepper:
         (they break the programmatic launch overlap at every boundary);
         record="top": events around the dominant kernel only."""
         moe, p, lay, s = self.moe, self.p, self.layer, self.layer.shape
-        cfg, w = lay.cfg, lay._keep
+        cfg, w, wl = lay.cfg, lay._keep, lay.expert_layout
         T, G, H, I = s.tokens, s.groups, s.hidden, s.inter
         rows = T * (s.top_k + s.num_shared)
         ev = []
@@ -204,7 +206,7 @@ class Stepper:
         if self.fused:   # decode batches: both expert GEMMs in one persistent kernel
             moe.expert_ffn(cfg, G, rows, p["xp"], p["xp_scales"], p["expert_offsets"], w["w13"],
                            w["w13_s"], w["w2"], w["w2_s"], p["h"], p["h_scales"], p["y"],
-                           p["ffn_sched"], self.sched_bytes, p["status"])
+                           p["ffn_sched"], self.sched_bytes, p["status"], w_layout=wl)
             mark()
             moe.combine(cfg, T, p["y"], p["row_of_slot"], p["topk_w"], p["expert_offsets"],
                         self.out, moe.OUT_F32)
@@ -213,18 +215,19 @@ class Stepper:
             return
         if self.wide:   # the layer's two-kernel path for wide batches
             moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"], p["expert_offsets"],
-                             w["w13"], w.get("w13_s"), p["gate_up"], moe.OUT_F32, p["status"])
+                             w["w13"], w.get("w13_s"), p["gate_up"], moe.OUT_F32, p["status"],
+                             w_layout=wl)
             moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, p["gate_up"], p["h"], p["h_scales"],
                             rows_dev=p["expert_offsets"] + 4 * G)
         else:
             moe.grouped_gemm_swiglu(cfg, G, I, H, rows, p["xp"],
                                     p["xp_scales"] if self.fp8 else None, p["expert_offsets"],
                                     w["w13"], w.get("w13_s"), p["h"],
-                                    p["h_scales"] if self.fp8 else None, p["status"])
+                                    p["h_scales"] if self.fp8 else None, p["status"], w_layout=wl)
         mark()
         moe.grouped_gemm(cfg, G, H, I, rows, p["h"], p["h_scales"] if self.fp8 else None,
                          p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_F32,
-                         p["status"])
+                         p["status"], w_layout=wl)
         mark()
         moe.combine(cfg, T, p["y"], p["row_of_slot"], p["topk_w"], p["expert_offsets"], self.out,
                     moe.OUT_F32)

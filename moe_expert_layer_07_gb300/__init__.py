@@ -19,7 +19,8 @@ __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_
            "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
            "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
            "count_coactivation", "affinity_permutation", "grouped_gemm_swiglu",
-           "expert_ffn", "expert_ffn_sched_bytes",
+           "expert_ffn", "expert_ffn_sched_bytes", "pack_expert_weights", "LAYOUT_ROWS",
+           "LAYOUT_TILES",
            "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
            "ACT_SILU_MUL"]
 
@@ -28,6 +29,7 @@ BF16, FP8 = 0, 1
 OUT_F32, OUT_BF16 = 0, 1
 ACT_IDENTITY, ACT_SILU_MUL = 0, 1
 DEV_BAD_EXPERT_ID, DEV_BAD_OFFSETS, DEV_TIMEOUT = 1, 2, 4
+LAYOUT_ROWS, LAYOUT_TILES = 0, 1
 
 
 class MoEError(RuntimeError):
@@ -46,7 +48,7 @@ class Config(ctypes.Structure):
 class Weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_gate", "e_bias", "logit_offset", "log2phys", "w13", "w13_scales", "w2",
-                 "w2_scales")]
+                 "w2_scales")] + [("expert_layout", ctypes.c_int32)]
 
 
 class WsLayout(ctypes.Structure):
@@ -66,7 +68,7 @@ _SIGS = {
     "moe_act_requant": [_CP, _I, _I, _P, _P, _P, _P, _P],
     "moe_permute_workspace_size": [_CP, _I, ctypes.POINTER(ctypes.c_size_t)],
     "moe_permute": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
-    "moe_grouped_gemm": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P],
+    "moe_grouped_gemm": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P],
     "moe_combine": [_CP, _I, _P, _P, _P, _P, _P, _I, _P],
     "moe_workspace_size": [_CP, ctypes.POINTER(ctypes.c_size_t)],
     "moe_layer_forward": [_CP, ctypes.POINTER(Weights), _I, _P, _P, _I, _P, ctypes.c_size_t, _P],
@@ -77,14 +79,15 @@ _SIGS = {
     "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
     "moe_permute_static_scratch": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_count_expert_rows": [_CP, _P, _P, _P],
-    "moe_grouped_gemm_swiglu": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "moe_grouped_gemm_swiglu": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P],
+    "moe_pack_expert_weights": [_CP, _I, _I, _I, _P, _P, _P],
     "moe_count_coactivation": [_CP, _I, _P, _P, _P, _P],
     "expert_affinity_permutation": [_P, _P, _I, _I, ctypes.c_double, _P, _P,
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
     "moe_relayout_experts": [_P, _P, _P, _I, ctypes.c_int64, _P, _P],
     "moe_selftest_ffn_flag_timeout": [_P, ctypes.c_size_t, _P, _P],
-    "moe_expert_ffn": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t,
-                       _P, _P],
+    "moe_expert_ffn": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
+                       ctypes.c_size_t, _P, _P],
 }
 
 
@@ -189,19 +192,33 @@ def permute_static_scratch(cfg: Config, T, topk_ids, x_rows, x_scales, expert_of
 
 
 def grouped_gemm(cfg: Config, groups, n_out, k_dim, rows, a, a_scales, expert_offsets, w,
-                 w_scales, c, c_dtype, status=None, stream=None):
+                 w_scales, c, c_dtype, status=None, stream=None, w_layout=None):
     _check(lib().moe_grouped_gemm(ctypes.byref(cfg), groups, n_out, k_dim, rows, _ptr(a),
                                   _ptr(a_scales), _ptr(expert_offsets), _ptr(w), _ptr(w_scales),
-                                  _ptr(c), c_dtype, _ptr(status), _stream(stream)),
+                                  LAYOUT_ROWS if w_layout is None else w_layout, _ptr(c),
+                                  c_dtype, _ptr(status), _stream(stream)),
            "moe_grouped_gemm")
 
 
 def grouped_gemm_swiglu(cfg: Config, groups, inter, k_dim, rows, a, a_scales, expert_offsets,
-                        w13, w13_scales, h, h_scales, status=None, stream=None):
+                        w13, w13_scales, h, h_scales, status=None, stream=None, w_layout=None):
     _check(lib().moe_grouped_gemm_swiglu(ctypes.byref(cfg), groups, inter, k_dim, rows, _ptr(a),
                                          _ptr(a_scales), _ptr(expert_offsets), _ptr(w13),
-                                         _ptr(w13_scales), _ptr(h), _ptr(h_scales), _ptr(status),
-                                         _stream(stream)), "moe_grouped_gemm_swiglu")
+                                         _ptr(w13_scales),
+                                         LAYOUT_ROWS if w_layout is None else w_layout, _ptr(h),
+                                         _ptr(h_scales), _ptr(status), _stream(stream)),
+           "moe_grouped_gemm_swiglu")
+
+
+def pack_expert_weights(cfg: Config, w, out=None, stream=None):
+    """W [groups, N, K] row-major -> the same tensor shape in MOE_LAYOUT_TILES
+    (a new tensor unless `out` is given)."""
+    import torch
+    out = torch.empty_like(w) if out is None else out
+    G, N, K = w.shape
+    _check(lib().moe_pack_expert_weights(ctypes.byref(cfg), G, N, K, _ptr(w), _ptr(out),
+                                         _stream(stream)), "moe_pack_expert_weights")
+    return out
 
 
 def expert_ffn_sched_bytes(groups, rows) -> int:
@@ -210,12 +227,14 @@ def expert_ffn_sched_bytes(groups, rows) -> int:
 
 
 def expert_ffn(cfg: Config, groups, rows, a, a_scales, expert_offsets, w13, w13_scales, w2,
-               w2_scales, h, h_scales, y, sched, sched_bytes, status=None, stream=None):
+               w2_scales, h, h_scales, y, sched, sched_bytes, status=None, stream=None,
+               w_layout=None):
     """Both expert GEMMs with SwiGLU between them, one persistent kernel (FP8)."""
     _check(lib().moe_expert_ffn(ctypes.byref(cfg), groups, rows, _ptr(a), _ptr(a_scales),
                                 _ptr(expert_offsets), _ptr(w13), _ptr(w13_scales), _ptr(w2),
-                                _ptr(w2_scales), _ptr(h), _ptr(h_scales), _ptr(y), _ptr(sched),
-                                sched_bytes, _ptr(status), _stream(stream)), "moe_expert_ffn")
+                                _ptr(w2_scales), LAYOUT_ROWS if w_layout is None else w_layout,
+                                _ptr(h), _ptr(h_scales), _ptr(y), _ptr(sched), sched_bytes,
+                                _ptr(status), _stream(stream)), "moe_expert_ffn")
 
 
 def combine(cfg: Config, T, y, row_of_slot, topk_w, expert_offsets, out, out_dtype, stream=None):
@@ -314,13 +333,22 @@ class MoELayer:
 
     weights: dict of device tensors with keys wg, e_bias, logit_offset, w13,
     w13_s, w2, w2_s (expert weights in physical order, shared experts last)
-    and optionally log2phys (int32).
+    and optionally log2phys (int32) and expert_layout (LAYOUT_*, default
+    row-major).  With pack_weights (the default) row-major expert weights are
+    packed once into 128 x 128-byte tiles (MOE_LAYOUT_TILES), which the
+    tensor-core kernels stream faster; the caller's tensors are not changed.
     """
 
-    def __init__(self, shape, weights: dict, max_tokens: int | None = None, log2phys=None):
+    def __init__(self, shape, weights: dict, max_tokens: int | None = None, log2phys=None,
+                 pack_weights: bool = True):
         import torch
         self.cfg = make_config(shape, max_tokens)
         self.shape = shape
+        weights = dict(weights)
+        if pack_weights and weights.get("expert_layout", LAYOUT_ROWS) == LAYOUT_ROWS:
+            weights["w13"] = pack_expert_weights(self.cfg, weights["w13"])
+            weights["w2"] = pack_expert_weights(self.cfg, weights["w2"])
+            weights["expert_layout"] = LAYOUT_TILES
         self.set_weights(weights, log2phys)
         self.ws_bytes = workspace_size(self.cfg)
         self.layout = workspace_layout(self.cfg)
@@ -336,11 +364,14 @@ class MoELayer:
         else:
             keep.pop("log2phys", None)
         self._keep = keep
+        keep.setdefault("expert_layout", LAYOUT_ROWS)
+        self.expert_layout = keep["expert_layout"]
         self.weights = Weights(w_gate=_ptr(keep["wg"]), e_bias=_ptr(keep.get("e_bias")),
                                logit_offset=_ptr(keep.get("logit_offset")),
                                log2phys=_ptr(keep.get("log2phys")), w13=_ptr(keep["w13"]),
                                w13_scales=_ptr(keep.get("w13_s")), w2=_ptr(keep["w2"]),
-                               w2_scales=_ptr(keep.get("w2_s")))
+                               w2_scales=_ptr(keep.get("w2_s")),
+                               expert_layout=self.expert_layout)
 
     def forward(self, x, out, out_dtype=OUT_F32, T=None, stream=None):
         """x bf16 [T, H] and out [T, H] (fp32 or bf16) device tensors."""

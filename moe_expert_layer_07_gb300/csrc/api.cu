@@ -51,6 +51,13 @@ namespace {
 
 bool al16(const void *p) { return p == nullptr || aligned16(p); }
 
+bool layout_ok(int32_t l) { return l == MOE_LAYOUT_ROWS || l == MOE_LAYOUT_TILES; }
+
+// Tiled weights are addressed as rows of a [tiles * 128, 128-byte] view.
+bool tiled_fits(int64_t groups, int64_t n_out, int64_t k_dim, bool fp8) {
+    return groups * n_out * (k_dim / (fp8 ? 128 : 64)) <= INT32_MAX;
+}
+
 // Groups averaging 16 rows or more: the gate/up GEMM with 64-row tiles and a
 // separate SiLU-mul kernel beats the fused SwiGLU epilogue (whose two fp32
 // accumulators keep it at 32-row tiles); decode batches take the fused path.
@@ -181,43 +188,52 @@ int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_ids, const
 int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32_t k_dim,
                      int32_t rows, const void *a, const float *a_scales,
                      const int32_t *expert_offsets, const void *w, const float *w_scales,
-                     void *c, int32_t c_dtype, int32_t *dev_status, void *stream) {
+                     int32_t w_layout, void *c, int32_t c_dtype, int32_t *dev_status,
+                     void *stream) {
     int rc = check_config(cfg);
     if (rc) return rc;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
     if (groups <= 0 || rows < 0 || n_out <= 0 || k_dim <= 0) return MOE_ERR_INVALID_ARG;
+    if (!layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
     if (c_dtype != MOE_OUT_F32 && c_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
     if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (n_out % 128 || k_dim % (fp8 ? 128 : 64)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (fp8 && k_dim > 7168) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)groups * n_out > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (w_layout == MOE_LAYOUT_TILES && !tiled_fits(groups, n_out, k_dim, fp8))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return MOE_OK;
     if (!a || !w || !c || !expert_offsets || (fp8 && (!a_scales || !w_scales)))
         return MOE_ERR_INVALID_ARG;
     if (!al16(a) || !al16(w) || !al16(c)) return MOE_ERR_INVALID_ARG;
     return launch_grouped_gemm(fp8, groups, n_out, k_dim, rows, a, a_scales, expert_offsets, w,
-                               w_scales, c, c_dtype, dev_status, static_cast<cudaStream_t>(stream));
+                               w_scales, w_layout == MOE_LAYOUT_TILES, c, c_dtype, dev_status,
+                               static_cast<cudaStream_t>(stream));
 }
 
 int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter, int32_t k_dim,
                             int32_t rows, const void *a, const float *a_scales,
                             const int32_t *expert_offsets, const void *w13,
-                            const float *w13_scales, void *h, float *h_scales,
+                            const float *w13_scales, int32_t w_layout, void *h, float *h_scales,
                             int32_t *dev_status, void *stream) {
     int rc = check_config(cfg);
     if (rc) return rc;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
     if (groups <= 0 || rows < 0 || inter <= 0 || k_dim <= 0) return MOE_ERR_INVALID_ARG;
+    if (!layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
     if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (inter % 128 || k_dim % (fp8 ? 128 : 64)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (fp8 && k_dim > 7168) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)groups * 2 * inter > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (w_layout == MOE_LAYOUT_TILES && !tiled_fits(groups, 2 * (int64_t)inter, k_dim, fp8))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return MOE_OK;
     if (!a || !w13 || !h || !expert_offsets || (fp8 && (!a_scales || !w13_scales || !h_scales)))
         return MOE_ERR_INVALID_ARG;
     if (!al16(a) || !al16(w13) || !al16(h)) return MOE_ERR_INVALID_ARG;
     return launch_grouped_gemm_swiglu(fp8, groups, inter, k_dim, rows, a, a_scales,
-                                      expert_offsets, w13, w13_scales, h, h_scales, dev_status,
+                                      expert_offsets, w13, w13_scales,
+                                      w_layout == MOE_LAYOUT_TILES, h, h_scales, dev_status,
                                       static_cast<cudaStream_t>(stream));
 }
 
@@ -228,12 +244,12 @@ size_t moe_expert_ffn_sched_bytes(int32_t groups, int32_t rows) {
 
 int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const void *a,
                    const float *a_scales, const int32_t *expert_offsets, const void *w13,
-                   const float *w13_scales, const void *w2, const float *w2_scales, void *h,
-                   float *h_scales, float *y, int32_t *sched, size_t sched_bytes,
-                   int32_t *dev_status, void *stream) {
+                   const float *w13_scales, const void *w2, const float *w2_scales,
+                   int32_t w_layout, void *h, float *h_scales, float *y, int32_t *sched,
+                   size_t sched_bytes, int32_t *dev_status, void *stream) {
     int rc = check_config(cfg);
     if (rc) return rc;
-    if (groups <= 0 || rows < 0) return MOE_ERR_INVALID_ARG;
+    if (groups <= 0 || rows < 0 || !layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
     if (cfg->dtype != MOE_DTYPE_FP8_BLOCK128 || cfg->inter % 256 || groups > 1024)
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)groups * 2 * cfg->inter > INT32_MAX || (int64_t)groups * cfg->hidden > INT32_MAX)
@@ -245,8 +261,9 @@ int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const vo
     if (!al16(a) || !al16(w13) || !al16(w2) || !al16(h) || !al16(y)) return MOE_ERR_INVALID_ARG;
     if (sched_bytes < ffn_sched_bytes(groups, rows)) return MOE_ERR_WORKSPACE_TOO_SMALL;
     return launch_expert_ffn(groups, cfg->hidden, cfg->inter, rows, a, a_scales, expert_offsets,
-                             w13, w13_scales, w2, w2_scales, h, h_scales, y, sched, false,
-                             dev_status, static_cast<cudaStream_t>(stream));
+                             w13, w13_scales, w2, w2_scales, w_layout == MOE_LAYOUT_TILES, h,
+                             h_scales, y, sched, false, dev_status,
+                             static_cast<cudaStream_t>(stream));
 }
 
 int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
@@ -299,6 +316,11 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     if (!w->w_gate || !w->w13 || !w->w2 || (fp8 && (!w->w13_scales || !w->w2_scales)))
         return MOE_ERR_INVALID_ARG;
     if (w->e_bias && cfg->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+    if (!layout_ok(w->expert_layout)) return MOE_ERR_INVALID_ARG;
+    const bool tiled = w->expert_layout == MOE_LAYOUT_TILES;
+    if (tiled && (!tiled_fits(groups_of(cfg), 2 * (int64_t)cfg->inter, cfg->hidden, fp8) ||
+                  !tiled_fits(groups_of(cfg), cfg->hidden, cfg->inter, fp8)))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (!al16(x) || !al16(out) || !al16(ws) || !al16(w->w_gate) || !al16(w->w13) ||
         !al16(w->w2))
         return MOE_ERR_INVALID_ARG;
@@ -338,6 +360,7 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
         pf.groups = G;
         pf.units = 2 * sm_count();
         pf.bytes = H < 1024 ? H : 1024;
+        pf.tiled = tiled;
     }
     rc = launch_route(cfg, T, x, w->w_gate, w->e_bias, w->logit_offset, w->log2phys, logits, ids,
                       tw, status, s, fused ? &pf : nullptr);
@@ -358,7 +381,7 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     if (fused) {
         rc = launch_expert_ffn(G, H, I, rows, base + L.xp,
                                reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
-                               w->w13_scales, w->w2, w->w2_scales, base + L.h,
+                               w->w13_scales, w->w2, w->w2_scales, tiled, base + L.h,
                                reinterpret_cast<float *>(base + L.h_scales),
                                reinterpret_cast<float *>(base + L.y),
                                reinterpret_cast<int32_t *>(base + L.ffn_sched), true, status, s);
@@ -368,20 +391,21 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     if (wide_rows(cfg, T)) {
         rc = launch_grouped_gemm(fp8, G, 2 * I, H, rows, base + L.xp,
                                  reinterpret_cast<const float *>(base + L.xp_scales), offsets,
-                                 w->w13, w->w13_scales, base + L.gate_up, MOE_OUT_F32, status, s);
+                                 w->w13, w->w13_scales, tiled, base + L.gate_up, MOE_OUT_F32,
+                                 status, s);
         if (rc) return rc;
         rc = launch_act_requant(cfg, MOE_ACT_SILU_MUL, rows, offsets + G, base + L.gate_up,
                                 base + L.h, reinterpret_cast<float *>(base + L.h_scales), s);
     } else {
         rc = launch_grouped_gemm_swiglu(fp8, G, I, H, rows, base + L.xp,
                                         reinterpret_cast<const float *>(base + L.xp_scales),
-                                        offsets, w->w13, w->w13_scales, base + L.h,
+                                        offsets, w->w13, w->w13_scales, tiled, base + L.h,
                                         reinterpret_cast<float *>(base + L.h_scales), status, s);
     }
     if (rc) return rc;
     rc = launch_grouped_gemm(fp8, G, H, I, rows, base + L.h,
                              reinterpret_cast<const float *>(base + L.h_scales), offsets, w->w2,
-                             w->w2_scales, base + L.y, MOE_OUT_F32, status, s);
+                             w->w2_scales, tiled, base + L.y, MOE_OUT_F32, status, s);
     if (rc) return rc;
     return launch_combine(cfg, T, base + L.y, ros, tw, offsets, out, out_dtype, s);
 }

@@ -91,6 +91,7 @@ struct FfnArgs {
     float *h_scales;           // [rows, inter/128]
     float *y;                  // [rows, hidden]
     int32_t *sched;            // [0] next unit; [1 + j] finished gate/up tiles of activation tile j
+    int w_tiled;               // W13, W2 in MOE_LAYOUT_TILES
     int32_t *status;
 };
 
@@ -277,6 +278,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint64_t pol_w =
                     (s_off[u.g + 1] - s_off[u.g] > kBN) ? pol_w_shared : pol_w_once;
                 const int wrow = u.down ? u.g * H + u.mt * kBM : u.g * 2 * I + u.mt * kBM;
+                // tiled weights: box (128-row block b, K block kb) at rows
+                // (b * KB + kb) * 128 of a [tiles * 128, 128-byte] view
+                const int tb_gate = (u.g * 2 * MT1 + u.mt) * KB1;
+                const int tb_up = tb_gate + MT1 * KB1;
+                const int tb_down = (u.g * MT2 + u.mt) * KB2;
+                const bool tiled = args.w_tiled != 0;
                 for (int ks = 0; ks < nsteps; ++ks) {
                     if (!wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag,
                                       args.status, MOE_DEV_TIMEOUT)) {
@@ -288,8 +295,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     if (!u.down) {
-                        tma_load_2d(sa, &tmW13, ks * 128, wrow, fb, pol_w);            // gate rows
-                        tma_load_2d(sa + kABytes, &tmW13, ks * 128, wrow + I, fb, pol_w);   // up rows
+                        if (tiled) {
+                            tma_load_2d(sa, &tmW13, 0, (tb_gate + ks) * kBM, fb, pol_w);
+                            tma_load_2d(sa + kABytes, &tmW13, 0, (tb_up + ks) * kBM, fb, pol_w);
+                        } else {
+                            tma_load_2d(sa, &tmW13, ks * 128, wrow, fb, pol_w);            // gate
+                            tma_load_2d(sa + kABytes, &tmW13, ks * 128, wrow + I, fb, pol_w);   // up
+                        }
                         for (int b = 0; b < nbox; ++b)
                             tma_load_2d(sb + b * kBoxRows * 128, &tmX, ks * 128,
                                         u.row0 + b * kBoxRows, fb, pol_a);
@@ -297,7 +309,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                         for (int hk = 0; hk < 2; ++hk) {
                             const int k0 = (2 * ks + hk) * 128;
-                            tma_load_2d(sa + hk * kABytes, &tmW2, k0, wrow, fb, pol_w);
+                            if (tiled)
+                                tma_load_2d(sa + hk * kABytes, &tmW2, 0,
+                                            (tb_down + 2 * ks + hk) * kBM, fb, pol_w);
+                            else
+                                tma_load_2d(sa + hk * kABytes, &tmW2, k0, wrow, fb, pol_w);
                             for (int b = 0; b < nbox; ++b)
                                 tma_load_2d(sb + hk * kBBytes + b * kBoxRows * 128, &tmH, k0,
                                             u.row0 + b * kBoxRows, fb, pol_a);
@@ -594,9 +610,9 @@ size_t ffn_sched_bytes(int groups, int rows) {
 
 int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *xp,
                       const float *xp_scales, const int32_t *offsets, const void *w13,
-                      const float *w13_scales, const void *w2, const float *w2_scales, void *h,
-                      float *h_scales, float *y, int32_t *sched, bool sched_zeroed,
-                      int32_t *status, cudaStream_t s) {
+                      const float *w13_scales, const void *w2, const float *w2_scales,
+                      bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
+                      bool sched_zeroed, int32_t *status, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
     static std::once_flag attr_once[64];
     static int attr_rc[64];
@@ -610,9 +626,14 @@ int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *x
     });
     if (attr_rc[dev]) return MOE_ERR_CUDA;
     CUtensorMap tmW13, tmX, tmW2, tmH;
-    if (!encode_2d(&tmW13, w13, true, (uint64_t)hidden, (uint64_t)groups * 2 * inter, kBM) ||
+    const uint64_t w13_rows = (uint64_t)groups * 2 * inter, w2_rows = (uint64_t)groups * hidden;
+    const bool w_ok =
+        w_tiled ? encode_2d(&tmW13, w13, true, 128, w13_rows * (hidden / 128), kBM) &&
+                      encode_2d(&tmW2, w2, true, 128, w2_rows * (inter / 128), kBM)
+                : encode_2d(&tmW13, w13, true, (uint64_t)hidden, w13_rows, kBM) &&
+                      encode_2d(&tmW2, w2, true, (uint64_t)inter, w2_rows, kBM);
+    if (!w_ok ||
         !encode_2d(&tmX, xp, true, (uint64_t)hidden, (uint64_t)rows, kBoxRows) ||
-        !encode_2d(&tmW2, w2, true, (uint64_t)inter, (uint64_t)groups * hidden, kBM) ||
         !encode_2d(&tmH, h, true, (uint64_t)inter, (uint64_t)rows, kBoxRows))
         return MOE_ERR_CUDA;
     if (!sched_zeroed) MOE_CUDA_TRY(cudaMemsetAsync(sched, 0, ffn_sched_bytes(groups, rows), s));
@@ -629,6 +650,7 @@ int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *x
     a.h_scales = h_scales;
     a.y = y;
     a.sched = sched;
+    a.w_tiled = w_tiled;
     a.status = status;
     const int64_t units_bound =
         (int64_t)(inter / kBM + hidden / kBM) * (groups + ceil_div(rows, kBN));
@@ -707,7 +729,7 @@ extern "C" MOE_API int moe_selftest_ffn_flag_timeout(void *scratch, size_t scrat
     return launch_expert_ffn(1, kSelftestH, kSelftestI, 1, b + L.xp,
                              reinterpret_cast<const float *>(b + L.xs), off, b + L.w13,
                              reinterpret_cast<const float *>(b + L.w13s), b + L.w2,
-                             reinterpret_cast<const float *>(b + L.w2s), b + L.h,
+                             reinterpret_cast<const float *>(b + L.w2s), false, b + L.h,
                              reinterpret_cast<float *>(b + L.hs), reinterpret_cast<float *>(b + L.y),
                              sched, true, dev_status, s);
 }

@@ -93,6 +93,7 @@ struct GemmArgs {
     void *c;          // C [rows, n_out]; SwiGLU: h [rows, n_out/2] (e4m3 or bf16)
     float *h_scales;  // SwiGLU + FP8: [rows, n_out/256]
     int c_bf16;
+    int w_tiled;      // W in MOE_LAYOUT_TILES
     int32_t *status;
 };
 
@@ -246,6 +247,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const uint32_t bytes = S::kNA * S::kABytes + nbox * kBoxRows * 128;
                 const int wrow = tl.g * args.n_out + tl.mt * kBM;   // SwiGLU: gate rows
                 const int wrow_up = wrow + args.n_out / 2;          // SwiGLU: up rows
+                // tiled W: the box of (128-row block b, K block kb) is rows
+                // (b * KB + kb) * 128 of a [tiles * 128, 128-byte] view
+                const int tb = (tl.g * MTW + tl.mt) * KB;
+                const int tb_up = tb + (MTW / 2) * KB;
                 const uint64_t pol_w =
                     (s_off[tl.g + 1] - s_off[tl.g] > BN) ? pol_w_shared : pol_w_once;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -258,8 +263,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const uint32_t sb = sa + S::kNA * S::kABytes;
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
-                    tma_load_2d(sa, &tmW, kb * S::kKPerStage, wrow, fb, pol_w);
-                    if (SW) tma_load_2d(sa + S::kABytes, &tmW, kb * S::kKPerStage, wrow_up, fb, pol_w);
+                    if (args.w_tiled) {
+                        tma_load_2d(sa, &tmW, 0, (tb + kb) * kBM, fb, pol_w);
+                        if (SW) tma_load_2d(sa + S::kABytes, &tmW, 0, (tb_up + kb) * kBM, fb, pol_w);
+                    } else {
+                        tma_load_2d(sa, &tmW, kb * S::kKPerStage, wrow, fb, pol_w);
+                        if (SW)
+                            tma_load_2d(sa + S::kABytes, &tmW, kb * S::kKPerStage, wrow_up, fb,
+                                        pol_w);
+                    }
                     for (int b = 0; b < nbox; ++b)
                         tma_load_2d(sb + b * kBoxRows * 128, &tmA, kb * S::kKPerStage,
                                     tl.row0 + b * kBoxRows, fb, pol_a);
@@ -632,8 +644,12 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
     });
     if (attr_rc[dev]) return MOE_ERR_CUDA;
     CUtensorMap tmW, tmA;
-    if (!encode_2d(&tmW, w, FP8, (uint64_t)args.k_dim, (uint64_t)args.groups * args.n_out, kBM))
-        return MOE_ERR_CUDA;
+    const bool tmw_ok =
+        args.w_tiled
+            ? encode_2d(&tmW, w, FP8, (uint64_t)Sh::kKPerStage,
+                        (uint64_t)args.groups * args.n_out * (args.k_dim / Sh::kKPerStage), kBM)
+            : encode_2d(&tmW, w, FP8, (uint64_t)args.k_dim, (uint64_t)args.groups * args.n_out, kBM);
+    if (!tmw_ok) return MOE_ERR_CUDA;
     if (!encode_2d(&tmA, a, FP8, (uint64_t)args.k_dim, (uint64_t)args.rows, kBoxRows))
         return MOE_ERR_CUDA;
     const int64_t tiles_bound =
@@ -650,8 +666,8 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
 
 int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, const void *a,
                         const float *a_scales, const int32_t *offsets, const void *w,
-                        const float *w_scales, void *c, int c_dtype, int32_t *status,
-                        cudaStream_t s) {
+                        const float *w_scales, bool w_tiled, void *c, int c_dtype,
+                        int32_t *status, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
     GemmArgs args;
     args.groups = groups;
@@ -664,6 +680,7 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     args.c = c;
     args.h_scales = nullptr;
     args.c_bf16 = c_dtype == MOE_OUT_BF16;
+    args.w_tiled = w_tiled;
     args.status = status;
     // Decode-sized groups (a few rows each) stream best with 32-row tiles;
     // larger groups re-read each weight tile fewer times with 64-row tiles.
@@ -675,7 +692,7 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
 
 int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int rows,
                                const void *a, const float *a_scales, const int32_t *offsets,
-                               const void *w13, const float *w13_scales, void *h,
+                               const void *w13, const float *w13_scales, bool w_tiled, void *h,
                                float *h_scales, int32_t *status, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
     GemmArgs args;
@@ -689,6 +706,7 @@ int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int r
     args.c = h;
     args.h_scales = h_scales;
     args.c_bf16 = !fp8;
+    args.w_tiled = w_tiled;
     args.status = status;
     if (fp8) return launch_impl<true, 32, 2, true>(args, a, w13, s);
     return launch_impl<false, 32, 2, true>(args, a, w13, s);

@@ -36,6 +36,7 @@ int sm_count();
 struct L2Prefetch {
     const uint8_t *w13 = nullptr;   // e4m3 [groups, 2*inter, hidden]
     int hidden = 0, inter = 0, groups = 0, units = 0, bytes = 0;
+    int tiled = 0;                  // MOE_LAYOUT_TILES: the K prefix of a row block is contiguous
 };
 int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate,
                  const float *e_bias, const float *logit_offset, const int32_t *log2phys,
@@ -50,11 +51,11 @@ int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const 
                    int32_t *status, cudaStream_t s);
 int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, const void *a,
                         const float *a_scales, const int32_t *offsets, const void *w,
-                        const float *w_scales, void *c, int c_dtype, int32_t *status,
-                        cudaStream_t s);
+                        const float *w_scales, bool w_tiled, void *c, int c_dtype,
+                        int32_t *status, cudaStream_t s);
 int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int rows,
                                const void *a, const float *a_scales, const int32_t *offsets,
-                               const void *w13, const float *w13_scales, void *h,
+                               const void *w13, const float *w13_scales, bool w_tiled, void *h,
                                float *h_scales, int32_t *status, cudaStream_t s);
 // The experts' FFN in one persistent kernel (FP8): gate/up + SwiGLU + requant,
 // then down.  `sched` holds ffn_sched_bytes(groups, rows) bytes; it is
@@ -62,9 +63,9 @@ int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int r
 size_t ffn_sched_bytes(int groups, int rows);
 int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *xp,
                       const float *xp_scales, const int32_t *offsets, const void *w13,
-                      const float *w13_scales, const void *w2, const float *w2_scales, void *h,
-                      float *h_scales, float *y, int32_t *sched, bool sched_zeroed,
-                      int32_t *status, cudaStream_t s);
+                      const float *w13_scales, const void *w2, const float *w2_scales,
+                      bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
+                      bool sched_zeroed, int32_t *status, cudaStream_t s);
 int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *row_of_slot,
                    const float *topk_w, const int32_t *offsets, void *out, int out_dtype,
                    cudaStream_t s);

@@ -68,7 +68,22 @@ __global__ void __launch_bounds__(256)
                        int E, int H, const L2Prefetch pf) {
     extern __shared__ __align__(16) uint8_t smem[];
     ptx::pdl_launch_dependents();   // the selection kernel may take its SM slots now
-    if (pf.units > 0) {   // L2 prefetch of the expert FFN's first weight rows (a hint)
+    if (pf.units > 0 && pf.tiled) {
+        // tiled weights: the first K blocks of a 128-row block are one
+        // contiguous run of 16 KB tiles; one prefetch per tile
+        const int mt1 = pf.inter / 128, kbt = pf.hidden / 128, nt = pf.bytes / 128;
+        const long jobs = (long)pf.units * 2 * nt;
+        const long nthreads = (long)gridDim.x * gridDim.y * blockDim.x;
+        for (long j = ((long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
+             j < jobs; j += nthreads) {
+            const int u = (int)(j / (2 * nt)), r = (int)(j % (2 * nt));
+            const int g = u / mt1, mt = u - g * mt1;
+            if (g >= pf.groups) break;
+            const long block = (long)g * 2 * mt1 + (r < nt ? 0 : mt1) + mt;
+            const long tile = block * kbt + (r % nt);
+            ptx::prefetch_l2(pf.w13 + tile * (128 * 128), 128 * 128);
+        }
+    } else if (pf.units > 0) {   // L2 prefetch of the expert FFN's first weight rows (a hint)
         const int mt1 = pf.inter / 128;
         const long jobs = (long)pf.units * 256;
         const long nthreads = (long)gridDim.x * gridDim.y * blockDim.x;

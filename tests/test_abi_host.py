@@ -94,9 +94,21 @@ def test_bad_arguments_are_rejected_before_launch(L):
     assert L.moe_route(ctypes.byref(bad), 4, fake, fake, None, None, None, fake, fake, fake,
                        None, None) == -2
     assert L.moe_grouped_gemm(ctypes.byref(cfg), 3, 200, 128, 10, fake, fake, fake, fake, fake,
-                              fake, 0, None, None) == -2
+                              0, fake, 0, None, None) == -2
     assert L.moe_grouped_gemm(ctypes.byref(cfg), 2000, 128, 128, 10, fake, fake, fake, fake,
-                              fake, fake, 0, None, None) == -2
+                              fake, 0, fake, 0, None, None) == -2
+    # unknown weight layout
+    assert L.moe_grouped_gemm(ctypes.byref(cfg), 3, 256, 128, 10, fake, fake, fake, fake, fake,
+                              7, fake, 0, None, None) == -1
+    assert L.moe_grouped_gemm_swiglu(ctypes.byref(cfg), 3, 256, 128, 10, fake, fake, fake, fake,
+                                     fake, 2, fake, fake, None, None) == -1
+    # packing: shapes and overlap
+    assert L.moe_pack_expert_weights(ctypes.byref(cfg), 2, 200, 128, fake, P(0x100000),
+                                     None) == -2
+    assert L.moe_pack_expert_weights(ctypes.byref(cfg), 2, 256, 128, fake, P(0x1000 + 4096),
+                                     None) == -1
+    assert L.moe_pack_expert_weights(ctypes.byref(cfg), 2, 256, 128, P(0x1008), P(0x100000),
+                                     None) == -1
     # workspace too small
     need = moe.permute_workspace_size(cfg, 37)
     assert L.moe_permute(ctypes.byref(cfg), 37, fake, fake, fake, fake, fake, fake, fake, fake,
@@ -117,15 +129,19 @@ def test_bad_arguments_are_rejected_before_launch(L):
                        None, None) == -1
     # T beyond max_tokens
     w = moe.Weights(w_gate=0x1000, w13=0x1000, w2=0x1000, w13_scales=0x1000, w2_scales=0x1000)
+    bad_layout = moe.Weights(w_gate=0x1000, w13=0x1000, w2=0x1000, w13_scales=0x1000,
+                             w2_scales=0x1000, expert_layout=3)
+    assert L.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(bad_layout), 4, fake, fake, 0,
+                               fake, 1 << 40, None) == -1
     assert L.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 38, fake, fake, 0, fake,
                                1 << 40, None) == -1
     assert L.moe_layer_forward(ctypes.byref(cfg), ctypes.byref(w), 4, fake, fake, 0, fake,
                                16, None) == -3
     # the one-kernel expert FFN: FP8 with inter % 256 == 0 only, enough scratch
     r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
-    ffn = lambda c, groups, rows, nbytes: L.moe_expert_ffn(
-        ctypes.byref(c), groups, rows, fake, fake, fake, fake, fake, fake, fake, fake, fake, fake,
-        fake, nbytes, None, None)
+    ffn = lambda c, groups, rows, nbytes, layout=0: L.moe_expert_ffn(
+        ctypes.byref(c), groups, rows, fake, fake, fake, fake, fake, fake, fake, layout, fake,
+        fake, fake, fake, nbytes, None, None)
     need = moe.expert_ffn_sched_bytes(257, 1152)
     assert need == 4 * (1 + 257 + 36)
     assert ffn(b16, 9, 10, 1 << 20) == -2
@@ -133,10 +149,11 @@ def test_bad_arguments_are_rejected_before_launch(L):
     assert ffn(r1, 257, 1152, need - 4) == -3
     assert ffn(r1, 0, 10, need) == -1
     assert ffn(r1, 2000, 10, 1 << 20) == -2
+    assert ffn(r1, 257, 1152, need, layout=5) == -1
     assert L.moe_expert_ffn(ctypes.byref(r1), 257, 1152, P(0x1001), fake, fake, fake, fake, fake,
-                            fake, fake, fake, fake, fake, need, None, None) == -1
+                            fake, 0, fake, fake, fake, fake, need, None, None) == -1
     assert L.moe_expert_ffn(ctypes.byref(r1), 257, 0, None, None, None, None, None, None, None,
-                            None, None, None, None, 0, None, None) == 0
+                            0, None, None, None, None, 0, None, None) == 0
     # the FFN flag self-test needs its scratch
     n = L.moe_selftest_ffn_flag_timeout_scratch_bytes()
     assert 0 < n < (1 << 20)
