@@ -39,6 +39,21 @@ static_assert(kTB * kEB == 32, "one output per lane");
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
 
+// Two independent fp32 FMAs in one instruction (each lane an IEEE fma, the
+// same result as fmaf): d = a * b + c on {lo, hi} pairs.
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack2(float lo, float hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+__device__ __forceinline__ float lo2(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float hi2(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+
 // element e (0..7, increasing h) of 8 packed bf16 values, widened to fp32
 __device__ __forceinline__ float bf_elem(const uint4 &a, int e) {
     const uint32_t w = e < 2 ? a.x : e < 4 ? a.y : e < 6 ? a.z : a.w;
@@ -117,11 +132,12 @@ __global__ void __launch_bounds__(256)
         }
     };
 
-    float acc[kTB][kEB];
+    // accumulators of experts (2p, 2p + 1) side by side for the paired FMA
+    uint64_t acc2[kTB][kEB / 2];
 #pragma unroll
     for (int i = 0; i < kTB; ++i)
 #pragma unroll
-        for (int j = 0; j < kEB; ++j) acc[i][j] = 0.0f;
+        for (int p = 0; p < kEB / 2; ++p) acc2[i][p] = 0ull;
     const int wt = warp >> 1, we = warp & 1;   // warp tile: tokens 4wt.., experts 8we..
 
 #pragma unroll
@@ -144,18 +160,22 @@ __global__ void __launch_bounds__(256)
             wv[j] = *reinterpret_cast<const uint4 *>(buf + (kCT + we * kEB + j) * (kStepElems * 2) + lane * 16);
         // outer products over the chunk's 8 elements: each bf16 value is
         // widened once per step, and every accumulator still takes its 8
-        // products in increasing h
+        // products in increasing h (two accumulators per paired FMA)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            float xf[kTB], wf[kEB];
+            uint64_t x2[kTB], w2[kEB / 2];
 #pragma unroll
-            for (int i = 0; i < kTB; ++i) xf[i] = bf_elem(xv[i], e);
+            for (int i = 0; i < kTB; ++i) {
+                const float xf = bf_elem(xv[i], e);
+                x2[i] = pack2(xf, xf);
+            }
 #pragma unroll
-            for (int j = 0; j < kEB; ++j) wf[j] = bf_elem(wv[j], e);
+            for (int p = 0; p < kEB / 2; ++p)
+                w2[p] = pack2(bf_elem(wv[2 * p], e), bf_elem(wv[2 * p + 1], e));
 #pragma unroll
             for (int i = 0; i < kTB; ++i)
 #pragma unroll
-                for (int j = 0; j < kEB; ++j) acc[i][j] = fmaf(xf[i], wf[j], acc[i][j]);
+                for (int p = 0; p < kEB / 2; ++p) acc2[i][p] = fma2(x2[i], w2[p], acc2[i][p]);
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -165,7 +185,7 @@ __global__ void __launch_bounds__(256)
     for (int i = 0; i < kTB; ++i)
 #pragma unroll
         for (int j = 0; j < kEB; ++j) {
-            float v = acc[i][j];
+            float v = (j & 1) ? hi2(acc2[i][j >> 1]) : lo2(acc2[i][j >> 1]);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
             if (lane == i * kEB + j) mine = v;
