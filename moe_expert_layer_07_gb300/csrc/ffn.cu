@@ -95,6 +95,18 @@ struct FfnArgs {
     int32_t *status;
 };
 
+// Two independent IEEE fp32 FMAs in one instruction (the bits of two fmaf).
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+
 struct Unit {
     bool down;
     int g, mt, j, row0, nvalid;
@@ -432,11 +444,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
             const int nchunks = (u.nvalid + 15) / 16;
             const bool row_ok = lane < u.nvalid;   // lane n holds activation row n's scale
-            float acc[kBN], accu[kBN];
+            // columns (2p, 2p + 1) side by side for the paired FMA
+            uint64_t acc2[kBN / 2], accu2[kBN / 2];
 #pragma unroll
-            for (int n = 0; n < kBN; ++n) {
-                acc[n] = 0.0f;
-                accu[n] = 0.0f;
+            for (int p = 0; p < kBN / 2; ++p) {
+                acc2[p] = 0ull;
+                accu2[p] = 0ull;
             }
             const int KB = u.down ? KB2 : KB1;
             const float *wsp, *wup = nullptr, *xsp;
@@ -500,12 +513,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     if (c < nchunks) {
 #pragma unroll
                         for (int j4 = 0; j4 < 4; ++j4) {
-                            const float4 f = reinterpret_cast<const float4 *>(sxw)[c * 4 + j4];
-                            const int n = c * 16 + j4 * 4;
-                            acc[n] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, acc[n]);
-                            acc[n + 1] = fmaf(__uint_as_float(v[c][j4 * 4 + 1]), f.y, acc[n + 1]);
-                            acc[n + 2] = fmaf(__uint_as_float(v[c][j4 * 4 + 2]), f.z, acc[n + 2]);
-                            acc[n + 3] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, acc[n + 3]);
+                            const uint4 f = reinterpret_cast<const uint4 *>(sxw)[c * 4 + j4];
+                            const int p = (c * 16 + j4 * 4) / 2;
+                            acc2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]), pack2(f.x, f.y),
+                                           acc2[p]);
+                            acc2[p + 1] = fma2(pack2(v[c][j4 * 4 + 2], v[c][j4 * 4 + 3]),
+                                               pack2(f.z, f.w), acc2[p + 1]);
                         }
                     }
                 if (!u.down) {   // up rows: same activation scales, their own block scale
@@ -521,13 +534,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         if (c < nchunks) {
 #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4) {
-                                const float4 f =
-                                    reinterpret_cast<const float4 *>(sxw + kBN)[c * 4 + j4];
-                                const int n = c * 16 + j4 * 4;
-                                accu[n] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, accu[n]);
-                                accu[n + 1] = fmaf(__uint_as_float(v[c][j4 * 4 + 1]), f.y, accu[n + 1]);
-                                accu[n + 2] = fmaf(__uint_as_float(v[c][j4 * 4 + 2]), f.z, accu[n + 2]);
-                                accu[n + 3] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, accu[n + 3]);
+                                const uint4 f =
+                                    reinterpret_cast<const uint4 *>(sxw + kBN)[c * 4 + j4];
+                                const int p = (c * 16 + j4 * 4) / 2;
+                                accu2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]),
+                                                pack2(f.x, f.y), accu2[p]);
+                                accu2[p + 1] = fma2(pack2(v[c][j4 * 4 + 2], v[c][j4 * 4 + 3]),
+                                                    pack2(f.z, f.w), accu2[p + 1]);
                             }
                         }
                 }
@@ -540,6 +553,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
             }
             if (!ok) break;
+            float acc[kBN], accu[kBN];
+#pragma unroll
+            for (int p = 0; p < kBN / 2; ++p) {
+                acc[2 * p] = __uint_as_float((uint32_t)acc2[p]);
+                acc[2 * p + 1] = __uint_as_float((uint32_t)(acc2[p] >> 32));
+                accu[2 * p] = __uint_as_float((uint32_t)accu2[p]);
+                accu[2 * p + 1] = __uint_as_float((uint32_t)(accu2[p] >> 32));
+            }
 
             if (!u.down) {
                 // h = silu(gate) * up; row n is quantised over the tile's 128
