@@ -302,7 +302,7 @@ int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
     // gate/up GEMM with SwiGLU + down GEMM; or, for wide batches, GEMM +
     // SiLU-mul + down GEMM), combine
     const int ffn = fused_ffn(cfg, T) ? 1 : (wide_rows(cfg, T) ? 3 : 2);
-    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count() + ffn + 1;
+    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count(cfg, T) + ffn + 1;
 }
 
 int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, const void *x,

@@ -92,7 +92,7 @@ int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 
 // Kernel launches per call, for the layer's launch count.
 int route_kernel_count();
-int permute_kernel_count();
+int permute_kernel_count(const moe_config *cfg, int T);
 
 }  // namespace moe
 

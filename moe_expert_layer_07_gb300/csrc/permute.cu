@@ -7,7 +7,8 @@
 // Row of routed slot i with expert e:
 //   expert_offsets[e] + #{ i' < i : e_i' = e }
 // so rows within an expert are in slot order and the result does not depend
-// on the order threads run in.  Three kernels:
+// on the order threads run in.  Three kernels (the first two as one for
+// batches of at most 1024 routed slots):
 //   permute_count    1024 slots per CTA: warp-level __match_any_sync gives
 //                    each slot its rank among equal ids of its warp, a
 //                    shared-memory table of per-warp counts gives the rank
@@ -39,13 +40,11 @@ struct PermArgs {
     int32_t *status;
 };
 
-__global__ void __launch_bounds__(kChunk) permute_count_kernel(const PermArgs a) {
-    extern __shared__ int32_t wc[];   // [32 warps][E]
-    ptx::pdl_launch_dependents();
-    ptx::pdl_wait();   // routing ids
+// Counts of chunk `chunk` (1024 slots): ranks among equal ids, histogram.
+__device__ __forceinline__ void count_chunk(const PermArgs &a, int chunk, int32_t *wc) {
     const int R = a.T * a.k;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int i = blockIdx.x * kChunk + tid;
+    const int i = chunk * kChunk + tid;
     for (int j = tid; j < 32 * a.E; j += kChunk) wc[j] = 0;
     int e = -1;
     if (i < R) {
@@ -68,8 +67,15 @@ __global__ void __launch_bounds__(kChunk) permute_count_kernel(const PermArgs a)
     for (int ee = tid; ee < a.E; ee += kChunk) {
         int c = 0;
         for (int w = 0; w < 32; ++w) c += wc[w * a.E + ee];
-        a.chunk_counts[(size_t)blockIdx.x * a.E + ee] = c;
+        a.chunk_counts[(size_t)chunk * a.E + ee] = c;
     }
+}
+
+__global__ void __launch_bounds__(kChunk) permute_count_kernel(const PermArgs a) {
+    extern __shared__ int32_t wc[];   // [32 warps][E]
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // routing ids
+    count_chunk(a, blockIdx.x, wc);
 }
 
 // Exclusive scan of `v` over the CTA (1024 threads); returns the total too.
@@ -101,10 +107,8 @@ __device__ int block_exclusive_scan(int v, int *total, int *sh) {
     return res;
 }
 
-__global__ void __launch_bounds__(1024) permute_scan_kernel(const PermArgs a, int chunks) {
-    __shared__ int sh[33];
-    ptx::pdl_launch_dependents();
-    ptx::pdl_wait();   // per-chunk counts
+// Offsets of all groups and the first row of every (chunk, expert).
+__device__ __forceinline__ void scan_chunks(const PermArgs &a, int chunks, int *sh) {
     const int G = a.E + a.S;
     const int per = (G + 1023) / 1024;   // consecutive groups per thread
     const int g0 = threadIdx.x * per;
@@ -136,6 +140,26 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(const PermArgs a, in
         }
     }
     if (threadIdx.x == 0) a.offsets[G] = total;
+}
+
+__global__ void __launch_bounds__(1024) permute_scan_kernel(const PermArgs a, int chunks) {
+    __shared__ int sh[33];
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // per-chunk counts
+    scan_chunks(a, chunks, sh);
+}
+
+// Decode batches (at most 1024 routed slots, one chunk): count and scan in
+// one CTA, one launch fewer.  The CTA barrier orders the counts written to
+// global memory before the scan reads them.
+__global__ void __launch_bounds__(kChunk) permute_count_scan_kernel(const PermArgs a) {
+    extern __shared__ int32_t wc[];   // [32 warps][E]
+    __shared__ int sh[33];
+    ptx::pdl_launch_dependents();
+    ptx::pdl_wait();   // routing ids
+    count_chunk(a, 0, wc);
+    __syncthreads();
+    scan_chunks(a, 1, sh);
 }
 
 __global__ void __launch_bounds__(256) permute_scatter_kernel(const PermArgs a) {
@@ -179,7 +203,9 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const PermArgs a) 
 
 }  // namespace
 
-int permute_kernel_count() { return 3; }
+int permute_kernel_count(const moe_config *cfg, int T) {
+    return (int64_t)T * cfg->top_k <= kChunk ? 2 : 3;
+}
 
 size_t permute_scratch_bytes(const moe_config *cfg, int T) {
     const int64_t R = (int64_t)T * cfg->top_k;
@@ -216,7 +242,15 @@ int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const 
     a.status = status;
 
     const size_t smem = 32 * sizeof(int32_t) * (size_t)a.E;
-    if (chunks > 0) {
+    if (chunks <= 1) {   // count (if any slot) and scan in one CTA
+        if (smem > 48 * 1024)
+            MOE_CUDA_TRY(cudaFuncSetAttribute(permute_count_scan_kernel,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)smem));
+        if (launch_dependent(permute_count_scan_kernel, dim3(1), dim3(kChunk), smem, s, a))
+            return MOE_ERR_CUDA;
+        MOE_LAUNCH_CHECK();
+    } else {
         if (smem > 48 * 1024)
             MOE_CUDA_TRY(cudaFuncSetAttribute(permute_count_kernel,
                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -224,10 +258,10 @@ int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const 
         if (launch_dependent(permute_count_kernel, dim3(chunks), dim3(kChunk), smem, s, a))
             return MOE_ERR_CUDA;
         MOE_LAUNCH_CHECK();
+        if (launch_dependent(permute_scan_kernel, dim3(1), dim3(1024), 0, s, a, chunks))
+            return MOE_ERR_CUDA;
+        MOE_LAUNCH_CHECK();
     }
-    if (launch_dependent(permute_scan_kernel, dim3(1), dim3(1024), 0, s, a, chunks))
-        return MOE_ERR_CUDA;
-    MOE_LAUNCH_CHECK();
     const int64_t rows = total_rows(cfg, T);
     if (rows > 0) {
         if (launch_dependent(permute_scatter_kernel, dim3((unsigned)ceil_div(rows, 8)), dim3(256),

@@ -66,14 +66,16 @@ def test_workspace_size_r1_decode(L):
 
 
 def test_layer_kernel_counts(L):
-    # route (2) + quantise x + permute (3) + experts' FFN + combine
+    # route (2) + quantise x + permute (2 for at most 1024 routed slots, else 3)
+    # + experts' FFN + combine
     r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
-    assert moe.layer_kernel_count(r1, 128) == 8        # one-kernel FFN
+    assert moe.layer_kernel_count(r1, 128) == 7        # one-kernel FFN, 1024 slots
+    assert moe.layer_kernel_count(r1, 129) == 8        # 1032 slots: count and scan apart
     assert moe.layer_kernel_count(r1, 4096) == 10      # wide: GEMM, SiLU-mul, GEMM
     mini = moe.make_config(synth.CONFIGS["r1_mini"])   # inter 384: two GEMM kernels
-    assert moe.layer_kernel_count(mini, 37) == 9
+    assert moe.layer_kernel_count(mini, 37) == 8
     b16 = moe.make_config(synth.CONFIGS["bf16_mini"])
-    assert moe.layer_kernel_count(b16, 29) == 8
+    assert moe.layer_kernel_count(b16, 29) == 7
     assert moe.layer_kernel_count(r1, 0) == 0
 
 
