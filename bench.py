@@ -162,7 +162,7 @@ class Stepper:
         self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
         rows = s.tokens * (s.top_k + s.num_shared)
         self.wide = self.fp8 and rows >= 16 * s.groups   # as moe_layer_forward decides
-        self.fused = self.fp8 and not self.wide and s.inter % 256 == 0
+        self.fused = (not self.fp8) or (not self.wide and s.inter % 256 == 0)
         self.NAMES = self.NAMES_FUSED if self.fused else self.NAMES_SPLIT
         self.sched_bytes = moe.expert_ffn_sched_bytes(s.groups, rows)
         ws[L.status:L.status + 4].zero_()   # the device status word starts clear
@@ -204,9 +204,11 @@ class Stepper:
                     p["perm_scratch"], self.perm_bytes, p["status"])
         mark()
         if self.fused:   # decode batches: both expert GEMMs in one persistent kernel
-            moe.expert_ffn(cfg, G, rows, p["xp"], p["xp_scales"], p["expert_offsets"], w["w13"],
-                           w["w13_s"], w["w2"], w["w2_s"], p["h"], p["h_scales"], p["y"],
-                           p["ffn_sched"], self.sched_bytes, p["status"], w_layout=wl)
+            q = self.fp8
+            moe.expert_ffn(cfg, G, rows, p["xp"], p["xp_scales"] if q else None,
+                           p["expert_offsets"], w["w13"], w.get("w13_s"), w["w2"], w.get("w2_s"),
+                           p["h"], p["h_scales"] if q else None, p["y"], p["ffn_sched"],
+                           self.sched_bytes, p["status"], w_layout=wl)
             mark()
             moe.combine(cfg, T, p["y"], p["row_of_slot"], p["topk_w"], p["expert_offsets"],
                         self.out, moe.OUT_F32)
@@ -277,7 +279,7 @@ def algorithmic_bytes(shape, offsets):
     b["gemm_gate_up_swiglu"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i) + \
         (2 * rows * 2 * I * 4 if wide else 0)
     b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4
-    if fp8 and not wide and I % 256 == 0:   # one kernel holds both GEMMs
+    if (not fp8) or (not wide and I % 256 == 0):   # one kernel holds both GEMMs
         b["expert_ffn"] = b.pop("gemm_gate_up_swiglu") + b.pop("gemm_down")
     b["combine"] = T * (k + S) * H * 4 + 8 * T * k + T * H * 4
     flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)

@@ -242,14 +242,16 @@ MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32
                                     void *h, float *h_scales, int32_t *dev_status,
                                     void *stream);
 
-/* ---- the experts' FFN in one kernel (FP8 layers) ------------------------------
+/* ---- the experts' FFN in one kernel ------------------------------------------
  * For the rows r of every group g (offsets as in moe_grouped_gemm):
- *   g, u = A[r] W13[g]^T     (W13 e4m3 [groups, 2*inter, hidden], block scales
- *                             w13_scales fp32 [groups, 2*inter/128, hidden/128],
- *                             A e4m3 [rows, hidden], a_scales fp32 [rows, hidden/128]),
- *   h    = silu(g) * u, quantised per row and 128-feature group
- *          -> h e4m3 [rows, inter], h_scales fp32 [rows, inter/128],
- *   y[r] = h[r] W2[g]^T      (W2 e4m3 [groups, hidden, inter], w2_scales fp32
+ *   g, u = A[r] W13[g]^T     (W13 [groups, 2*inter, hidden], A [rows, hidden];
+ *                             FP8: e4m3 with block scales w13_scales fp32
+ *                             [groups, 2*inter/128, hidden/128] and a_scales fp32
+ *                             [rows, hidden/128]; BF16: bf16, scales unused),
+ *   h    = silu(g) * u: FP8 quantised per row and 128-feature group
+ *          -> h e4m3 [rows, inter], h_scales fp32 [rows, inter/128];
+ *          BF16 rounded -> h bf16 [rows, inter] (h_scales unused),
+ *   y[r] = h[r] W2[g]^T      (W2 [groups, hidden, inter], FP8 w2_scales fp32
  *                             [groups, hidden/128, inter/128]) -> y fp32 [rows, hidden].
  * The same bits as moe_grouped_gemm_swiglu followed by moe_grouped_gemm
  * (fp32 C), in one persistent launch: the report's fused MoE kernel
@@ -261,9 +263,9 @@ MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32
  *   sched: device scratch of at least moe_expert_ffn_sched_bytes(groups,
  *   rows) bytes, owned by the caller, cleared by the call on `stream`; one
  *   call at a time per buffer (else MOE_ERR_WORKSPACE_TOO_SMALL if short).
- * cfg supplies hidden and inter; cfg->dtype must be FP8_BLOCK128 and inter a
- * multiple of 256 (else MOE_ERR_UNSUPPORTED_SHAPE); groups <= 1024; a, w13,
- * w2, h and y 16-byte aligned; w_layout the MOE_LAYOUT_* of w13 and w2. */
+ * cfg supplies dtype, hidden and inter; FP8 needs inter a multiple of 256
+ * (else MOE_ERR_UNSUPPORTED_SHAPE); groups <= 1024; a, w13, w2, h and y
+ * 16-byte aligned; w_layout the MOE_LAYOUT_* of w13 and w2. */
 MOE_API size_t moe_expert_ffn_sched_bytes(int32_t groups, int32_t rows);
 MOE_API int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const void *a,
                            const float *a_scales, const int32_t *expert_offsets,
@@ -298,12 +300,12 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
 /* ---- the whole layer -------------------------------------------------------------
  * route -> (FP8: quantise x) -> permute -> the experts' FFN -> combine, all
  * on `stream`.  The experts' FFN is
- *   FP8, groups averaging fewer than 16 rows (decode), inter % 256 == 0:
- *     moe_expert_ffn (one persistent kernel);
+ *   BF16, and FP8 with groups averaging fewer than 16 rows (decode) and
+ *     inter % 256 == 0: moe_expert_ffn (one persistent kernel);
  *   FP8, groups averaging 16 rows or more: grouped GEMM gate/up (64-row
  *     tiles, fp32 rows), SiLU-mul + requantisation, grouped GEMM down;
- *   otherwise: grouped GEMM gate/up with the SwiGLU epilogue, grouped GEMM
- *     down;
+ *   other FP8 layers: grouped GEMM gate/up with the SwiGLU epilogue, grouped
+ *     GEMM down;
  * all with the same result bits (fp32 expert outputs), and
  * all intermediates inside `ws` (size from moe_workspace_size for
  * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..

@@ -66,10 +66,12 @@ bool wide_rows(const moe_config *cfg, int64_t T) {
            total_rows(cfg, T) >= 16 * (int64_t)groups_of(cfg);
 }
 
-// FP8 decode batches run both expert GEMMs in one persistent kernel (its
-// down stages hold two 128-wide K blocks, hence inter % 256).
+// Both expert GEMMs run in one persistent kernel for FP8 decode batches and
+// for BF16 layers (its down stages hold two 128-byte K blocks, hence FP8
+// inter % 256; BF16 inter % 128 always holds).
 bool fused_ffn(const moe_config *cfg, int64_t T) {
-    return cfg->dtype == MOE_DTYPE_FP8_BLOCK128 && !wide_rows(cfg, T) && cfg->inter % 256 == 0;
+    if (cfg->dtype != MOE_DTYPE_FP8_BLOCK128) return true;
+    return !wide_rows(cfg, T) && cfg->inter % 256 == 0;
 }
 
 int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
@@ -85,7 +87,7 @@ int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
     L->status = take(4);
     // the fused FFN's unit counter and per-tile h counters; sits right after
     // the status word so that one memset clears both
-    L->ffn_sched = take(fp8 && cfg->inter % 256 == 0
+    L->ffn_sched = take(!fp8 || cfg->inter % 256 == 0
                             ? (int64_t)ffn_sched_bytes((int)G, (int)Rt) : 0);
     L->logits = take(4 * Tm * E);
     L->topk_ids = take(4 * Tm * k);
@@ -250,17 +252,22 @@ int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const vo
     int rc = check_config(cfg);
     if (rc) return rc;
     if (groups <= 0 || rows < 0 || !layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
-    if (cfg->dtype != MOE_DTYPE_FP8_BLOCK128 || cfg->inter % 256 || groups > 1024)
-        return MOE_ERR_UNSUPPORTED_SHAPE;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    if ((fp8 && cfg->inter % 256) || groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)groups * 2 * cfg->inter > INT32_MAX || (int64_t)groups * cfg->hidden > INT32_MAX)
         return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (w_layout == MOE_LAYOUT_TILES &&
+        (!tiled_fits(groups, 2 * (int64_t)cfg->inter, cfg->hidden, fp8) ||
+         !tiled_fits(groups, cfg->hidden, cfg->inter, fp8)))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return MOE_OK;
-    if (!a || !a_scales || !expert_offsets || !w13 || !w13_scales || !w2 || !w2_scales || !h ||
-        !h_scales || !y || !sched)
+    if (!a || !expert_offsets || !w13 || !w2 || !h || !y || !sched ||
+        (fp8 && (!a_scales || !w13_scales || !w2_scales || !h_scales)))
         return MOE_ERR_INVALID_ARG;
     if (!al16(a) || !al16(w13) || !al16(w2) || !al16(h) || !al16(y)) return MOE_ERR_INVALID_ARG;
     if (sched_bytes < ffn_sched_bytes(groups, rows)) return MOE_ERR_WORKSPACE_TOO_SMALL;
-    return launch_expert_ffn(groups, cfg->hidden, cfg->inter, rows, a, a_scales, expert_offsets,
+    return launch_expert_ffn(fp8, groups, cfg->hidden, cfg->inter, rows, a, a_scales,
+                             expert_offsets,
                              w13, w13_scales, w2, w2_scales, w_layout == MOE_LAYOUT_TILES, h,
                              h_scales, y, sched, false, dev_status,
                              static_cast<cudaStream_t>(stream));
@@ -379,7 +386,7 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
                         status, s);
     if (rc) return rc;
     if (fused) {
-        rc = launch_expert_ffn(G, H, I, rows, base + L.xp,
+        rc = launch_expert_ffn(fp8, G, H, I, rows, base + L.xp,
                                reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
                                w->w13_scales, w->w2, w->w2_scales, tiled, base + L.h,
                                reinterpret_cast<float *>(base + L.h_scales),

@@ -139,6 +139,10 @@ __device__ __forceinline__ Unit decode_unit(int t, int n_gu, int MT1, int MT2, i
     return u;
 }
 
+// FP8: e4m3 operands with per-128-K-block promotion of the fp32 partial
+// sums; BF16: bf16 operands, one tensor-memory accumulation over all of K
+// per unit, h rounded to bf16.  K blocks are 128 bytes in both.
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     expert_ffn_kernel(const __grid_constant__ CUtensorMap tmW13,
                       const __grid_constant__ CUtensorMap tmX,
@@ -170,8 +174,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int G = args.groups, H = args.hidden, I = args.inter;
     const int MT1 = I / kBM;    // gate/up tiles per activation tile
     const int MT2 = H / kBM;    // down tiles per activation tile
-    const int KB1 = H / 128;    // K blocks of the gate/up GEMM
-    const int KB2 = I / 128;    // K blocks of the down GEMM (even)
+    constexpr int kKE = FP8 ? 128 : 64;   // elements per 128-byte K block
+    const int KB1 = H / kKE;    // K blocks of the gate/up GEMM
+    const int KB2 = I / kKE;    // K blocks of the down GEMM (even)
     volatile int *abort_flag = &s_abort;
 
     if (threadIdx.x == 0) {
@@ -311,16 +316,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                             tma_load_2d(sa, &tmW13, 0, (tb_gate + ks) * kBM, fb, pol_w);
                             tma_load_2d(sa + kABytes, &tmW13, 0, (tb_up + ks) * kBM, fb, pol_w);
                         } else {
-                            tma_load_2d(sa, &tmW13, ks * 128, wrow, fb, pol_w);            // gate
-                            tma_load_2d(sa + kABytes, &tmW13, ks * 128, wrow + I, fb, pol_w);   // up
+                            tma_load_2d(sa, &tmW13, ks * kKE, wrow, fb, pol_w);            // gate
+                            tma_load_2d(sa + kABytes, &tmW13, ks * kKE, wrow + I, fb, pol_w);   // up
                         }
                         for (int b = 0; b < nbox; ++b)
-                            tma_load_2d(sb + b * kBoxRows * 128, &tmX, ks * 128,
+                            tma_load_2d(sb + b * kBoxRows * 128, &tmX, ks * kKE,
                                         u.row0 + b * kBoxRows, fb, pol_a);
                     } else {
 #pragma unroll
                         for (int hk = 0; hk < 2; ++hk) {
-                            const int k0 = (2 * ks + hk) * 128;
+                            const int k0 = (2 * ks + hk) * kKE;
                             if (tiled)
                                 tma_load_2d(sa + hk * kABytes, &tmW2, 0,
                                             (tb_down + 2 * ks + hk) * kBM, fb, pol_w);
@@ -364,8 +369,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (t >= total) break;
                 const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
                 const int nmma = ((u.nvalid + 15) / 16) * 16;
-                const uint32_t idesc = idesc_e4m3(kBM, nmma);
+                const uint32_t idesc = FP8 ? idesc_e4m3(kBM, nmma) : idesc_bf16(kBM, nmma);
                 const int nsteps = u.down ? KB2 / 2 : KB1;
+                if (!FP8) {   // BF16: one accumulator for the whole unit
+                    if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
                 for (int ks = 0; ks < nsteps && ok; ++ks) {
                     if (!wait_bounded(smem_u32(&full_bar[stage]), phase, abort_flag, args.status,
                                       MOE_DEV_TIMEOUT)) {
@@ -377,33 +390,43 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const uint32_t sb = sa + 2 * kABytes;
                     const int nacc = u.down ? 2 : 1;
                     for (int hk = 0; hk < nacc; ++hk) {
-                        if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
-                                          args.status, MOE_DEV_TIMEOUT)) {
-                            ok = false;
-                            break;
+                        if (FP8) {   // one accumulator per K block
+                            if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
+                                              args.status, MOE_DEV_TIMEOUT)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
                         }
-                        tc_fence_after();
                         const uint32_t d = tmem_base + (uint32_t)(ab * kAccCols);
+                        // FP8 starts every K block afresh; BF16 only the unit's first
+                        const bool fresh = FP8 || (ks == 0 && hk == 0);
+                        auto mma = [&](uint32_t dd, uint64_t a, uint64_t b, bool acc) {
+                            if (FP8) mma_f8f6f4(dd, a, b, idesc, acc);
+                            else mma_f16(dd, a, b, idesc, acc);
+                        };
                         if (!u.down) {
                             const uint64_t dg = sdesc_k_sw128(sa);
                             const uint64_t du = sdesc_k_sw128(sa + kABytes);
                             const uint64_t db = sdesc_k_sw128(sb);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk) {   // 4 x 32 bytes of K
-                                mma_f8f6f4(d, dg + 2 * kk, db + 2 * kk, idesc, kk > 0);
-                                mma_f8f6f4(d + kBN, du + 2 * kk, db + 2 * kk, idesc, kk > 0);
+                                mma(d, dg + 2 * kk, db + 2 * kk, !(fresh && kk == 0));
+                                mma(d + kBN, du + 2 * kk, db + 2 * kk, !(fresh && kk == 0));
                             }
                         } else {
                             const uint64_t da = sdesc_k_sw128(sa + hk * kABytes);
                             const uint64_t db = sdesc_k_sw128(sb + hk * kBBytes);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_f8f6f4(d, da + 2 * kk, db + 2 * kk, idesc, kk > 0);
+                                mma(d, da + 2 * kk, db + 2 * kk, !(fresh && kk == 0));
                         }
-                        mma_commit(smem_u32(&acc_full[ab]));
-                        if (++ab == kAccBufs) {
-                            ab = 0;
-                            aphase ^= 1u;
+                        if (FP8 || (ks == nsteps - 1 && hk == nacc - 1)) {
+                            mma_commit(smem_u32(&acc_full[ab]));
+                            if (++ab == kAccBufs) {
+                                ab = 0;
+                                aphase ^= 1u;
+                            }
                         }
                     }
                     if (!ok) break;
@@ -444,106 +467,152 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
             const int nchunks = (u.nvalid + 15) / 16;
             const bool row_ok = lane < u.nvalid;   // lane n holds activation row n's scale
-            // columns (2p, 2p + 1) side by side for the paired FMA
-            uint64_t acc2[kBN / 2], accu2[kBN / 2];
-#pragma unroll
-            for (int p = 0; p < kBN / 2; ++p) {
-                acc2[p] = 0ull;
-                accu2[p] = 0ull;
-            }
-            const int KB = u.down ? KB2 : KB1;
-            const float *wsp, *wup = nullptr, *xsp;
-            if (!u.down) {
-                wsp = args.w13_scales + ((size_t)u.g * (2 * MT1) + u.mt) * KB1;
-                wup = wsp + (size_t)MT1 * KB1;
-                xsp = args.x_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB1;
+            float acc[kBN], accu[kBN];
+            if constexpr (FP8) {
+                // columns (2p, 2p + 1) side by side for the paired FMA
+                uint64_t acc2[kBN / 2], accu2[kBN / 2];
+    #pragma unroll
+                for (int p = 0; p < kBN / 2; ++p) {
+                    acc2[p] = 0ull;
+                    accu2[p] = 0ull;
+                }
+                const int KB = u.down ? KB2 : KB1;
+                const float *wsp, *wup = nullptr, *xsp;
+                if (!u.down) {
+                    wsp = args.w13_scales + ((size_t)u.g * (2 * MT1) + u.mt) * KB1;
+                    wup = wsp + (size_t)MT1 * KB1;
+                    xsp = args.x_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB1;
+                } else {
+                    // h and its scales are written by gate/up units of this launch:
+                    // the unit id is published before its producer has seen them
+                    // complete, so the epilogue acquires the completion count too
+                    // before it reads a scale (lane 0 polls; after the warp
+                    // barrier every lane's own acquire load reads the final count)
+                    bool dep = true;
+                    if (lane == 0)
+                        dep = wait_flag_geq(args.sched + 1 + u.j, MT1, abort_flag, args.status,
+                                            MOE_DEV_TIMEOUT);
+                    if (!__shfl_sync(0xffffffffu, dep, 0)) {
+                        ok = false;
+                        break;
+                    }
+                    __syncwarp();
+                    (void)ld_acquire_gpu(args.sched + 1 + u.j);
+                    wsp = args.w2_scales + ((size_t)u.g * MT2 + u.mt) * KB2;
+                    xsp = args.h_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB2;
+                }
+                // scales of K block kb + 1 are fetched while block kb is reduced;
+                // h_scales (written during this launch) take coherent loads, the
+                // rest the read-only path
+                auto xs_at = [&](int kb) {
+                    if (!row_ok) return 0.0f;
+                    return u.down ? ld_relaxed_gpu_f32(xsp + kb) : __ldg(xsp + kb);
+                };
+                float xs_n = xs_at(0), sw_n = __ldg(wsp), su_n = u.down ? 0.0f : __ldg(wup);
+                for (int kb = 0; kb < KB; ++kb) {
+                    const float xs = xs_n, sw = sw_n, su = su_n;
+                    if (kb + 1 < KB) {
+                        xs_n = xs_at(kb + 1);
+                        sw_n = __ldg(wsp + kb + 1);
+                        if (!u.down) su_n = __ldg(wup + kb + 1);
+                    }
+                    float *sxw = s_sx[q][kb & 1];
+                    sxw[lane] = __fmul_rn(xs, sw);   // lane n holds row n's activation scale
+                    if (!u.down) sxw[kBN + lane] = __fmul_rn(xs, su);
+                    __syncwarp();
+                    if (!wwait(&acc_full[ab], aphase)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t col = (uint32_t)(ab * kAccCols);
+                    uint32_t v[kBN / 16][16];
+    #pragma unroll
+                    for (int c = 0; c < kBN / 16; ++c)
+                        if (c < nchunks) tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
+    #pragma unroll
+                    for (int c = 0; c < kBN / 16; ++c)
+                        if (c < nchunks) tmem_wait_ld(v[c]);
+    #pragma unroll
+                    for (int c = 0; c < kBN / 16; ++c)
+                        if (c < nchunks) {
+    #pragma unroll
+                            for (int j4 = 0; j4 < 4; ++j4) {
+                                const uint4 f = reinterpret_cast<const uint4 *>(sxw)[c * 4 + j4];
+                                const int p = (c * 16 + j4 * 4) / 2;
+                                acc2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]), pack2(f.x, f.y),
+                                               acc2[p]);
+                                acc2[p + 1] = fma2(pack2(v[c][j4 * 4 + 2], v[c][j4 * 4 + 3]),
+                                                   pack2(f.z, f.w), acc2[p + 1]);
+                            }
+                        }
+                    if (!u.down) {   // up rows: same activation scales, their own block scale
+    #pragma unroll
+                        for (int c = 0; c < kBN / 16; ++c)
+                            if (c < nchunks)
+                                tmem_ld16(lane_base + col + (uint32_t)(kBN + c * 16), v[c]);
+    #pragma unroll
+                        for (int c = 0; c < kBN / 16; ++c)
+                            if (c < nchunks) tmem_wait_ld(v[c]);
+    #pragma unroll
+                        for (int c = 0; c < kBN / 16; ++c)
+                            if (c < nchunks) {
+    #pragma unroll
+                                for (int j4 = 0; j4 < 4; ++j4) {
+                                    const uint4 f =
+                                        reinterpret_cast<const uint4 *>(sxw + kBN)[c * 4 + j4];
+                                    const int p = (c * 16 + j4 * 4) / 2;
+                                    accu2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]),
+                                                    pack2(f.x, f.y), accu2[p]);
+                                    accu2[p + 1] = fma2(pack2(v[c][j4 * 4 + 2], v[c][j4 * 4 + 3]),
+                                                        pack2(f.z, f.w), accu2[p + 1]);
+                                }
+                            }
+                    }
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
+                    if (++ab == kAccBufs) {
+                        ab = 0;
+                        aphase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+    #pragma unroll
+                for (int p = 0; p < kBN / 2; ++p) {
+                    acc[2 * p] = __uint_as_float((uint32_t)acc2[p]);
+                    acc[2 * p + 1] = __uint_as_float((uint32_t)(acc2[p] >> 32));
+                    accu[2 * p] = __uint_as_float((uint32_t)accu2[p]);
+                    accu[2 * p + 1] = __uint_as_float((uint32_t)(accu2[p] >> 32));
+                }
             } else {
-                // h and its scales are written by gate/up units of this launch:
-                // the unit id is published before its producer has seen them
-                // complete, so the epilogue acquires the completion count too
-                // before it reads a scale (lane 0 polls; after the warp
-                // barrier every lane's own acquire load reads the final count)
-                bool dep = true;
-                if (lane == 0)
-                    dep = wait_flag_geq(args.sched + 1 + u.j, MT1, abort_flag, args.status,
-                                        MOE_DEV_TIMEOUT);
-                if (!__shfl_sync(0xffffffffu, dep, 0)) {
-                    ok = false;
-                    break;
-                }
-                __syncwarp();
-                (void)ld_acquire_gpu(args.sched + 1 + u.j);
-                wsp = args.w2_scales + ((size_t)u.g * MT2 + u.mt) * KB2;
-                xsp = args.h_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB2;
-            }
-            // scales of K block kb + 1 are fetched while block kb is reduced;
-            // h_scales (written during this launch) take coherent loads, the
-            // rest the read-only path
-            auto xs_at = [&](int kb) {
-                if (!row_ok) return 0.0f;
-                return u.down ? ld_relaxed_gpu_f32(xsp + kb) : __ldg(xsp + kb);
-            };
-            float xs_n = xs_at(0), sw_n = __ldg(wsp), su_n = u.down ? 0.0f : __ldg(wup);
-            for (int kb = 0; kb < KB; ++kb) {
-                const float xs = xs_n, sw = sw_n, su = su_n;
-                if (kb + 1 < KB) {
-                    xs_n = xs_at(kb + 1);
-                    sw_n = __ldg(wsp + kb + 1);
-                    if (!u.down) su_n = __ldg(wup + kb + 1);
-                }
-                float *sxw = s_sx[q][kb & 1];
-                sxw[lane] = __fmul_rn(xs, sw);   // lane n holds row n's activation scale
-                if (!u.down) sxw[kBN + lane] = __fmul_rn(xs, su);
-                __syncwarp();
-                if (!wwait(&acc_full[ab], aphase)) {
-                    ok = false;
-                    break;
-                }
+                // BF16: the unit's accumulator holds the full sums; the h rows
+                // a down unit reads arrive through TMA only (its producer
+                // waited for them), so the epilogue reads no scales
+                if (!wwait(&acc_full[ab], aphase)) break;
                 tc_fence_after();
                 const uint32_t col = (uint32_t)(ab * kAccCols);
-                uint32_t v[kBN / 16][16];
-#pragma unroll
-                for (int c = 0; c < kBN / 16; ++c)
-                    if (c < nchunks) tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
-#pragma unroll
-                for (int c = 0; c < kBN / 16; ++c)
-                    if (c < nchunks) tmem_wait_ld(v[c]);
+                uint32_t v[kBN / 16][16], vu[kBN / 16][16];
 #pragma unroll
                 for (int c = 0; c < kBN / 16; ++c)
                     if (c < nchunks) {
-#pragma unroll
-                        for (int j4 = 0; j4 < 4; ++j4) {
-                            const uint4 f = reinterpret_cast<const uint4 *>(sxw)[c * 4 + j4];
-                            const int p = (c * 16 + j4 * 4) / 2;
-                            acc2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]), pack2(f.x, f.y),
-                                           acc2[p]);
-                            acc2[p + 1] = fma2(pack2(v[c][j4 * 4 + 2], v[c][j4 * 4 + 3]),
-                                               pack2(f.z, f.w), acc2[p + 1]);
-                        }
+                        tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
+                        if (!u.down) tmem_ld16(lane_base + col + (uint32_t)(kBN + c * 16), vu[c]);
                     }
-                if (!u.down) {   // up rows: same activation scales, their own block scale
 #pragma unroll
-                    for (int c = 0; c < kBN / 16; ++c)
-                        if (c < nchunks)
-                            tmem_ld16(lane_base + col + (uint32_t)(kBN + c * 16), v[c]);
+                for (int c = 0; c < kBN / 16; ++c)
+                    if (c < nchunks) {
+                        tmem_wait_ld(v[c]);
+                        if (!u.down) tmem_wait_ld(vu[c]);
+                    }
 #pragma unroll
-                    for (int c = 0; c < kBN / 16; ++c)
-                        if (c < nchunks) tmem_wait_ld(v[c]);
+                for (int c = 0; c < kBN / 16; ++c)
 #pragma unroll
-                    for (int c = 0; c < kBN / 16; ++c)
-                        if (c < nchunks) {
-#pragma unroll
-                            for (int j4 = 0; j4 < 4; ++j4) {
-                                const uint4 f =
-                                    reinterpret_cast<const uint4 *>(sxw + kBN)[c * 4 + j4];
-                                const int p = (c * 16 + j4 * 4) / 2;
-                                accu2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]),
-                                                pack2(f.x, f.y), accu2[p]);
-                                accu2[p + 1] = fma2(pack2(v[c][j4 * 4 + 2], v[c][j4 * 4 + 3]),
-                                                    pack2(f.z, f.w), accu2[p + 1]);
-                            }
-                        }
-                }
+                    for (int jj = 0; jj < 16; ++jj) {
+                        acc[c * 16 + jj] = c < nchunks ? __uint_as_float(v[c][jj]) : 0.0f;
+                        accu[c * 16 + jj] =
+                            (c < nchunks && !u.down) ? __uint_as_float(vu[c][jj]) : 0.0f;
+                    }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&acc_empty[ab]));
@@ -552,46 +621,46 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     aphase ^= 1u;
                 }
             }
-            if (!ok) break;
-            float acc[kBN], accu[kBN];
-#pragma unroll
-            for (int p = 0; p < kBN / 2; ++p) {
-                acc[2 * p] = __uint_as_float((uint32_t)acc2[p]);
-                acc[2 * p + 1] = __uint_as_float((uint32_t)(acc2[p] >> 32));
-                accu[2 * p] = __uint_as_float((uint32_t)accu2[p]);
-                accu[2 * p + 1] = __uint_as_float((uint32_t)(accu2[p] >> 32));
-            }
 
             if (!u.down) {
-                // h = silu(gate) * up; row n is quantised over the tile's 128
-                // features (one per thread): warp maxima, then the four warps'
-                // maxima through shared memory
+                // h = silu(gate) * up; FP8: row n is quantised over the tile's
+                // 128 features (one per thread): warp maxima, then the four
+                // warps' maxima through shared memory; BF16: rounded to bf16
                 const int b = n_done_gu & 1;
                 const uint32_t par = (uint32_t)(n_done_gu >> 1) & 1u;
 #pragma unroll
                 for (int n = 0; n < kBN; ++n) acc[n] = silu_mul(acc[n], accu[n]);
-                float mine = 0.0f;
+                if constexpr (!FP8) {
+                    __nv_bfloat16 *hb = reinterpret_cast<__nv_bfloat16 *>(args.h);
 #pragma unroll
-                for (int n = 0; n < kBN; ++n) {
-                    float m = fabsf(acc[n]);
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                    if (n == lane) mine = m;
-                }
-                s_amax[b][q * kBN + lane] = mine;
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&amax_bar[b]));
-                if (!wwait(&amax_bar[b], par)) break;
-#pragma unroll
-                for (int n = 0; n < kBN; ++n)
-                    if (n < u.nvalid) {
-                        const float amax = fmaxf(fmaxf(s_amax[b][n], s_amax[b][kBN + n]),
-                                                 fmaxf(s_amax[b][2 * kBN + n], s_amax[b][3 * kBN + n]));
-                        const float sc = fp8_group_scale(amax);
-                        const size_t row = (size_t)(u.row0 + n);
-                        args.h[row * I + u.mt * kBM + m_local] = fp8_code(acc[n], sc);
-                        if (m_local == 0) args.h_scales[row * KB2 + u.mt] = sc;
+                    for (int n = 0; n < kBN; ++n)
+                        if (n < u.nvalid)
+                            hb[(size_t)(u.row0 + n) * I + u.mt * kBM + m_local] =
+                                __float2bfloat16_rn(acc[n]);
+                } else {
+                    float mine = 0.0f;
+    #pragma unroll
+                    for (int n = 0; n < kBN; ++n) {
+                        float m = fabsf(acc[n]);
+    #pragma unroll
+                        for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                        if (n == lane) mine = m;
                     }
+                    s_amax[b][q * kBN + lane] = mine;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&amax_bar[b]));
+                    if (!wwait(&amax_bar[b], par)) break;
+    #pragma unroll
+                    for (int n = 0; n < kBN; ++n)
+                        if (n < u.nvalid) {
+                            const float amax = fmaxf(fmaxf(s_amax[b][n], s_amax[b][kBN + n]),
+                                                     fmaxf(s_amax[b][2 * kBN + n], s_amax[b][3 * kBN + n]));
+                            const float sc = fp8_group_scale(amax);
+                            const size_t row = (size_t)(u.row0 + n);
+                            args.h[row * I + u.mt * kBM + m_local] = fp8_code(acc[n], sc);
+                            if (m_local == 0) args.h_scales[row * KB2 + u.mt] = sc;
+                        }
+                }
                 // publish: every epilogue warp's h stores, then one release
                 fence_proxy_async_global();
                 __syncwarp();
@@ -629,11 +698,14 @@ size_t ffn_sched_bytes(int groups, int rows) {
     return (size_t)4 * (1 + (size_t)groups + (size_t)ceil_div(rows, kBN));
 }
 
-int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *xp,
-                      const float *xp_scales, const int32_t *offsets, const void *w13,
-                      const float *w13_scales, const void *w2, const float *w2_scales,
-                      bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
-                      bool sched_zeroed, int32_t *status, cudaStream_t s) {
+namespace {
+
+template <bool FP8>
+int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
+                    const float *xp_scales, const int32_t *offsets, const void *w13,
+                    const float *w13_scales, const void *w2, const float *w2_scales,
+                    bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
+                    bool sched_zeroed, int32_t *status, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
     static std::once_flag attr_once[64];
     static int attr_rc[64];
@@ -641,21 +713,22 @@ int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *x
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
     std::call_once(attr_once[dev], [&] {
-        attr_rc[dev] = cudaFuncSetAttribute(expert_ffn_kernel,
+        attr_rc[dev] = cudaFuncSetAttribute(expert_ffn_kernel<FP8>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kSmemBytes) == cudaSuccess ? 0 : 1;
     });
     if (attr_rc[dev]) return MOE_ERR_CUDA;
+    constexpr int kKE = FP8 ? 128 : 64;
     CUtensorMap tmW13, tmX, tmW2, tmH;
     const uint64_t w13_rows = (uint64_t)groups * 2 * inter, w2_rows = (uint64_t)groups * hidden;
     const bool w_ok =
-        w_tiled ? encode_2d(&tmW13, w13, true, 128, w13_rows * (hidden / 128), kBM) &&
-                      encode_2d(&tmW2, w2, true, 128, w2_rows * (inter / 128), kBM)
-                : encode_2d(&tmW13, w13, true, (uint64_t)hidden, w13_rows, kBM) &&
-                      encode_2d(&tmW2, w2, true, (uint64_t)inter, w2_rows, kBM);
+        w_tiled ? encode_2d(&tmW13, w13, FP8, kKE, w13_rows * (hidden / kKE), kBM) &&
+                      encode_2d(&tmW2, w2, FP8, kKE, w2_rows * (inter / kKE), kBM)
+                : encode_2d(&tmW13, w13, FP8, (uint64_t)hidden, w13_rows, kBM) &&
+                      encode_2d(&tmW2, w2, FP8, (uint64_t)inter, w2_rows, kBM);
     if (!w_ok ||
-        !encode_2d(&tmX, xp, true, (uint64_t)hidden, (uint64_t)rows, kBoxRows) ||
-        !encode_2d(&tmH, h, true, (uint64_t)inter, (uint64_t)rows, kBoxRows))
+        !encode_2d(&tmX, xp, FP8, (uint64_t)hidden, (uint64_t)rows, kBoxRows) ||
+        !encode_2d(&tmH, h, FP8, (uint64_t)inter, (uint64_t)rows, kBoxRows))
         return MOE_ERR_CUDA;
     if (!sched_zeroed) MOE_CUDA_TRY(cudaMemsetAsync(sched, 0, ffn_sched_bytes(groups, rows), s));
     FfnArgs a;
@@ -667,7 +740,7 @@ int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *x
     a.x_scales = xp_scales;
     a.w13_scales = w13_scales;
     a.w2_scales = w2_scales;
-    a.h = static_cast<uint8_t *>(h);
+    a.h = static_cast<uint8_t *>(h);   // e4m3 or bf16 bytes
     a.h_scales = h_scales;
     a.y = y;
     a.sched = sched;
@@ -676,11 +749,23 @@ int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *x
     const int64_t units_bound =
         (int64_t)(inter / kBM + hidden / kBM) * (groups + ceil_div(rows, kBN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, units_bound);
-    if (launch_dependent(expert_ffn_kernel, dim3(grid), dim3(kThreads), kSmemBytes, s, tmW13, tmX,
-                         tmW2, tmH, a))
+    if (launch_dependent(expert_ffn_kernel<FP8>, dim3(grid), dim3(kThreads), kSmemBytes, s, tmW13,
+                         tmX, tmW2, tmH, a))
         return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
+}
+
+}  // namespace
+
+int launch_expert_ffn(bool fp8, int groups, int hidden, int inter, int rows, const void *xp,
+                      const float *xp_scales, const int32_t *offsets, const void *w13,
+                      const float *w13_scales, const void *w2, const float *w2_scales,
+                      bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
+                      bool sched_zeroed, int32_t *status, cudaStream_t s) {
+    auto f = fp8 ? launch_ffn_impl<true> : launch_ffn_impl<false>;
+    return f(groups, hidden, inter, rows, xp, xp_scales, offsets, w13, w13_scales, w2, w2_scales,
+             w_tiled, h, h_scales, y, sched, sched_zeroed, status, s);
 }
 
 }  // namespace moe
@@ -747,7 +832,7 @@ extern "C" MOE_API int moe_selftest_ffn_flag_timeout(void *scratch, size_t scrat
     const int n_gu = kSelftestI / 128;   // gate/up units of the one 32-row activation tile
     ffn_selftest_init_kernel<<<1, 32, 0, s>>>(off, sched, n_gu);
     MOE_LAUNCH_CHECK();
-    return launch_expert_ffn(1, kSelftestH, kSelftestI, 1, b + L.xp,
+    return launch_expert_ffn(true, 1, kSelftestH, kSelftestI, 1, b + L.xp,
                              reinterpret_cast<const float *>(b + L.xs), off, b + L.w13,
                              reinterpret_cast<const float *>(b + L.w13s), b + L.w2,
                              reinterpret_cast<const float *>(b + L.w2s), false, b + L.h,

@@ -57,11 +57,11 @@ int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int r
                                const void *a, const float *a_scales, const int32_t *offsets,
                                const void *w13, const float *w13_scales, bool w_tiled, void *h,
                                float *h_scales, int32_t *status, cudaStream_t s);
-// The experts' FFN in one persistent kernel (FP8): gate/up + SwiGLU + requant,
-// then down.  `sched` holds ffn_sched_bytes(groups, rows) bytes; it is
+// The experts' FFN in one persistent kernel (FP8 or BF16): gate/up + SwiGLU
+// (+ FP8 requant), then down.  `sched` holds ffn_sched_bytes(groups, rows) bytes; it is
 // cleared on `s` unless the caller has already zeroed it in stream order.
 size_t ffn_sched_bytes(int groups, int rows);
-int launch_expert_ffn(int groups, int hidden, int inter, int rows, const void *xp,
+int launch_expert_ffn(bool fp8, int groups, int hidden, int inter, int rows, const void *xp,
                       const float *xp_scales, const int32_t *offsets, const void *w13,
                       const float *w13_scales, const void *w2, const float *w2_scales,
                       bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,

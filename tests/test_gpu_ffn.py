@@ -159,3 +159,38 @@ def test_flag_wait_gives_up_and_context_survives(lib):
     h_ref, hs_ref, y_ref = _two_kernels(cfg, G, rows, H, I, *p[2:])
     h, hs, y, stv, _ = _fused(cfg, G, rows, H, I, *p[2:])
     assert stv == 0 and torch.equal(y, y_ref) and torch.equal(h, h_ref)
+
+
+def _bf16_problem(H, I, counts, seed):
+    counts = np.asarray(counts)
+    G = len(counts)
+    off = torch.as_tensor(np.concatenate([[0], np.cumsum(counts)]).astype(np.int32), device="cuda")
+    rows = int(counts.sum())
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    a = torch.randn(rows, H, device="cuda", generator=g).to(torch.bfloat16)
+    w13 = (torch.randn(G, 2 * I, H, device="cuda", generator=g) * 0.05).to(torch.bfloat16)
+    w2 = (torch.randn(G, H, I, device="cuda", generator=g) * 0.05).to(torch.bfloat16)
+    return G, rows, a, off, w13, w2
+
+
+@pytest.mark.parametrize("H,I,counts", [(1024, 512, [3, 0, 17, 40, 128, 1]),
+                                        (2048, 1408, [24, 0, 256, 5, 33]),   # V2-Lite sizes
+                                        (512, 384, [7])])
+def test_expert_ffn_bf16_equals_two_kernel_path(lib, H, I, counts):
+    cfg = moe.make_config(synth.MoEShape("ffn16", 1, H, I, 32, 1, 8, scoring="softmax",
+                                         dtype="bf16"))
+    G, rows, a, off, w13, w2 = _bf16_problem(H, I, counts, 12)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    h_ref = torch.empty((rows, I), dtype=torch.bfloat16, device="cuda")
+    y_ref = torch.empty((rows, H), device="cuda")
+    moe.grouped_gemm_swiglu(cfg, G, I, H, rows, a, None, off, w13, None, h_ref, None, st)
+    moe.grouped_gemm(cfg, G, H, I, rows, h_ref, None, off, w2, None, y_ref, moe.OUT_F32, st)
+    h = torch.zeros_like(h_ref)
+    y = torch.full_like(y_ref, float("nan"))
+    nbytes = moe.expert_ffn_sched_bytes(G, rows)
+    sched = torch.full((nbytes // 4,), 77, dtype=torch.int32, device="cuda")
+    moe.expert_ffn(cfg, G, rows, a, None, off, w13, None, w2, None, h, None, y, sched, nbytes, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert torch.equal(h.view(torch.int16), h_ref.view(torch.int16))
+    assert torch.equal(y, y_ref)
