@@ -1,8 +1,9 @@
-// The experts' FFN in one persistent kernel (FP8 layers):
+// The experts' FFN in one persistent kernel (FP8 and BF16 layers):
 //
 //   for every group g and its rows r:
-//     g, u = Xp[r] W13[g]^T            (gate and up, FP8 128x128 block scales)
-//     h    = silu(g) * u  -> e4m3 + one fp32 scale per 128 features
+//     g, u = Xp[r] W13[g]^T            (gate and up; FP8: 128x128 block scales)
+//     h    = silu(g) * u  -> FP8: e4m3 + one fp32 scale per 128 features;
+//                            BF16: rounded to bf16
 //     Y[r] = h W2[g]^T                 (fp32)
 //
 // Moreh report "21K output tokens/s DeepSeek inference on MI300X with Expert
@@ -20,24 +21,27 @@
 // tiles of (g, j) write.  Each finished gate/up tile adds one to a per-j
 // counter (release, after a proxy fence); the producer of a down tile waits
 // (bounded) until the counter reaches the number of gate/up tiles of j,
-// then issues its TMA loads of h, and the epilogue threads acquire the same
-// count before they read h's scales.  Every gate/up unit is claimed before any down
-// unit and a producer issues all loads of a unit before it claims the next,
-// so a unit that is waited on is always in some running CTA's pipeline: no
-// wait can be circular.
+// then issues its TMA loads of h, and (FP8) the epilogue threads acquire the
+// same count before they read h's scales.  Every gate/up unit is claimed
+// before any down unit and a producer issues all loads of a unit before it
+// claims the next, so a unit that is waited on is always in some running
+// CTA's pipeline: no wait can be circular.
 //
 // Per CTA (two per SM), 6 warps:
 //   warp 0     scheduler + TMA producer: a 2-deep ring of 40 KB stages; a
-//              gate/up stage holds one 128-wide K block (gate box, up box,
+//              gate/up stage holds one 128-byte K block (gate box, up box,
 //              activation rows), a down stage two K blocks (two W2 boxes,
-//              two h boxes).
-//   warp 1     MMA issuer: tcgen05.mma kind::f8f6f4, one TMEM accumulator
-//              per K block (four rotate), tcgen05.commit to mbarriers.
-//   warps 2-5  epilogue: per K block the partial product times
+//              two h boxes).  Weights are row-major or 128 x 128-byte tiles.
+//   warp 1     MMA issuer: tcgen05.mma (kind::f8f6f4 or kind::f16),
+//              tcgen05.commit to mbarriers; four TMEM accumulators rotate,
+//              FP8 one per K block, BF16 one per unit.
+//   warps 2-5  epilogue (thread = weight row, 32 activation rows):
+//              FP8: per K block the partial product times
 //              x_scale[r, kb] * w_scale[g, m/128, kb] is added to fp32
-//              registers (thread = weight row, 32 activation rows), then
-//              gate/up: SiLU-mul, row maxima across the four warps, e4m3
-//              codes and scales of h; down: Y rows (fp32).
+//              registers (paired FMAs; the factors reach the warp as
+//              shared-memory broadcasts); BF16: the unit's sums once; then
+//              gate/up: SiLU-mul and h (FP8: row maxima across the four
+//              warps, e4m3 codes and scales); down: Y rows (fp32).
 // The activation scales are read straight from global memory one K block
 // ahead (the tile's 32 rows x K/128 floats stay in L1), which frees the
 // shared memory that a second stage-sized buffer would need.
