@@ -10,9 +10,10 @@
 // the analogue here.
 //
 // Persistent CTAs, two per SM, 6 warps each:
-//   warp 0      TMA producer: per K-block a 128 x 128-byte weight box and
-//               ceil(rows/16) 16 x 128-byte activation boxes, 128-byte
-//               swizzled, into a STAGES-deep shared-memory ring.
+//   warp 0      TMA producer: per K-block a 128 x 128-byte weight box (from
+//               row-major weights, or one contiguous 16 KB tile of packed
+//               weights) and ceil(rows/16) 16 x 128-byte activation boxes,
+//               128-byte swizzled, into a STAGES-deep shared-memory ring.
 //   warp 1      MMA issuer (one thread): tcgen05.mma, K = 32 bytes per
 //               instruction, accumulators in tensor memory, completion
 //               signalled with tcgen05.commit.
@@ -23,7 +24,8 @@
 //                 to fp32 registers; four TMEM buffers rotate so the MMAs
 //                 of the next blocks run meanwhile, and the tile's scales
 //                 are copied to shared memory one tile ahead (cp.async,
-//                 completion on an mbarrier);
+//                 completion on an mbarrier), whence each column's factor
+//                 reaches the warp as a 16-byte broadcast;
 //                 BF16: one accumulation over all of K (the four TMEM
 //                 buffers rotate between tiles);
 //               and stores C (coalesced: a warp writes 32 consecutive n).
