@@ -419,11 +419,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8e4m3" if shape.dtype == "fp8" else "bf16", "data": "synthetic",
-        "config": {"workload": shape.name, "tokens": T, "hidden": H, "inter": shape.inter,
-                   "experts": shape.num_experts, "shared": shape.num_shared,
-                   "top_k": shape.top_k, "parallelism": "replicas" if world > 1 else "single",
-                   "l2": "inputs larger than L2 (expert weights streamed each step), no flush",
-                   **perm_info},
+        "config": {**workload_config(shape, world), **perm_info},
         "hbm_gbs": layer_bytes / (ms_step / 1e3) / 1e9,
         "layer_roofline_frac": (layer_bytes / (hbm_peak * 1e9)) / (ms_step / 1e3),
         "active_experts": active,
@@ -446,6 +442,14 @@ def main():
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def workload_config(shape, world):
+    """The `config` object of both arms' JSON lines."""
+    return {"workload": shape.name, "tokens": shape.tokens, "hidden": shape.hidden,
+            "inter": shape.inter, "experts": shape.num_experts, "shared": shape.num_shared,
+            "top_k": shape.top_k, "parallelism": "replicas" if world > 1 else "single",
+            "l2": "inputs larger than L2 (expert weights streamed each step), no flush"}
 
 
 def replica_seed(seed, rank):
@@ -573,7 +577,7 @@ def reference_arm(args, shape):
             "ms_per_step": 1e3 * t_total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "impl": "reference",
             "dtype": "f64", "data": "synthetic",
-            "config": {"workload": shape.name, "tokens": shape.tokens, "hidden": shape.hidden},
+            "config": workload_config(shape, 1),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{per_step} tokens per step of the same workload"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
