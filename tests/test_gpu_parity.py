@@ -550,3 +550,20 @@ def test_swiglu_epilogue_equals_gemm_then_silu_requant(lib, fp8, inter, K, count
 def dataclasses_replace(shape, **kw):
     import dataclasses
     return dataclasses.replace(shape, **kw)
+
+
+@pytest.mark.parametrize("name", ["r1_mini_i512", "bf16_mini", "r1_mini"])
+def test_bench_steps_equal_the_layer_call(lib, name):
+    """bench.py times the layer as C-ABI steps; they compute the layer call's bits."""
+    import bench
+    wl = workload(name)
+    layer = wl.layer()
+    s = wl.shape
+    ref = torch.full((s.tokens, s.hidden), float("nan"), device="cuda")
+    layer.forward(wl.dev["x"], ref)
+    out = torch.full_like(ref, float("nan"))
+    stepper = bench.Stepper(layer, wl.dev["x"], out)
+    stepper.step()
+    torch.cuda.synchronize()
+    assert layer.status() == 0
+    assert torch.equal(out, ref)
