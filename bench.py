@@ -162,7 +162,7 @@ class Stepper:
         self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
         rows = s.tokens * (s.top_k + s.num_shared)
         self.wide = self.fp8 and rows >= 16 * s.groups   # as moe_layer_forward decides
-        self.fused = (not self.fp8) or (not self.wide and s.inter % 256 == 0)
+        self.fused = not self.wide   # as moe_layer_forward decides
         self.NAMES = self.NAMES_FUSED if self.fused else self.NAMES_SPLIT
         self.sched_bytes = moe.expert_ffn_sched_bytes(s.groups, rows)
         ws[L.status:L.status + 4].zero_()   # the device status word starts clear
@@ -279,7 +279,7 @@ def algorithmic_bytes(shape, offsets):
     b["gemm_gate_up_swiglu"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i) + \
         (2 * rows * 2 * I * 4 if wide else 0)
     b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4
-    if (not fp8) or (not wide and I % 256 == 0):   # one kernel holds both GEMMs
+    if not wide:   # one kernel holds both GEMMs
         b["expert_ffn"] = b.pop("gemm_gate_up_swiglu") + b.pop("gemm_down")
     b["combine"] = T * (k + S) * H * 4 + 8 * T * k + T * H * 4
     flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)

@@ -263,9 +263,9 @@ MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32
  *   sched: device scratch of at least moe_expert_ffn_sched_bytes(groups,
  *   rows) bytes, owned by the caller, cleared by the call on `stream`; one
  *   call at a time per buffer (else MOE_ERR_WORKSPACE_TOO_SMALL if short).
- * cfg supplies dtype, hidden and inter; FP8 needs inter a multiple of 256
- * (else MOE_ERR_UNSUPPORTED_SHAPE); groups <= 1024; a, w13, w2, h and y
- * 16-byte aligned; w_layout the MOE_LAYOUT_* of w13 and w2. */
+ * cfg supplies dtype, hidden and inter; groups <= 1024 (else
+ * MOE_ERR_UNSUPPORTED_SHAPE); a, w13, w2, h and y 16-byte aligned; w_layout
+ * the MOE_LAYOUT_* of w13 and w2. */
 MOE_API size_t moe_expert_ffn_sched_bytes(int32_t groups, int32_t rows);
 MOE_API int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const void *a,
                            const float *a_scales, const int32_t *expert_offsets,
@@ -300,12 +300,10 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
 /* ---- the whole layer -------------------------------------------------------------
  * route -> (FP8: quantise x) -> permute -> the experts' FFN -> combine, all
  * on `stream`.  The experts' FFN is
- *   BF16, and FP8 with groups averaging fewer than 16 rows (decode) and
- *     inter % 256 == 0: moe_expert_ffn (one persistent kernel);
+ *   BF16, and FP8 with groups averaging fewer than 16 rows (decode):
+ *     moe_expert_ffn (one persistent kernel);
  *   FP8, groups averaging 16 rows or more: grouped GEMM gate/up (64-row
  *     tiles, fp32 rows), SiLU-mul + requantisation, grouped GEMM down;
- *   other FP8 layers: grouped GEMM gate/up with the SwiGLU epilogue, grouped
- *     GEMM down;
  * all with the same result bits (fp32 expert outputs), and
  * all intermediates inside `ws` (size from moe_workspace_size for
  * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..

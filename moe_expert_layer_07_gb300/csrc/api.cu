@@ -66,12 +66,10 @@ bool wide_rows(const moe_config *cfg, int64_t T) {
            total_rows(cfg, T) >= 16 * (int64_t)groups_of(cfg);
 }
 
-// Both expert GEMMs run in one persistent kernel for FP8 decode batches and
-// for BF16 layers (its down stages hold two 128-byte K blocks, hence FP8
-// inter % 256; BF16 inter % 128 always holds).
+// Both expert GEMMs run in one persistent kernel for BF16 layers and FP8
+// decode batches.
 bool fused_ffn(const moe_config *cfg, int64_t T) {
-    if (cfg->dtype != MOE_DTYPE_FP8_BLOCK128) return true;
-    return !wide_rows(cfg, T) && cfg->inter % 256 == 0;
+    return cfg->dtype != MOE_DTYPE_FP8_BLOCK128 || !wide_rows(cfg, T);
 }
 
 int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
@@ -87,8 +85,7 @@ int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
     L->status = take(4);
     // the fused FFN's unit counter and per-tile h counters; sits right after
     // the status word so that one memset clears both
-    L->ffn_sched = take(!fp8 || cfg->inter % 256 == 0
-                            ? (int64_t)ffn_sched_bytes((int)G, (int)Rt) : 0);
+    L->ffn_sched = take((int64_t)ffn_sched_bytes((int)G, (int)Rt));
     L->logits = take(4 * Tm * E);
     L->topk_ids = take(4 * Tm * k);
     L->topk_w = take(4 * Tm * k);
@@ -253,7 +250,7 @@ int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const vo
     if (rc) return rc;
     if (groups <= 0 || rows < 0 || !layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
-    if ((fp8 && cfg->inter % 256) || groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)groups * 2 * cfg->inter > INT32_MAX || (int64_t)groups * cfg->hidden > INT32_MAX)
         return MOE_ERR_UNSUPPORTED_SHAPE;
     if (w_layout == MOE_LAYOUT_TILES &&

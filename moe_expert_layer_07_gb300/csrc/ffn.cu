@@ -31,7 +31,8 @@
 //   warp 0     scheduler + TMA producer: a 2-deep ring of 40 KB stages; a
 //              gate/up stage holds one 128-byte K block (gate box, up box,
 //              activation rows), a down stage two K blocks (two W2 boxes,
-//              two h boxes).  Weights are row-major or 128 x 128-byte tiles.
+//              two h boxes; one of each in the last stage when the count
+//              is odd).  Weights are row-major or 128 x 128-byte tiles.
 //   warp 1     MMA issuer: tcgen05.mma (kind::f8f6f4 or kind::f16),
 //              tcgen05.commit to mbarriers; four TMEM accumulators rotate,
 //              FP8 one per K block, BF16 one per unit.
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int MT2 = H / kBM;    // down tiles per activation tile
     constexpr int kKE = FP8 ? 128 : 64;   // elements per 128-byte K block
     const int KB1 = H / kKE;    // K blocks of the gate/up GEMM
-    const int KB2 = I / kKE;    // K blocks of the down GEMM (even)
+    const int KB2 = I / kKE;    // K blocks of the down GEMM (an odd count ends on a 1-block stage)
     volatile int *abort_flag = &s_abort;
 
     if (threadIdx.x == 0) {
@@ -293,9 +294,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     fence_proxy_async_global();
                 }
                 const int nbox = (u.nvalid + kBoxRows - 1) / kBoxRows;
-                const int nsteps = u.down ? KB2 / 2 : KB1;
-                const uint32_t bytes =
-                    2 * kABytes + (u.down ? 2 : 1) * nbox * kBoxRows * 128;
+                const int nsteps = u.down ? (KB2 + 1) / 2 : KB1;
                 const uint64_t pol_w =
                     (s_off[u.g + 1] - s_off[u.g] > kBN) ? pol_w_shared : pol_w_once;
                 const int wrow = u.down ? u.g * H + u.mt * kBM : u.g * 2 * I + u.mt * kBM;
@@ -314,6 +313,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     const uint32_t sa = smem_base + stage * kStageBytes;
                     const uint32_t sb = sa + 2 * kABytes;
                     const uint32_t fb = smem_u32(&full_bar[stage]);
+                    // a down stage holds K blocks 2ks and (if it exists) 2ks + 1
+                    const bool two = 2 * ks + 1 < KB2;
+                    const uint32_t bytes =
+                        u.down ? (two ? 2u : 1u) * (kABytes + nbox * kBoxRows * 128)
+                               : 2 * kABytes + nbox * kBoxRows * 128;
                     mbar_arrive_expect_tx(fb, bytes);
                     if (!u.down) {
                         if (tiled) {
@@ -329,6 +333,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     } else {
 #pragma unroll
                         for (int hk = 0; hk < 2; ++hk) {
+                            if (hk == 1 && !two) break;
                             const int k0 = (2 * ks + hk) * kKE;
                             if (tiled)
                                 tma_load_2d(sa + hk * kABytes, &tmW2, 0,
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
                 const int nmma = ((u.nvalid + 15) / 16) * 16;
                 const uint32_t idesc = FP8 ? idesc_e4m3(kBM, nmma) : idesc_bf16(kBM, nmma);
-                const int nsteps = u.down ? KB2 / 2 : KB1;
+                const int nsteps = u.down ? (KB2 + 1) / 2 : KB1;
                 if (!FP8) {   // BF16: one accumulator for the whole unit
                     if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,
                                       args.status, MOE_DEV_TIMEOUT)) {
@@ -392,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     tc_fence_after();
                     const uint32_t sa = smem_base + stage * kStageBytes;
                     const uint32_t sb = sa + 2 * kABytes;
-                    const int nacc = u.down ? 2 : 1;
+                    const int nacc = (u.down && 2 * ks + 1 < KB2) ? 2 : 1;
                     for (int hk = 0; hk < nacc; ++hk) {
                         if (FP8) {   // one accumulator per K block
                             if (!wait_bounded(smem_u32(&acc_empty[ab]), aphase ^ 1u, abort_flag,

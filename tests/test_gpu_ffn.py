@@ -82,6 +82,7 @@ CASES = [
     (384, 256, [5]),                                   # one group, one down step
     (7168, 2048, [3, 0, 17, 40, 128, 1]),             # R1 sizes
     (2048, 768, [0, 0, 33, 0, 64, 0, 1, 31, 32]),     # exact tile edges
+    (1024, 384, [3, 0, 17, 40, 128, 1]),              # 3 K blocks of W2: a 1-block last stage
 ]
 
 
