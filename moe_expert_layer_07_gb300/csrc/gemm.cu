@@ -51,7 +51,6 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kMaxGroups = 1024;
-constexpr int kThreads = 192;
 // Two CTAs share each SM: each CTA's MMA work does not overlap its own weight
 // stream, and a second CTA fills those gaps (measured on the R1 decode layer:
 // 5.5 -> 6.8 TB/s for the gate/up GEMM).
@@ -62,8 +61,15 @@ constexpr int kMaxKBlocks = 56; // FP8: K <= 7168
 // SW (SwiGLU epilogue): a tile covers 128 gate rows and the matching 128 up
 // rows of W13 (two A tiles per stage sharing one activation tile) and writes
 // h = silu(gate) * up instead of C.
-template <bool FP8, int BN, int STAGES, bool SW>
+// EW: epilogue warpgroups.  Warp 2 + 4h + j (h < EW) reads TMEM lanes
+// [32 (warp & 3), +32) of columns [h BN/EW, (h + 1) BN/EW), so two groups give
+// each SM sub-partition twice the warps to hide the promotion's latencies.
+template <bool FP8, int BN, int STAGES, bool SW, int EW = 1>
 struct GemmShape {
+    static constexpr int kEpiThreads = 128 * EW;
+    static constexpr int kThreads = 64 + kEpiThreads;    // producer, MMA, epilogue warps
+    static constexpr int kCB = BN / EW;                  // columns per epilogue warp
+    static_assert(EW == 1 || (FP8 && !SW && kCB % 16 == 0), "EW");
     static constexpr int kNA = SW ? 2 : 1;               // weight tiles per stage
     static constexpr int kABytes = kBM * 128;            // one weight tile
     static constexpr int kBBytes = BN * 128;
@@ -79,7 +85,7 @@ struct GemmShape {
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 64, "BN");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols * kCtasPerSm <= 512,
                   "TMEM columns");
-    static constexpr int kSxElems = FP8 ? 4 * 2 * kNA * BN : 1;   // per warp, per K-block parity
+    static constexpr int kSxElems = FP8 ? 4 * EW * 2 * kNA * kCB : 1;   // per warp, per K-block parity
     static_assert((kSmemBytes + 8 * kXsElems + 8 * kWsElems + 8 * kAmaxElems + 4 * kSxElems +
                    8 * 1024 + 1024) *
                           kCtasPerSm <=
@@ -123,11 +129,12 @@ __device__ __forceinline__ Tile decode_tile(int t, int G, const int *s_tiles, co
     return tl;
 }
 
-template <bool FP8, int BN, int STAGES, bool SW>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+template <bool FP8, int BN, int STAGES, bool SW, int EW>
+__global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmA, const GemmArgs args) {
-    using S = GemmShape<FP8, BN, STAGES, SW>;
+    using S = GemmShape<FP8, BN, STAGES, SW, EW>;
+    constexpr int CB = S::kCB;
     constexpr int NB = S::kAccBufs;
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -170,11 +177,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         for (int b = 0; b < NB; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
-            mbar_init(smem_u32(&acc_empty[b]), 4);
+            mbar_init(smem_u32(&acc_empty[b]), 4 * EW);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&scale_full[b]), 128);   // every epilogue thread's copies
-            mbar_init(smem_u32(&scale_empty[b]), 4);    // every epilogue warp done reading
+            mbar_init(smem_u32(&scale_full[b]), S::kEpiThreads);   // every epilogue thread's copies
+            mbar_init(smem_u32(&scale_empty[b]), 4 * EW);          // every epilogue warp done reading
             mbar_init(smem_u32(&amax_bar[b]), 4);       // every epilogue warp's row maxima
         }
         mbar_init(smem_u32(&drain_bar), 1);
@@ -191,9 +198,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tma_prefetch_desc(&tmA);
     }
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
-    for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = args.offsets[i];
+    for (int i = threadIdx.x; i <= G; i += S::kThreads) s_off[i] = args.offsets[i];
     __syncthreads();
-    for (int g = threadIdx.x; g < G; g += kThreads) {
+    for (int g = threadIdx.x; g < G; g += S::kThreads) {
         const int a = s_off[g], b = s_off[g + 1];
         if (a < 0 || b < a || b > args.rows) s_bad = 1;
     }
@@ -352,9 +359,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         __syncwarp();
     } else {
-        // ------------------------------ epilogue (warps 2..5)
+        // ------------------------------ epilogue (warps 2 .. 1 + 4 EW)
         const int q = warp & 3;                    // TMEM lanes [32q, 32q + 32)
-        const int etid = threadIdx.x - 64;         // 0..127
+        const int ew = warp - 2;                   // epilogue warp 0 .. 4 EW - 1
+        const int n0 = (ew >> 2) * CB;             // first of this warp's CB columns
+        const int etid = threadIdx.x - 64;         // 0 .. 128 EW - 1
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         const int m_local = q * 32 + lane;
         const int n_h = args.n_out / 2;            // SwiGLU: width of h
@@ -368,13 +377,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
             const float *wsp = args.w_scales + ((size_t)tl.g * MTW + tl.mt) * KB;
             const float *xsp = args.a_scales + (size_t)tl.row0 * KB;
-            for (int i = etid; i < KB; i += 128) cp_async4(smem_u32(&s_ws[b][i]), wsp + i);
+            for (int i = etid; i < KB; i += S::kEpiThreads) cp_async4(smem_u32(&s_ws[b][i]), wsp + i);
             if (SW) {   // up rows' block scales
                 const float *wup = wsp + (size_t)(MTW / 2) * KB;
-                for (int i = etid; i < KB; i += 128) cp_async4(smem_u32(&s_ws[b][KB + i]), wup + i);
+                for (int i = etid; i < KB; i += S::kEpiThreads)
+                    cp_async4(smem_u32(&s_ws[b][KB + i]), wup + i);
             }
             const int n_el = tl.nvalid * KB;
-            for (int i = etid; i < n_el; i += 128) {
+            for (int i = etid; i < n_el; i += S::kEpiThreads) {
                 const int n = i / KB, kb = i - n * KB;
                 cp_async4(smem_u32(&s_xs[b][kb * BN + n]), xsp + i);
             }
@@ -407,22 +417,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     ok = false;
                     break;
                 }
-                float acc[BN];
+                float acc[CB];   // columns n0 .. n0 + CB - 1
                 float accu[SW ? BN : 1];
 #pragma unroll
-                for (int n = 0; n < BN; ++n) acc[n] = 0.0f;
+                for (int n = 0; n < CB; ++n) acc[n] = 0.0f;
 #pragma unroll
                 for (int n = 0; n < (SW ? BN : 1); ++n) accu[n] = 0.0f;
                 for (int kb = 0; kb < KB; ++kb) {
                     const float sw = s_ws[b][kb];
                     const float swu = SW ? s_ws[b][KB + kb] : 0.0f;
-                    float *sxw = s_sx + (q * 2 + (kb & 1)) * (S::kNA * BN);
+                    // factors of this warp's columns n0 + j, at sxw[j] (gate) and sxw[CB + j] (up)
+                    float *sxw = s_sx + (ew * 2 + (kb & 1)) * (S::kNA * CB);
 #pragma unroll
-                    for (int h = 0; h < BN / 32; ++h) {
-                        const int n = h * 32 + lane;
-                        const float xv = n < tl.nvalid ? s_xs[b][kb * BN + n] : 0.0f;
-                        sxw[n] = __fmul_rn(xv, sw);
-                        if (SW) sxw[BN + n] = __fmul_rn(xv, swu);
+                    for (int h = 0; h < (CB + 31) / 32; ++h) {
+                        const int j = h * 32 + lane, n = n0 + j;
+                        if (j < CB) {
+                            const float xv = n < tl.nvalid ? s_xs[b][kb * BN + n] : 0.0f;
+                            sxw[j] = __fmul_rn(xv, sw);
+                            if (SW) sxw[CB + j] = __fmul_rn(xv, swu);
+                        }
                     }
                     __syncwarp();
                     if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
@@ -432,16 +445,17 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                     tc_fence_after();
                     const uint32_t col = (uint32_t)(ab * S::kAccCols);
-                    uint32_t v[BN / 16][16];
+                    const int nch = nchunks - n0 / 16;   // this warp's valid 16-column chunks
+                    uint32_t v[CB / 16][16];
 #pragma unroll
-                    for (int c = 0; c < BN / 16; ++c)
-                        if (c < nchunks) tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
+                    for (int c = 0; c < CB / 16; ++c)
+                        if (c < nch) tmem_ld16(lane_base + col + (uint32_t)(n0 + c * 16), v[c]);
 #pragma unroll
-                    for (int c = 0; c < BN / 16; ++c)
-                        if (c < nchunks) tmem_wait_ld(v[c]);
+                    for (int c = 0; c < CB / 16; ++c)
+                        if (c < nch) tmem_wait_ld(v[c]);
 #pragma unroll
-                    for (int c = 0; c < BN / 16; ++c)
-                        if (c < nchunks) {
+                    for (int c = 0; c < CB / 16; ++c)
+                        if (c < nch) {
 #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4) {
                                 const float4 f = reinterpret_cast<const float4 *>(sxw)[c * 4 + j4];
@@ -452,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                                 acc[n + 3] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, acc[n + 3]);
                             }
                         }
-                    if (SW) {   // up rows: same activation scales, their own block scale
+                    if constexpr (SW) {   // up rows: same activation scales, their own block scale
 #pragma unroll
                         for (int c = 0; c < BN / 16; ++c)
                             if (c < nchunks)
@@ -466,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 #pragma unroll
                                 for (int j4 = 0; j4 < 4; ++j4) {
                                     const float4 f =
-                                        reinterpret_cast<const float4 *>(sxw + BN)[c * 4 + j4];
+                                        reinterpret_cast<const float4 *>(sxw + CB)[c * 4 + j4];
                                     const int n = c * 16 + j4 * 4;
                                     float *au = accu + (SW ? n : 0);
                                     au[0] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, au[0]);
@@ -487,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (!ok) break;
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&scale_empty[b]));
-                if (SW) {
+                if constexpr (SW) {
                     // h = silu(gate) * up; each row n is quantised over the
                     // tile's 128 features (one per thread): warp maxima, then
                     // the four warps' maxima through shared memory.
@@ -526,14 +540,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 } else if (args.c_bf16) {
                     __nv_bfloat16 *C = static_cast<__nv_bfloat16 *>(args.c);
 #pragma unroll
-                    for (int n = 0; n < BN; ++n)
-                        if (n < tl.nvalid)
-                            C[(size_t)(tl.row0 + n) * args.n_out + m_glob] = __float2bfloat16_rn(acc[n]);
+                    for (int n = 0; n < CB; ++n)
+                        if (n0 + n < tl.nvalid)
+                            C[(size_t)(tl.row0 + n0 + n) * args.n_out + m_glob] =
+                                __float2bfloat16_rn(acc[n]);
                 } else {
                     float *C = static_cast<float *>(args.c);
 #pragma unroll
-                    for (int n = 0; n < BN; ++n)
-                        if (n < tl.nvalid) C[(size_t)(tl.row0 + n) * args.n_out + m_glob] = acc[n];
+                    for (int n = 0; n < CB; ++n)
+                        if (n0 + n < tl.nvalid)
+                            C[(size_t)(tl.row0 + n0 + n) * args.n_out + m_glob] = acc[n];
                 }
             } else {
                 if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
@@ -629,10 +645,10 @@ bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint6
 
 namespace {
 
-template <bool FP8, int BN, int STAGES, bool SW = false>
+template <bool FP8, int BN, int STAGES, bool SW = false, int EW = 1>
 int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t s) {
-    using Sh = GemmShape<FP8, BN, STAGES, SW>;
-    auto kern = grouped_gemm_kernel<FP8, BN, STAGES, SW>;
+    using Sh = GemmShape<FP8, BN, STAGES, SW, EW>;
+    auto kern = grouped_gemm_kernel<FP8, BN, STAGES, SW, EW>;
     static std::once_flag attr_once[64];
     static int attr_rc[64];
     int dev = 0;
@@ -658,7 +674,7 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
         (int64_t)(args.n_out / kBM / (SW ? 2 : 1)) * (args.groups + ceil_div(args.rows, BN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, tiles_bound);
     if (grid <= 0) return MOE_OK;
-    if (launch_dependent(kern, dim3(grid), dim3(kThreads), Sh::kSmemBytes, s, tmW, tmA, args))
+    if (launch_dependent(kern, dim3(grid), dim3(Sh::kThreads), Sh::kSmemBytes, s, tmW, tmA, args))
         return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
@@ -687,7 +703,7 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     // Decode-sized groups (a few rows each) stream best with 32-row tiles;
     // larger groups re-read each weight tile fewer times with 64-row tiles.
     const bool wide = (int64_t)rows >= 16 * (int64_t)groups;
-    if (fp8) return wide ? launch_impl<true, 64, 3>(args, a, w, s)
+    if (fp8) return wide ? launch_impl<true, 64, 3, false, 2>(args, a, w, s)
                          : launch_impl<true, 32, 4>(args, a, w, s);
     return launch_impl<false, 32, 4>(args, a, w, s);
 }
