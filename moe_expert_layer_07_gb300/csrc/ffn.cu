@@ -67,7 +67,6 @@ namespace {
 constexpr int kBM = 128;                // weight rows per tile (MMA M)
 constexpr int kBN = 32;                 // activation rows per tile (MMA N)
 constexpr int kBoxRows = 16;            // activation rows per TMA box
-constexpr int kThreads = 192;
 constexpr int kCtasPerSm = 2;
 constexpr int kStages = 2;
 constexpr int kABytes = kBM * 128;                         // 16 KB weight box
@@ -147,8 +146,11 @@ __device__ __forceinline__ Unit decode_unit(int t, int n_gu, int MT1, int MT2, i
 // FP8: e4m3 operands with per-128-K-block promotion of the fp32 partial
 // sums; BF16: bf16 operands, one tensor-memory accumulation over all of K
 // per unit, h rounded to bf16.  K blocks are 128 bytes in both.
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+//
+// EW epilogue warpgroups: warp 2 + 4h + j (h < EW) reads TMEM lane quarter
+// warp & 3 of the CB = 32/EW activation columns [h CB, (h + 1) CB).
+template <bool FP8, int EW>
+__global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
     expert_ffn_kernel(const __grid_constant__ CUtensorMap tmW13,
                       const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmW2,
@@ -171,7 +173,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     __shared__ float s_amax[2][4 * kBN];   // per gate/up tile: each epilogue warp's row maxima
     // per epilogue warp and K-block parity: every column's promotion factor
     // x_scale[n, kb] * w_scale[kb] (gate, then up), read as 16-byte broadcasts
-    __shared__ __align__(16) float s_sx[4][2][2 * kBN];
+    constexpr int CB = kBN / EW;   // activation columns per epilogue warp
+    static_assert(CB % 16 == 0, "whole 16-column TMEM loads");
+    __shared__ __align__(16) float s_sx[4 * EW][2][2 * CB];
 
     using namespace ptx;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -191,15 +195,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         for (int b = 0; b < kAccBufs; ++b) {
             mbar_init(smem_u32(&acc_full[b]), 1);
-            mbar_init(smem_u32(&acc_empty[b]), 4);
+            mbar_init(smem_u32(&acc_empty[b]), 4 * EW);
         }
         for (int r = 0; r < kRing; ++r) {
             mbar_init(smem_u32(&unit_full[r]), 1);
-            mbar_init(smem_u32(&unit_empty[r]), 5);   // the MMA thread + four epilogue warps
+            mbar_init(smem_u32(&unit_empty[r]), 1 + 4 * EW);   // the MMA thread + every epilogue warp
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_u32(&amax_bar[b]), 4);
-            mbar_init(smem_u32(&hdone_bar[b]), 4);
+            mbar_init(smem_u32(&amax_bar[b]), 4 * EW);
+            mbar_init(smem_u32(&hdone_bar[b]), 4 * EW);
         }
         mbar_init(smem_u32(&drain_bar), 1);
         s_abort = 0;
@@ -217,9 +221,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         tma_prefetch_desc(&tmH);
     }
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
-    for (int i = threadIdx.x; i <= G; i += kThreads) s_off[i] = args.offsets[i];
+    for (int i = threadIdx.x; i <= G; i += (int)blockDim.x) s_off[i] = args.offsets[i];
     __syncthreads();
-    for (int g = threadIdx.x; g < G; g += kThreads) {
+    for (int g = threadIdx.x; g < G; g += (int)blockDim.x) {
         const int a = s_off[g], b = s_off[g + 1];
         if (a < 0 || b < a || b > args.rows) s_bad = 1;
     }
@@ -452,8 +456,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
         __syncwarp();
     } else {
-        // ------------------------------ epilogue (warps 2..5)
+        // ------------------------------ epilogue (warps 2 .. 1 + 4 EW)
         const int q = warp & 3;                    // TMEM lanes [32q, 32q + 32)
+        const int ew = warp - 2;                   // epilogue warp 0 .. 4 EW - 1
+        const int n0 = (ew >> 2) * CB;             // first of this warp's CB columns
         const uint32_t lane_base = tmem_base + ((uint32_t)(q * 32) << 16);
         const int m_local = q * 32 + lane;
         // a wait's outcome is made warp-uniform: the tcgen05.ld that follow
@@ -474,14 +480,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (lane == 0) mbar_arrive(smem_u32(&unit_empty[slot]));
             if (t >= total) break;
             const Unit u = decode_unit(t, n_gu, MT1, MT2, G, s_nt, s_off);
-            const int nchunks = (u.nvalid + 15) / 16;
-            const bool row_ok = lane < u.nvalid;   // lane n holds activation row n's scale
-            float acc[kBN], accu[kBN];
+            const int nch = (u.nvalid + 15) / 16 - n0 / 16;   // this warp's valid 16-column chunks
+            // lane j < CB holds the scale of activation row n0 + j
+            const bool row_ok = lane < CB && n0 + lane < u.nvalid;
+            float acc[CB], accu[CB];   // columns n0 .. n0 + CB - 1
             if constexpr (FP8) {
                 // columns (2p, 2p + 1) side by side for the paired FMA
-                uint64_t acc2[kBN / 2], accu2[kBN / 2];
+                uint64_t acc2[CB / 2], accu2[CB / 2];
     #pragma unroll
-                for (int p = 0; p < kBN / 2; ++p) {
+                for (int p = 0; p < CB / 2; ++p) {
                     acc2[p] = 0ull;
                     accu2[p] = 0ull;
                 }
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (!u.down) {
                     wsp = args.w13_scales + ((size_t)u.g * (2 * MT1) + u.mt) * KB1;
                     wup = wsp + (size_t)MT1 * KB1;
-                    xsp = args.x_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB1;
+                    xsp = args.x_scales + (size_t)(u.row0 + (row_ok ? n0 + lane : 0)) * KB1;
                 } else {
                     // h and its scales are written by gate/up units of this launch:
                     // the unit id is published before its producer has seen them
@@ -508,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     __syncwarp();
                     (void)ld_acquire_gpu(args.sched + 1 + u.j);
                     wsp = args.w2_scales + ((size_t)u.g * MT2 + u.mt) * KB2;
-                    xsp = args.h_scales + (size_t)(u.row0 + (row_ok ? lane : 0)) * KB2;
+                    xsp = args.h_scales + (size_t)(u.row0 + (row_ok ? n0 + lane : 0)) * KB2;
                 }
                 // scales of K block kb + 1 are fetched while block kb is reduced;
                 // h_scales (written during this launch) take coherent loads, the
@@ -525,9 +532,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         sw_n = __ldg(wsp + kb + 1);
                         if (!u.down) su_n = __ldg(wup + kb + 1);
                     }
-                    float *sxw = s_sx[q][kb & 1];
-                    sxw[lane] = __fmul_rn(xs, sw);   // lane n holds row n's activation scale
-                    if (!u.down) sxw[kBN + lane] = __fmul_rn(xs, su);
+                    float *sxw = s_sx[ew][kb & 1];
+                    if (lane < CB) {   // factors of columns n0 + lane: gate at [lane], up at [CB + lane]
+                        sxw[lane] = __fmul_rn(xs, sw);
+                        if (!u.down) sxw[CB + lane] = __fmul_rn(xs, su);
+                    }
                     __syncwarp();
                     if (!wwait(&acc_full[ab], aphase)) {
                         ok = false;
@@ -535,16 +544,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     }
                     tc_fence_after();
                     const uint32_t col = (uint32_t)(ab * kAccCols);
-                    uint32_t v[kBN / 16][16];
+                    uint32_t v[CB / 16][16];
     #pragma unroll
-                    for (int c = 0; c < kBN / 16; ++c)
-                        if (c < nchunks) tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
+                    for (int c = 0; c < CB / 16; ++c)
+                        if (c < nch) tmem_ld16(lane_base + col + (uint32_t)(n0 + c * 16), v[c]);
     #pragma unroll
-                    for (int c = 0; c < kBN / 16; ++c)
-                        if (c < nchunks) tmem_wait_ld(v[c]);
+                    for (int c = 0; c < CB / 16; ++c)
+                        if (c < nch) tmem_wait_ld(v[c]);
     #pragma unroll
-                    for (int c = 0; c < kBN / 16; ++c)
-                        if (c < nchunks) {
+                    for (int c = 0; c < CB / 16; ++c)
+                        if (c < nch) {
     #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4) {
                                 const uint4 f = reinterpret_cast<const uint4 *>(sxw)[c * 4 + j4];
@@ -557,19 +566,19 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                         }
                     if (!u.down) {   // up rows: same activation scales, their own block scale
     #pragma unroll
-                        for (int c = 0; c < kBN / 16; ++c)
-                            if (c < nchunks)
-                                tmem_ld16(lane_base + col + (uint32_t)(kBN + c * 16), v[c]);
+                        for (int c = 0; c < CB / 16; ++c)
+                            if (c < nch)
+                                tmem_ld16(lane_base + col + (uint32_t)(kBN + n0 + c * 16), v[c]);
     #pragma unroll
-                        for (int c = 0; c < kBN / 16; ++c)
-                            if (c < nchunks) tmem_wait_ld(v[c]);
+                        for (int c = 0; c < CB / 16; ++c)
+                            if (c < nch) tmem_wait_ld(v[c]);
     #pragma unroll
-                        for (int c = 0; c < kBN / 16; ++c)
-                            if (c < nchunks) {
+                        for (int c = 0; c < CB / 16; ++c)
+                            if (c < nch) {
     #pragma unroll
                                 for (int j4 = 0; j4 < 4; ++j4) {
                                     const uint4 f =
-                                        reinterpret_cast<const uint4 *>(sxw + kBN)[c * 4 + j4];
+                                        reinterpret_cast<const uint4 *>(sxw + CB)[c * 4 + j4];
                                     const int p = (c * 16 + j4 * 4) / 2;
                                     accu2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]),
                                                     pack2(f.x, f.y), accu2[p]);
@@ -588,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 }
                 if (!ok) break;
     #pragma unroll
-                for (int p = 0; p < kBN / 2; ++p) {
+                for (int p = 0; p < CB / 2; ++p) {
                     acc[2 * p] = __uint_as_float((uint32_t)acc2[p]);
                     acc[2 * p + 1] = __uint_as_float((uint32_t)(acc2[p] >> 32));
                     accu[2 * p] = __uint_as_float((uint32_t)accu2[p]);
@@ -601,26 +610,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (!wwait(&acc_full[ab], aphase)) break;
                 tc_fence_after();
                 const uint32_t col = (uint32_t)(ab * kAccCols);
-                uint32_t v[kBN / 16][16], vu[kBN / 16][16];
+                uint32_t v[CB / 16][16], vu[CB / 16][16];
 #pragma unroll
-                for (int c = 0; c < kBN / 16; ++c)
-                    if (c < nchunks) {
-                        tmem_ld16(lane_base + col + (uint32_t)(c * 16), v[c]);
-                        if (!u.down) tmem_ld16(lane_base + col + (uint32_t)(kBN + c * 16), vu[c]);
+                for (int c = 0; c < CB / 16; ++c)
+                    if (c < nch) {
+                        tmem_ld16(lane_base + col + (uint32_t)(n0 + c * 16), v[c]);
+                        if (!u.down)
+                            tmem_ld16(lane_base + col + (uint32_t)(kBN + n0 + c * 16), vu[c]);
                     }
 #pragma unroll
-                for (int c = 0; c < kBN / 16; ++c)
-                    if (c < nchunks) {
+                for (int c = 0; c < CB / 16; ++c)
+                    if (c < nch) {
                         tmem_wait_ld(v[c]);
                         if (!u.down) tmem_wait_ld(vu[c]);
                     }
 #pragma unroll
-                for (int c = 0; c < kBN / 16; ++c)
+                for (int c = 0; c < CB / 16; ++c)
 #pragma unroll
                     for (int jj = 0; jj < 16; ++jj) {
-                        acc[c * 16 + jj] = c < nchunks ? __uint_as_float(v[c][jj]) : 0.0f;
-                        accu[c * 16 + jj] =
-                            (c < nchunks && !u.down) ? __uint_as_float(vu[c][jj]) : 0.0f;
+                        acc[c * 16 + jj] = c < nch ? __uint_as_float(v[c][jj]) : 0.0f;
+                        accu[c * 16 + jj] = (c < nch && !u.down) ? __uint_as_float(vu[c][jj]) : 0.0f;
                     }
                 tc_fence_before();
                 __syncwarp();
@@ -638,35 +647,37 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 const int b = n_done_gu & 1;
                 const uint32_t par = (uint32_t)(n_done_gu >> 1) & 1u;
 #pragma unroll
-                for (int n = 0; n < kBN; ++n) acc[n] = silu_mul(acc[n], accu[n]);
+                for (int n = 0; n < CB; ++n) acc[n] = silu_mul(acc[n], accu[n]);
                 if constexpr (!FP8) {
                     __nv_bfloat16 *hb = reinterpret_cast<__nv_bfloat16 *>(args.h);
 #pragma unroll
-                    for (int n = 0; n < kBN; ++n)
-                        if (n < u.nvalid)
-                            hb[(size_t)(u.row0 + n) * I + u.mt * kBM + m_local] =
+                    for (int n = 0; n < CB; ++n)
+                        if (n0 + n < u.nvalid)
+                            hb[(size_t)(u.row0 + n0 + n) * I + u.mt * kBM + m_local] =
                                 __float2bfloat16_rn(acc[n]);
                 } else {
+                    // s_amax[b][q' kBN + n]: lane quarter q's maximum of column n
                     float mine = 0.0f;
     #pragma unroll
-                    for (int n = 0; n < kBN; ++n) {
+                    for (int n = 0; n < CB; ++n) {
                         float m = fabsf(acc[n]);
     #pragma unroll
                         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
                         if (n == lane) mine = m;
                     }
-                    s_amax[b][q * kBN + lane] = mine;
+                    if (lane < CB) s_amax[b][q * kBN + n0 + lane] = mine;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&amax_bar[b]));
                     if (!wwait(&amax_bar[b], par)) break;
     #pragma unroll
-                    for (int n = 0; n < kBN; ++n)
-                        if (n < u.nvalid) {
+                    for (int j = 0; j < CB; ++j)
+                        if (n0 + j < u.nvalid) {
+                            const int n = n0 + j;
                             const float amax = fmaxf(fmaxf(s_amax[b][n], s_amax[b][kBN + n]),
                                                      fmaxf(s_amax[b][2 * kBN + n], s_amax[b][3 * kBN + n]));
                             const float sc = fp8_group_scale(amax);
                             const size_t row = (size_t)(u.row0 + n);
-                            args.h[row * I + u.mt * kBM + m_local] = fp8_code(acc[n], sc);
+                            args.h[row * I + u.mt * kBM + m_local] = fp8_code(acc[j], sc);
                             if (m_local == 0) args.h_scales[row * KB2 + u.mt] = sc;
                         }
                 }
@@ -674,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 fence_proxy_async_global();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&hdone_bar[b]));
-                if (q == 2) {   // warp 2 publishes
+                if (ew == 0) {   // warp 2 publishes
                     if (!wwait(&hdone_bar[b], par)) break;
                     if (lane == 0) {
                         __threadfence();
@@ -686,9 +697,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 ++n_done_gu;
             } else {
 #pragma unroll
-                for (int n = 0; n < kBN; ++n)
-                    if (n < u.nvalid)
-                        args.y[(size_t)(u.row0 + n) * H + u.mt * kBM + m_local] = acc[n];
+                for (int n = 0; n < CB; ++n)
+                    if (n0 + n < u.nvalid)
+                        args.y[(size_t)(u.row0 + n0 + n) * H + u.mt * kBM + m_local] = acc[n];
             }
         }
     }
@@ -716,13 +727,15 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
                     bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
                     bool sched_zeroed, int32_t *status, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
+    // FP8 promotes every K block in the epilogue: two warpgroups share that work
+    constexpr int kEW = FP8 ? 2 : 1;
     static std::once_flag attr_once[64];
     static int attr_rc[64];
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
     std::call_once(attr_once[dev], [&] {
-        attr_rc[dev] = cudaFuncSetAttribute(expert_ffn_kernel<FP8>,
+        attr_rc[dev] = cudaFuncSetAttribute(expert_ffn_kernel<FP8, kEW>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
                                             kSmemBytes) == cudaSuccess ? 0 : 1;
     });
@@ -758,7 +771,7 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
     const int64_t units_bound =
         (int64_t)(inter / kBM + hidden / kBM) * (groups + ceil_div(rows, kBN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, units_bound);
-    if (launch_dependent(expert_ffn_kernel<FP8>, dim3(grid), dim3(kThreads), kSmemBytes, s, tmW13,
+    if (launch_dependent(expert_ffn_kernel<FP8, kEW>, dim3(grid), dim3(64 + 128 * kEW), kSmemBytes, s, tmW13,
                          tmX, tmW2, tmH, a))
         return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
