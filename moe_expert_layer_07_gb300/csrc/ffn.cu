@@ -27,7 +27,7 @@
 // claims the next, so a unit that is waited on is always in some running
 // CTA's pipeline: no wait can be circular.
 //
-// Per CTA (two per SM), 6 warps:
+// Per CTA (two per SM), 10 warps (FP8) or 6 (BF16):
 //   warp 0     scheduler + TMA producer: a 2-deep ring of 40 KB stages; a
 //              gate/up stage holds one 128-byte K block (gate box, up box,
 //              activation rows), a down stage two K blocks (two W2 boxes,
@@ -36,13 +36,15 @@
 //   warp 1     MMA issuer: tcgen05.mma (kind::f8f6f4 or kind::f16),
 //              tcgen05.commit to mbarriers; four TMEM accumulators rotate,
 //              FP8 one per K block, BF16 one per unit.
-//   warps 2-5  epilogue (thread = weight row, 32 activation rows):
+//   warps 2-9  epilogue (FP8: eight warps, each a TMEM lane quarter of 16
+//   (BF16 2-5) of the 32 activation columns; BF16: four warps, all 32;
+//              thread = weight row):
 //              FP8: per K block the partial product times
 //              x_scale[r, kb] * w_scale[g, m/128, kb] is added to fp32
 //              registers (paired FMAs; the factors reach the warp as
 //              shared-memory broadcasts); BF16: the unit's sums once; then
 //              gate/up: SiLU-mul and h (FP8: row maxima across the four
-//              warps, e4m3 codes and scales); down: Y rows (fp32).
+//              lane quarters, e4m3 codes and scales); down: Y rows (fp32).
 // The activation scales are read straight from global memory one K block
 // ahead (the tile's 32 rows x K/128 floats stay in L1), which frees the
 // shared memory that a second stage-sized buffer would need.
