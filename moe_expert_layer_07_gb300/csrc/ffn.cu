@@ -101,18 +101,6 @@ struct FfnArgs {
     int32_t *status;
 };
 
-// Two independent IEEE fp32 FMAs in one instruction (the bits of two fmaf).
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t pack2(uint32_t lo, uint32_t hi) {
-    uint64_t d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
-    return d;
-}
-
 struct Unit {
     bool down;
     int g, mt, j, row0, nvalid;

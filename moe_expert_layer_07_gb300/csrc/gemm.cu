@@ -417,10 +417,11 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                     ok = false;
                     break;
                 }
-                float acc[CB];   // columns n0 .. n0 + CB - 1
+                // columns n0 + 2p, n0 + 2p + 1 side by side for the paired FMA
+                uint64_t acc2[CB / 2];
                 float accu[SW ? BN : 1];
 #pragma unroll
-                for (int n = 0; n < CB; ++n) acc[n] = 0.0f;
+                for (int p = 0; p < CB / 2; ++p) acc2[p] = 0ull;
 #pragma unroll
                 for (int n = 0; n < (SW ? BN : 1); ++n) accu[n] = 0.0f;
                 for (int kb = 0; kb < KB; ++kb) {
@@ -458,12 +459,12 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                         if (c < nch) {
 #pragma unroll
                             for (int j4 = 0; j4 < 4; ++j4) {
-                                const float4 f = reinterpret_cast<const float4 *>(sxw)[c * 4 + j4];
-                                const int n = c * 16 + j4 * 4;
-                                acc[n] = fmaf(__uint_as_float(v[c][j4 * 4]), f.x, acc[n]);
-                                acc[n + 1] = fmaf(__uint_as_float(v[c][j4 * 4 + 1]), f.y, acc[n + 1]);
-                                acc[n + 2] = fmaf(__uint_as_float(v[c][j4 * 4 + 2]), f.z, acc[n + 2]);
-                                acc[n + 3] = fmaf(__uint_as_float(v[c][j4 * 4 + 3]), f.w, acc[n + 3]);
+                                const uint4 f = reinterpret_cast<const uint4 *>(sxw)[c * 4 + j4];
+                                const int p = (c * 16 + j4 * 4) / 2;
+                                acc2[p] = fma2(pack2(v[c][j4 * 4], v[c][j4 * 4 + 1]), pack2(f.x, f.y),
+                                               acc2[p]);
+                                acc2[p + 1] = fma2(pack2(v[c][j4 * 4 + 2], v[c][j4 * 4 + 3]),
+                                                   pack2(f.z, f.w), acc2[p + 1]);
                             }
                         }
                     if constexpr (SW) {   // up rows: same activation scales, their own block scale
@@ -499,6 +500,12 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                     }
                 }
                 if (!ok) break;
+                float acc[CB];   // columns n0 .. n0 + CB - 1
+#pragma unroll
+                for (int p = 0; p < CB / 2; ++p) {
+                    acc[2 * p] = __uint_as_float((uint32_t)acc2[p]);
+                    acc[2 * p + 1] = __uint_as_float((uint32_t)(acc2[p] >> 32));
+                }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&scale_empty[b]));
                 if constexpr (SW) {
