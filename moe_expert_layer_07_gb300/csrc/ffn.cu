@@ -27,7 +27,7 @@
 // claims the next, so a unit that is waited on is always in some running
 // CTA's pipeline: no wait can be circular.
 //
-// Per CTA (two per SM), 10 warps (FP8) or 6 (BF16):
+// Per CTA (two per SM), 10 warps:
 //   warp 0     scheduler + TMA producer: a 2-deep ring of 40 KB stages; a
 //              gate/up stage holds one 128-byte K block (gate box, up box,
 //              activation rows), a down stage two K blocks (two W2 boxes,
@@ -36,9 +36,8 @@
 //   warp 1     MMA issuer: tcgen05.mma (kind::f8f6f4 or kind::f16),
 //              tcgen05.commit to mbarriers; four TMEM accumulators rotate,
 //              FP8 one per K block, BF16 one per unit.
-//   warps 2-9  epilogue (FP8: eight warps, each a TMEM lane quarter of 16
-//   (BF16 2-5) of the 32 activation columns; BF16: four warps, all 32;
-//              thread = weight row):
+//   warps 2-9  epilogue: each warp reads one TMEM lane quarter (thread =
+//              weight row) of 16 of the 32 activation columns:
 //              FP8: per K block the partial product times
 //              x_scale[r, kb] * w_scale[g, m/128, kb] is added to fp32
 //              registers (paired FMAs; the factors reach the warp as
@@ -674,6 +673,13 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                 // publish: every epilogue warp's h stores, then one release
                 fence_proxy_async_global();
                 __syncwarp();
+                if constexpr (!FP8) {
+                    // hdone_bar[b] served gate/up tile n_done_gu - 2 before: that
+                    // phase must be complete before this arrival, or a warp two
+                    // tiles ahead could finish it for a slower one (FP8 warps
+                    // are held in step by the amax exchange)
+                    if (!wwait(&hdone_bar[b], par ^ 1u)) break;
+                }
                 if (lane == 0) mbar_arrive(smem_u32(&hdone_bar[b]));
                 if (ew == 0) {   // warp 2 publishes
                     if (!wwait(&hdone_bar[b], par)) break;
@@ -717,8 +723,9 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
                     bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
                     bool sched_zeroed, int32_t *status, cudaStream_t s) {
     if (rows == 0) return MOE_OK;
-    // FP8 promotes every K block in the epilogue: two warpgroups share that work
-    constexpr int kEW = FP8 ? 2 : 1;
+    // two epilogue warpgroups: FP8 promotes every K block, and more warps per
+    // SM sub-partition hide those latencies (BF16: neutral to slightly faster)
+    constexpr int kEW = 2;
     static std::once_flag attr_once[64];
     static int attr_rc[64];
     int dev = 0;
