@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
     __shared__ int s_ring[kRing];
     __shared__ int s_off[kMaxGroups + 1];
     __shared__ int s_nt[kMaxGroups + 1];
-    __shared__ float s_amax[2][4 * kBN];   // per gate/up tile: each epilogue warp's row maxima
+    __shared__ float s_amax[2][4 * kBN];   // per gate/up tile: each lane quarter's column maxima
     // per epilogue warp and K-block parity: every column's promotion factor
     // x_scale[n, kb] * w_scale[kb] (gate, then up), read as 16-byte broadcasts
     constexpr int CB = kBN / EW;   // activation columns per epilogue warp
