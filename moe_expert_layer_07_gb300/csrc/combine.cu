@@ -23,7 +23,10 @@ constexpr int kMaxRows = kMaxShared + kMaxK;
 
 // grid: (T, column blocks); each thread handles 4 consecutive columns.  All
 // rows of the token are loaded before the first addition, so their memory
-// latencies overlap; the additions then run in the fixed order.
+// latencies overlap; the additions then run in the fixed order.  NR bounds
+// the rows per token (shared + top-k) held in registers: a small bound keeps
+// the kernel's registers, and so its resident CTAs and loads in flight, up.
+template <int NR>
 __global__ void __launch_bounds__(kThreads)
     combine_kernel(const float *__restrict__ y, const int32_t *__restrict__ row_of_slot,
                    const float *__restrict__ topk_w, const int32_t *__restrict__ offsets,
@@ -45,14 +48,14 @@ __global__ void __launch_bounds__(kThreads)
     const int v = blockIdx.y * kThreads + threadIdx.x;   // 4-column vector index
     if (v * 4 >= H) return;
     const int n = S + k;
-    float4 val[kMaxRows];
+    float4 val[NR];
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r)
+    for (int r = 0; r < NR; ++r)
         if (r < n && rows[r] >= 0)
             val[r] = __ldg(reinterpret_cast<const float4 *>(y + rows[r] * H) + v);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int r = 0; r < kMaxRows; ++r) {
+    for (int r = 0; r < NR; ++r) {
         if (r >= n || rows[r] < 0) continue;
         const float x[4] = {val[r].x, val[r].y, val[r].z, val[r].w};
         if (r < S) {
@@ -86,7 +89,8 @@ int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *r
     const int H = cfg->hidden;
     if (cfg->num_shared + cfg->top_k > kMaxRows) return MOE_ERR_UNSUPPORTED_SHAPE;
     const dim3 grid(T, (unsigned)ceil_div(H / 4, kThreads));
-    if (launch_dependent(combine_kernel, grid, dim3(kThreads), 0, s, static_cast<const float *>(y),
+    auto kern = cfg->num_shared + cfg->top_k <= 10 ? combine_kernel<10> : combine_kernel<kMaxRows>;
+    if (launch_dependent(kern, grid, dim3(kThreads), 0, s, static_cast<const float *>(y),
                          row_of_slot, topk_w, offsets, out, (int)(out_dtype == MOE_OUT_BF16), T,
                          H, cfg->num_experts, cfg->num_shared, cfg->top_k))
         return MOE_ERR_CUDA;
