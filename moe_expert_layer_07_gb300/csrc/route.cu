@@ -32,9 +32,7 @@
 namespace moe {
 namespace {
 
-constexpr int kTB = 4;   // tokens per warp tile
-constexpr int kEB = 8;   // experts per warp tile
-static_assert(kTB * kEB == 32, "one output per lane");
+constexpr int kEB = 8;   // experts per warp tile (tokens per warp tile: TB, 4 or 8)
 
 __device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
@@ -60,11 +58,14 @@ __device__ __forceinline__ float bf_elem(const uint4 &a, int e) {
     return (e & 1) ? bf_hi(w) : bf_lo(w);
 }
 
-// CTA tile of 16 tokens x 16 experts, 8 warps of 4 tokens x 8 experts each.
-// The CTA stages 256 hidden elements of its 32 rows per step in shared
-// memory (cp.async, 4-deep ring), so every row is fetched once per CTA
-// instead of once per warp.  Lane L still reads elements 8L..8L+7 of every
-// 256-element step, i.e. the hidden slice (h/8) mod 32 == L, in increasing h.
+// CTA tile of 16 tokens x 16 experts: 8 warps of 4 tokens x 8 experts each
+// (TB = 4), or 4 warps of 8 x 8 (TB = 8: each staged value feeds twice the
+// FMAs, for fewer shared-memory loads and widenings per output, at the cost
+// of registers; taken for large batches).  The CTA stages 256 hidden
+// elements of its 32 rows per step in shared memory (cp.async, 4-deep ring),
+// so every row is fetched once per CTA instead of once per warp.  Lane L
+// reads elements 8L..8L+7 of every 256-element step, i.e. the hidden slice
+// (h/8) mod 32 == L, in increasing h, whatever TB.
 constexpr int kCT = 16, kCE = 16;           // CTA tile
 constexpr int kStepElems = 256;             // hidden elements per stage
 constexpr int kLogitStages = 4;
@@ -77,7 +78,8 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool v
                  : "memory");
 }
 
-__global__ void __launch_bounds__(256)
+template <int TB>
+__global__ void __launch_bounds__(TB == 4 ? 256 : 128)
     gate_logits_kernel(const uint16_t *__restrict__ x, const uint16_t *__restrict__ wg,
                        const float *__restrict__ offset, float *__restrict__ logits, int T,
                        int E, int H, const L2Prefetch pf) {
@@ -117,11 +119,12 @@ __global__ void __launch_bounds__(256)
     const uint32_t sbase = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
 
     // stage s: 32 rows (16 tokens then 16 experts) x 32 pieces of 16 bytes
+    constexpr int NT = TB == 4 ? 256 : 128;   // threads: (16 / TB) x 2 warps
     auto issue = [&](int step) {
         const uint32_t buf = sbase + (step % kLogitStages) * kStageBytes;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int p = tid + 256 * i;
+        for (int i = 0; i < 1024 / NT; ++i) {
+            const int p = tid + NT * i;
             const int r = p >> 5, piece = p & 31;
             const int h = step * kStepElems + piece * 8;
             const bool is_x = r < kCT;
@@ -133,12 +136,12 @@ __global__ void __launch_bounds__(256)
     };
 
     // accumulators of experts (2p, 2p + 1) side by side for the paired FMA
-    uint64_t acc2[kTB][kEB / 2];
+    uint64_t acc2[TB][kEB / 2];
 #pragma unroll
-    for (int i = 0; i < kTB; ++i)
+    for (int i = 0; i < TB; ++i)
 #pragma unroll
         for (int p = 0; p < kEB / 2; ++p) acc2[i][p] = 0ull;
-    const int wt = warp >> 1, we = warp & 1;   // warp tile: tokens 4wt.., experts 8we..
+    const int wt = warp >> 1, we = warp & 1;   // warp tile: tokens TB wt.., experts 8we..
 
 #pragma unroll
     for (int st = 0; st < kLogitStages - 1; ++st) {
@@ -151,10 +154,10 @@ __global__ void __launch_bounds__(256)
         if (step + kLogitStages - 1 < steps) issue(step + kLogitStages - 1);
         asm volatile("cp.async.commit_group;" ::: "memory");
         const uint8_t *buf = smem + (step % kLogitStages) * kStageBytes;
-        uint4 xv[kTB], wv[kEB];
+        uint4 xv[TB], wv[kEB];
 #pragma unroll
-        for (int i = 0; i < kTB; ++i)
-            xv[i] = *reinterpret_cast<const uint4 *>(buf + (wt * kTB + i) * (kStepElems * 2) + lane * 16);
+        for (int i = 0; i < TB; ++i)
+            xv[i] = *reinterpret_cast<const uint4 *>(buf + (wt * TB + i) * (kStepElems * 2) + lane * 16);
 #pragma unroll
         for (int j = 0; j < kEB; ++j)
             wv[j] = *reinterpret_cast<const uint4 *>(buf + (kCT + we * kEB + j) * (kStepElems * 2) + lane * 16);
@@ -163,9 +166,9 @@ __global__ void __launch_bounds__(256)
         // products in increasing h (two accumulators per paired FMA)
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            uint64_t x2[kTB], w2[kEB / 2];
+            uint64_t x2[TB], w2[kEB / 2];
 #pragma unroll
-            for (int i = 0; i < kTB; ++i) {
+            for (int i = 0; i < TB; ++i) {
                 const float xf = bf_elem(xv[i], e);
                 x2[i] = pack2(xf, xf);
             }
@@ -173,25 +176,34 @@ __global__ void __launch_bounds__(256)
             for (int p = 0; p < kEB / 2; ++p)
                 w2[p] = pack2(bf_elem(wv[2 * p], e), bf_elem(wv[2 * p + 1], e));
 #pragma unroll
-            for (int i = 0; i < kTB; ++i)
+            for (int i = 0; i < TB; ++i)
 #pragma unroll
                 for (int p = 0; p < kEB / 2; ++p) acc2[i][p] = fma2(x2[i], w2[p], acc2[i][p]);
         }
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
 
-    float mine = 0.0f;
+    // output o = i kEB + j of the warp tile ends in lane o mod 32, slot o / 32
+    constexpr int NO = TB * kEB / 32;
+    float mine[NO];
 #pragma unroll
-    for (int i = 0; i < kTB; ++i)
+    for (int q = 0; q < NO; ++q) mine[q] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < TB; ++i)
 #pragma unroll
         for (int j = 0; j < kEB; ++j) {
             float v = (j & 1) ? hi2(acc2[i][j >> 1]) : lo2(acc2[i][j >> 1]);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) v = __fadd_rn(v, __shfl_xor_sync(0xffffffffu, v, o));
-            if (lane == i * kEB + j) mine = v;
+            if (lane == ((i * kEB + j) & 31)) mine[(i * kEB + j) >> 5] = v;
         }
-    const int t = t_base + wt * kTB + lane / kEB, e = e_base + we * kEB + lane % kEB;
-    if (t < T && e < E) logits[(size_t)t * E + e] = offset ? __fadd_rn(mine, offset[e]) : mine;
+#pragma unroll
+    for (int q = 0; q < NO; ++q) {
+        const int o = q * 32 + lane;
+        const int t = t_base + wt * TB + o / kEB, e = e_base + we * kEB + o % kEB;
+        if (t < T && e < E)
+            logits[(size_t)t * E + e] = offset ? __fadd_rn(mine[q], offset[e]) : mine[q];
+    }
 }
 
 struct SelectArgs {
@@ -445,15 +457,30 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
     std::call_once(attr_once[dev], [&] {
-        attr_rc[dev] = cudaFuncSetAttribute(gate_logits_kernel,
+        attr_rc[dev] = cudaFuncSetAttribute(gate_logits_kernel<4>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
-                               cudaSuccess ? 0 : 1;
+                               cudaSuccess &&
+                               cudaFuncSetAttribute(gate_logits_kernel<8>,
+                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                    smem) == cudaSuccess
+                           ? 0
+                           : 1;
     });
     if (attr_rc[dev]) return MOE_ERR_CUDA;
     const L2Prefetch none;
-    gate_logits_kernel<<<grid, 256, smem, s>>>(static_cast<const uint16_t *>(x),
-                                               static_cast<const uint16_t *>(w_gate),
-                                               logit_offset, logits, T, E, H, pf ? *pf : none);
+    // 8 x 8 warp tiles once the CTAs outnumber a few per SM; decode batches
+    // keep 8 warps per CTA for latency hiding.  Both give the same bits.
+    const bool big = (int64_t)grid.x * grid.y >= 4 * (int64_t)sm_count();
+    if (big)
+        gate_logits_kernel<8><<<grid, 128, smem, s>>>(static_cast<const uint16_t *>(x),
+                                                      static_cast<const uint16_t *>(w_gate),
+                                                      logit_offset, logits, T, E, H,
+                                                      pf ? *pf : none);
+    else
+        gate_logits_kernel<4><<<grid, 256, smem, s>>>(static_cast<const uint16_t *>(x),
+                                                      static_cast<const uint16_t *>(w_gate),
+                                                      logit_offset, logits, T, E, H,
+                                                      pf ? *pf : none);
     MOE_LAUNCH_CHECK();
 
     SelectArgs a;
