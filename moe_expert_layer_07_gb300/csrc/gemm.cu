@@ -85,7 +85,7 @@ struct GemmShape {
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 64, "BN");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols * kCtasPerSm <= 512,
                   "TMEM columns");
-    static constexpr int kSxElems = FP8 ? 4 * EW * 2 * kNA * kCB : 1;   // per warp, per K-block parity
+    static constexpr int kSxElems = (FP8 && SW) ? 4 * EW * 2 * kNA * kCB : 1;   // per warp, per K-block parity
     static_assert((kSmemBytes + 8 * kXsElems + 8 * kWsElems + 8 * kAmaxElems + 4 * kSxElems +
                    8 * 1024 + 1024) *
                           kCtasPerSm <=
@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
     __shared__ __align__(8) uint64_t scale_full[2];
     __shared__ __align__(8) uint64_t scale_empty[2];
     __shared__ __align__(8) uint64_t amax_bar[2];
+    __shared__ __align__(8) uint64_t fac_bar[2];
     __shared__ __align__(8) uint64_t drain_bar;
     __shared__ uint32_t tmem_slot;
     __shared__ int s_abort, s_bad;
@@ -153,7 +154,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
     // the weight-block scale, and the activation scale of every row n laid
     // out [kb][n] so that lanes read consecutive words.
     __shared__ float s_ws[2][S::kWsElems];
-    __shared__ float s_xs[2][S::kXsElems];
+    __shared__ __align__(16) float s_xs[2][S::kXsElems];
     // SwiGLU + FP8: per tile, each epilogue warp's |h| maximum of every row n
     __shared__ float s_amax[2][S::kAmaxElems];
     // FP8: per epilogue warp, the K block's promotion factor of every column
@@ -183,6 +184,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
             mbar_init(smem_u32(&scale_full[b]), S::kEpiThreads);   // every epilogue thread's copies
             mbar_init(smem_u32(&scale_empty[b]), 4 * EW);          // every epilogue warp done reading
             mbar_init(smem_u32(&amax_bar[b]), 4);       // every epilogue warp's row maxima
+            mbar_init(smem_u32(&fac_bar[b]), 4 * EW);   // every epilogue warp's share of factors
         }
         mbar_init(smem_u32(&drain_bar), 1);
         s_abort = 0;
@@ -417,6 +419,23 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                     ok = false;
                     break;
                 }
+                if constexpr (!SW) {
+                    // promotion factors of the whole tile, in place, once:
+                    // s_xs[b][kb BN + n] = x_scale[n, kb] * w_scale[kb] (0 past
+                    // the tile's rows); the K loop then reads them directly
+                    float *xs = s_xs[b];
+                    for (int i = etid; i < KB * BN; i += S::kEpiThreads) {
+                        const int kb = i / BN, n = i - kb * BN;
+                        xs[i] = n < tl.nvalid ? __fmul_rn(xs[i], s_ws[b][kb]) : 0.0f;
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&fac_bar[b]));
+                    if (!wait_bounded(smem_u32(&fac_bar[b]), ((uint32_t)it >> 1) & 1u, abort_flag,
+                                      args.status, MOE_DEV_TIMEOUT)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 // columns n0 + 2p, n0 + 2p + 1 side by side for the paired FMA
                 uint64_t acc2[CB / 2];
                 float accu[SW ? BN : 1];
@@ -425,20 +444,25 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
 #pragma unroll
                 for (int n = 0; n < (SW ? BN : 1); ++n) accu[n] = 0.0f;
                 for (int kb = 0; kb < KB; ++kb) {
-                    const float sw = s_ws[b][kb];
-                    const float swu = SW ? s_ws[b][KB + kb] : 0.0f;
-                    // factors of this warp's columns n0 + j, at sxw[j] (gate) and sxw[CB + j] (up)
-                    float *sxw = s_sx + (ew * 2 + (kb & 1)) * (S::kNA * CB);
+                    // factors of this warp's columns n0 + j: SwiGLU at sxw[j] (gate) and
+                    // sxw[CB + j] (up), made per K block; otherwise the tile's own
+                    const float *sxw = s_xs[b] + kb * BN + n0;
+                    if constexpr (SW) {
+                        const float sw = s_ws[b][kb];
+                        const float swu = s_ws[b][KB + kb];
+                        float *sx = s_sx + (ew * 2 + (kb & 1)) * (S::kNA * CB);
 #pragma unroll
-                    for (int h = 0; h < (CB + 31) / 32; ++h) {
-                        const int j = h * 32 + lane, n = n0 + j;
-                        if (j < CB) {
-                            const float xv = n < tl.nvalid ? s_xs[b][kb * BN + n] : 0.0f;
-                            sxw[j] = __fmul_rn(xv, sw);
-                            if (SW) sxw[CB + j] = __fmul_rn(xv, swu);
+                        for (int h = 0; h < (CB + 31) / 32; ++h) {
+                            const int j = h * 32 + lane, n = n0 + j;
+                            if (j < CB) {
+                                const float xv = n < tl.nvalid ? s_xs[b][kb * BN + n] : 0.0f;
+                                sx[j] = __fmul_rn(xv, sw);
+                                sx[CB + j] = __fmul_rn(xv, swu);
+                            }
                         }
+                        __syncwarp();
+                        sxw = sx;
                     }
-                    __syncwarp();
                     if (!wait_bounded(smem_u32(&acc_full[ab]), aphase, abort_flag, args.status,
                                       MOE_DEV_TIMEOUT)) {
                         ok = false;
