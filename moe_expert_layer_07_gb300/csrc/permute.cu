@@ -194,7 +194,18 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const PermArgs a) 
     const long row_bytes = a.fp8 ? a.H : 2L * a.H;
     const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (long)t * row_bytes);
     uint4 *dst = reinterpret_cast<uint4 *>(a.xp + row * row_bytes);
-    for (long v = lane; v < row_bytes / 16; v += 32) dst[v] = __ldg(src + v);
+    // up to 8 loads per lane in flight before their stores (a 7168-byte row:
+    // two rounds; same-box at 4096 tokens 68.6 -> 67.1 us)
+    const long nvec = row_bytes / 16;
+    for (long v0 = lane; v0 < nvec; v0 += 32 * 8) {
+        uint4 buf[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (v0 + 32 * u < nvec) buf[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+            if (v0 + 32 * u < nvec) dst[v0 + 32 * u] = buf[u];
+    }
     if (a.fp8) {
         const int ng = a.H / 128;
         for (int g = lane; g < ng; g += 32) a.xps[row * ng + g] = __ldg(a.xs + (long)t * ng + g);
