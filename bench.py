@@ -257,8 +257,10 @@ class Stepper:
         return {n: v / k for n, v in acc.items()}
 
 
-def algorithmic_bytes(shape, offsets):
-    """Bytes the method must move, per stage, given the rows per group."""
+def path_bytes(shape, offsets):
+    """Bytes this path moves, per stage, given the rows per group: the method's
+    bytes plus the intermediates it keeps at higher precision (fp32 Y; the wide
+    path's fp32 gate/up rows).  Used for the per-stage split only."""
     T, H, I, E, S, k = (shape.tokens, shape.hidden, shape.inter, shape.num_experts,
                         shape.num_shared, shape.top_k)
     fp8 = shape.dtype == "fp8"
@@ -266,8 +268,7 @@ def algorithmic_bytes(shape, offsets):
     rows = T * (k + S)
     counts = np.diff(offsets)
     active = int((counts > 0).sum())
-    w13 = 2 * I * H * eb + (4 * (2 * I // 128) * (H // 128) if fp8 else 0)
-    w2 = H * I * eb + (4 * (H // 128) * (I // 128) if fp8 else 0)
+    w13, w2 = expert_weight_bytes(shape)
     sc_h = 4 * (H // 128) if fp8 else 0
     sc_i = 4 * (I // 128) if fp8 else 0
     b = {}
@@ -284,6 +285,44 @@ def algorithmic_bytes(shape, offsets):
     b["combine"] = T * (k + S) * H * 4 + 8 * T * k + T * H * 4
     flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)
     return b, active, flops
+
+
+def expert_weight_bytes(shape):
+    """Weights + block scales of one expert group: (gate/up, down).  R1:
+    29,360,128 + 7,168 and 14,680,064 + 3,584 bytes."""
+    H, I = shape.hidden, shape.inter
+    fp8 = shape.dtype == "fp8"
+    eb = 1 if fp8 else 2
+    w13 = 2 * I * H * eb + (4 * (2 * I // 128) * (H // 128) if fp8 else 0)
+    w2 = H * I * eb + (4 * (H // 128) * (I // 128) if fp8 else 0)
+    return w13, w2
+
+
+def method_bytes(shape, active):
+    """Bytes the layer must move by its definition, whatever the kernels keep
+    in between: every active group's weights and block scales once, the gate
+    weights, x read, its FP8 codes (and row scales) written and read, the
+    dispatched rows written and read, h written and read, the expert outputs Y
+    as bf16 written and read, and the bf16 output.  This path's wider
+    intermediates (fp32 Y, fp32 gate/up rows of wide batches) are not counted,
+    so the layer's roofline fraction is not flattered by them."""
+    T, H, I, E, S, k = (shape.tokens, shape.hidden, shape.inter, shape.num_experts,
+                        shape.num_shared, shape.top_k)
+    fp8 = shape.dtype == "fp8"
+    eb = 1 if fp8 else 2
+    rows = T * (k + S)
+    sc_h = 4 * (H // 128) if fp8 else 0
+    sc_i = 4 * (I // 128) if fp8 else 0
+    w13, w2 = expert_weight_bytes(shape)
+    b = active * (w13 + w2) + 2 * E * H            # experts + gate
+    b += 2 * T * H                                 # x
+    if fp8:
+        b += 2 * T * (H + sc_h)                    # x codes written and read
+    b += 2 * rows * (H * eb + sc_h)                # dispatched rows
+    b += 2 * rows * (I * eb + sc_i)                # h
+    b += 2 * rows * H * 2                          # Y (bf16)
+    b += 2 * T * H                                 # output (bf16)
+    return b
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -383,16 +422,22 @@ def main():
     torch.cuda.synchronize()
     kms = stepper.kernel_ms()
     offsets = layer.view("expert_offsets", torch.int32, (shape.groups + 1,)).cpu().numpy()
-    bytes_per, active, flops = algorithmic_bytes(shape, offsets)
+    bytes_per, active, flops = path_bytes(shape, offsets)
     ms_step = elapsed_ms / args.steps
     value = job_tokens_per_s(T, world, args.steps, elapsed_ms)
 
     hbm_peak, bf16_peak, peak_src = load_peaks()
-    layer_bytes = sum(bytes_per.values())
+    layer_bytes = method_bytes(shape, active)      # the method's bytes per step
+    path_total = sum(bytes_per.values())           # + this path's wider intermediates
     top = "expert_ffn" if stepper.fused else "gemm_gate_up_swiglu"
     top_label = ("expert_ffn (gate/up + SwiGLU + down, one kernel)" if stepper.fused
                  else "grouped_gemm gate/up + SwiGLU")
-    achieved = bytes_per[top] / (top_ms / 1e3) / 1e9
+    # algorithmic bytes of the dominant launch: the weights and block scales of
+    # every active group it streams (gate/up + down, or gate/up alone)
+    w13_b, w2_b = expert_weight_bytes(shape)
+    unit_bytes = w13_b + w2_b if stepper.fused else w13_b
+    top_bytes = active * unit_bytes
+    achieved = top_bytes / (top_ms / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168 and \
@@ -422,6 +467,9 @@ def main():
         "config": {**workload_config(shape, world), **perm_info},
         "hbm_gbs": layer_bytes / (ms_step / 1e3) / 1e9,
         "layer_roofline_frac": (layer_bytes / (hbm_peak * 1e9)) / (ms_step / 1e3),
+        "layer_bytes": layer_bytes,
+        "path_bytes": path_total,
+        "path_hbm_gbs": path_total / (ms_step / 1e3) / 1e9,
         "active_experts": active,
         "kernels_ms": {k: round(v, 5) for k, v in kms.items()},
         "kernels_ms_note": "per-stage split from a separate pass with events between all "
@@ -429,7 +477,10 @@ def main():
                            "kernel only",
         "roofline": {"bound": "hbm", "kernel": top_label, "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)"},
+                     "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
+                     "bytes_per_unit": unit_bytes, "units": active,
+                     "work_unit": "active expert group (weights + block scales)",
+                     "ms_per_launch": top_ms},
         "tensor_pipe_frac_of_bf16x2": (flops / (ms_step / 1e3)) / (2 * bf16_peak * 1e12),
         "gpu_launches": args.steps * moe.layer_kernel_count(layer.cfg, T),
         "device_status": status,
