@@ -526,9 +526,13 @@ def test_bounded_wait_reports_timeout_and_context_survives(lib):
 
 @pytest.mark.parametrize("fp8,inter,K,counts", [
     (True, 384, 1024, GEMM_ROWS), (True, 2048, 7168, [3, 0, 17, 40, 128, 1]),
+    (True, 384, 1024, [0, 1, 15, 16, 17, 3, 9, 2, 0, 5, 31]),
+    (True, 2048, 7168, [2, 0, 9, 1, 14, 3]),
     (False, 384, 512, GEMM_ROWS)])
 def test_swiglu_epilogue_equals_gemm_then_silu_requant(lib, fp8, inter, K, counts):
-    """The fused gate/up + SwiGLU kernel gives the bits of the two-kernel path."""
+    """The fused gate/up + SwiGLU kernel gives the bits of the two-kernel path,
+    for groups averaging 16 rows or more (the first two cases, where the plain
+    GEMM takes 64-row tiles) and fewer (the next two)."""
     s = synth.CONFIGS["r1_mini" if fp8 else "bf16_mini"]
     cfg = moe.make_config(s)
     counts = np.array(counts)
