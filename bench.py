@@ -11,8 +11,10 @@ tensors of the workload's shape, resident in HBM before timing starts; the
 flush is needed between steps.
 
 Prints one JSON line (rank 0).  `value` is tokens/s over all ranks;
-`roofline` describes the dominant kernel (grouped GEMM gate/up) against the
-measured HBM copy bandwidth; `e2e` is the same metric through the layer's
+`layer_roofline_frac` divides the bytes the layer must move by its definition
+by the measured HBM copy bandwidth; `roofline` describes the dominant kernel
+(the one-kernel expert FFN at decode, the gate/up GEMM for wide batches) by
+the weight bytes it streams; `e2e` is the same metric through the layer's
 public call with pinned host buffers copied in and out each step;
 `cpu_baseline` times the CPU oracle on a bounded sample of the workload.
 --impl reference times the CPU oracle itself as the reference arm.
