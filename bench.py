@@ -4,8 +4,9 @@
                   [--workload r1_decode_t128] [--seed S]
 
 A step is one pass of the whole hot path over one batch: routing, FP8
-quantisation of x, dispatch permutation, grouped GEMM gate/up, SiLU-mul +
-requantisation, grouped GEMM down, combine.  Inputs are seeded synthetic
+quantisation of x, dispatch permutation, the expert FFN (one persistent
+kernel for decode batches and BF16 layers; gate/up GEMM, SiLU-mul +
+requantisation and down GEMM for wide FP8 batches), combine.  Inputs are seeded synthetic
 tensors of the workload's shape, resident in HBM before timing starts; the
 11 GB of expert weights streamed per step are far larger than L2, so no L2
 flush is needed between steps.
