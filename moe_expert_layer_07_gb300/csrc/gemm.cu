@@ -3,13 +3,14 @@
 //   C[r, n] = sum_k A[r, k] W[g, n, k]   for rows r of group g
 //
 // Weight rows are the MMA's M side (128 per tile) and the few token rows of
-// an expert its N side (16..BN = 32 per tile), so that a decode-sized expert with
-// a handful of rows still streams its weights at full tile efficiency.  The
-// SGLang/H20 article (section "SwapAB GEMM") makes the same swap on Hopper,
-// where WGMMA fixes M = 64; tcgen05 with M = 128 and N a multiple of 16 is
-// the analogue here.
+// an expert its N side (16..BN per tile, BN = 32 for decode-sized groups and
+// 64 for groups averaging 16 rows or more), so that a decode-sized expert
+// with a handful of rows still streams its weights at full tile efficiency.
+// The SGLang/H20 article (section "SwapAB GEMM") makes the same swap on
+// Hopper, where WGMMA fixes M = 64; tcgen05 with M = 128 and N a multiple of
+// 16 is the analogue here.
 //
-// Persistent CTAs, two per SM, 6 warps each:
+// Persistent CTAs, two per SM, 2 + 4 EW warps each:
 //   warp 0      TMA producer: per K-block a 128 x 128-byte weight box (from
 //               row-major weights, or one contiguous 16 KB tile of packed
 //               weights) and ceil(rows/16) 16 x 128-byte activation boxes,
@@ -17,15 +18,17 @@
 //   warp 1      MMA issuer (one thread): tcgen05.mma, K = 32 bytes per
 //               instruction, accumulators in tensor memory, completion
 //               signalled with tcgen05.commit.
-//   warps 2-5   epilogue: tcgen05.ld of the accumulator (thread = weight
-//               row), then
+//   warps 2..   epilogue (EW warpgroups; warp 2 + 4h + j reads TMEM lane
+//               quarter j of the h-th BN/EW columns; thread = weight row):
+//               tcgen05.ld of the accumulator, then
 //                 FP8: per 128-wide K block, the block's partial product is
 //                 scaled by w_scale[g, m/128, kb] * a_scale[r, kb] and added
-//                 to fp32 registers; four TMEM buffers rotate so the MMAs
-//                 of the next blocks run meanwhile, and the tile's scales
-//                 are copied to shared memory one tile ahead (cp.async,
-//                 completion on an mbarrier), whence each column's factor
-//                 reaches the warp as a 16-byte broadcast;
+//                 to fp32 registers (paired FMAs); four TMEM buffers rotate
+//                 so the MMAs of the next blocks run meanwhile, and the
+//                 tile's scales are copied to shared memory one tile ahead
+//                 (cp.async, completion on an mbarrier), turned into the
+//                 tile's promotion factors once, and read back as 16-byte
+//                 broadcasts;
 //                 BF16: one accumulation over all of K (the four TMEM
 //                 buffers rotate between tiles);
 //               and stores C (coalesced: a warp writes 32 consecutive n).
