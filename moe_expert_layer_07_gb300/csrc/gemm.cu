@@ -27,8 +27,9 @@
 //                 so the MMAs of the next blocks run meanwhile, and the
 //                 tile's scales are copied to shared memory one tile ahead
 //                 (cp.async, completion on an mbarrier), turned into the
-//                 tile's promotion factors once, and read back as 16-byte
-//                 broadcasts;
+//                 tile's promotion factors once (the SwiGLU instance makes
+//                 its gate and up factors per K block), and read back as
+//                 16-byte broadcasts;
 //                 BF16: one accumulation over all of K (the four TMEM
 //                 buffers rotate between tiles);
 //               and stores C (coalesced: a warp writes 32 consecutive n).
