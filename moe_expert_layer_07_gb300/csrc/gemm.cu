@@ -13,8 +13,9 @@
 // Persistent CTAs, two per SM, 2 + 4 EW warps each:
 //   warp 0      TMA producer: per K-block a 128 x 128-byte weight box (from
 //               row-major weights, or one contiguous 16 KB tile of packed
-//               weights) and ceil(rows/16) 16 x 128-byte activation boxes,
-//               128-byte swizzled, into a STAGES-deep shared-memory ring.
+//               weights) and ceil(rows/16) 16 x 128-byte activation boxes
+//               (wide FP8 tiles: one 64-row box), 128-byte swizzled, into a
+//               STAGES-deep shared-memory ring.
 //   warp 1      MMA issuer (one thread): tcgen05.mma, K = 32 bytes per
 //               instruction, accumulators in tensor memory, completion
 //               signalled with tcgen05.commit.
@@ -86,6 +87,10 @@ struct GemmShape {
     static constexpr int kXsElems = FP8 ? BN * kMaxKBlocks : 1;
     static constexpr int kWsElems = FP8 ? kNA * kMaxKBlocks : 1;
     static constexpr int kAmaxElems = (SW && FP8) ? 4 * BN : 1;
+    // activation rows per TMA box: the wide FP8 tiles load all BN rows with
+    // one box (a TMA instruction less in the producer's loop per 16 rows);
+    // the others ceil(rows / 16) boxes of 16
+    static constexpr int kABox = (FP8 && !SW && EW > 1) ? BN : kBoxRows;
     static_assert(BN % 16 == 0 && BN >= 32 && BN <= 64, "BN");
     static_assert((kTmemCols & (kTmemCols - 1)) == 0 && kTmemCols * kCtasPerSm <= 512,
                   "TMEM columns");
@@ -258,8 +263,8 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
             bool ok = true;
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile<BN>(t, G, s_tiles, s_off);
-                const int nbox = (tl.nvalid + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = S::kNA * S::kABytes + nbox * kBoxRows * 128;
+                const int nbox = (tl.nvalid + S::kABox - 1) / S::kABox;
+                const uint32_t bytes = S::kNA * S::kABytes + nbox * S::kABox * 128;
                 const int wrow = tl.g * args.n_out + tl.mt * kBM;   // SwiGLU: gate rows
                 const int wrow_up = wrow + args.n_out / 2;          // SwiGLU: up rows
                 // tiled W: the box of (128-row block b, K block kb) is rows
@@ -288,8 +293,8 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                                         pol_w);
                     }
                     for (int b = 0; b < nbox; ++b)
-                        tma_load_2d(sb + b * kBoxRows * 128, &tmA, kb * S::kKPerStage,
-                                    tl.row0 + b * kBoxRows, fb, pol_a);
+                        tma_load_2d(sb + b * S::kABox * 128, &tmA, kb * S::kKPerStage,
+                                    tl.row0 + b * S::kABox, fb, pol_a);
                     issued |= 1u << stage;
                     parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
@@ -703,7 +708,7 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
                         (uint64_t)args.groups * args.n_out * (args.k_dim / Sh::kKPerStage), kBM)
             : encode_2d(&tmW, w, FP8, (uint64_t)args.k_dim, (uint64_t)args.groups * args.n_out, kBM);
     if (!tmw_ok) return MOE_ERR_CUDA;
-    if (!encode_2d(&tmA, a, FP8, (uint64_t)args.k_dim, (uint64_t)args.rows, kBoxRows))
+    if (!encode_2d(&tmA, a, FP8, (uint64_t)args.k_dim, (uint64_t)args.rows, Sh::kABox))
         return MOE_ERR_CUDA;
     const int64_t tiles_bound =
         (int64_t)(args.n_out / kBM / (SW ? 2 : 1)) * (args.groups + ceil_div(args.rows, BN));
