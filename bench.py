@@ -147,7 +147,7 @@ class Stepper:
     """The hot path as its C-ABI steps on one stream, CUDA events around each."""
 
     NAMES_FUSED = ["route", "quant_x", "permute", "expert_ffn", "combine"]
-    NAMES_SPLIT = ["route", "quant_x", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
+    NAMES_WIDE = ["route", "quant_x", "permute", "gemm_gate_up", "silu_mul", "gemm_down", "combine"]
 
     def __init__(self, layer, x, out):
         import torch
@@ -166,14 +166,14 @@ class Stepper:
         rows = s.tokens * (s.top_k + s.num_shared)
         self.wide = self.fp8 and rows >= 16 * s.groups   # as moe_layer_forward decides
         self.fused = not self.wide   # as moe_layer_forward decides
-        self.NAMES = self.NAMES_FUSED if self.fused else self.NAMES_SPLIT
+        self.NAMES = self.NAMES_FUSED if self.fused else self.NAMES_WIDE
         self.sched_bytes = moe.expert_ffn_sched_bytes(s.groups, rows)
         ws[L.status:L.status + 4].zero_()   # the device status word starts clear
         self.k = {}
         self.events = []
         self.top_events = []
 
-    TOP = 3   # stage index of the dominant kernel (expert FFN, or the gate/up GEMM)
+    TOP = 3   # stage index of the dominant kernel (expert FFN, or the gate/up GEMM alone)
 
     def step(self, record=None):
         """One pass of the layer.  record="all": CUDA events between all stages
@@ -218,17 +218,13 @@ class Stepper:
             mark()
             self._keep_events(record, ev)
             return
-        if self.wide:   # the layer's two-kernel path for wide batches
-            moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"], p["expert_offsets"],
-                             w["w13"], w.get("w13_s"), p["gate_up"], moe.OUT_F32, p["status"],
-                             w_layout=wl)
-            moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, p["gate_up"], p["h"], p["h_scales"],
-                            rows_dev=p["expert_offsets"] + 4 * G)
-        else:
-            moe.grouped_gemm_swiglu(cfg, G, I, H, rows, p["xp"],
-                                    p["xp_scales"] if self.fp8 else None, p["expert_offsets"],
-                                    w["w13"], w.get("w13_s"), p["h"],
-                                    p["h_scales"] if self.fp8 else None, p["status"], w_layout=wl)
+        # wide FP8 batches: the layer's gate/up GEMM, SiLU-mul and down GEMM
+        moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"], p["expert_offsets"],
+                         w["w13"], w.get("w13_s"), p["gate_up"], moe.OUT_F32, p["status"],
+                         w_layout=wl)
+        mark()
+        moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, p["gate_up"], p["h"], p["h_scales"],
+                        rows_dev=p["expert_offsets"] + 4 * G)
         mark()
         moe.grouped_gemm(cfg, G, H, I, rows, p["h"], p["h_scales"] if self.fp8 else None,
                          p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_F32,
@@ -279,12 +275,13 @@ def path_bytes(shape, offsets):
     b["quant_x"] = (2 * T * H + T * H + T * sc_h) if fp8 else 0
     b["permute"] = 4 * T * k * 3 + rows * (H * eb + sc_h) * 2
     wide = fp8 and rows >= 16 * (E + S)
-    # gate/up with SwiGLU; wide batches also write and re-read fp32 gate/up rows
-    b["gemm_gate_up_swiglu"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i) + \
-        (2 * rows * 2 * I * 4 if wide else 0)
+    if wide:   # gate/up GEMM to fp32 rows, then SiLU-mul + requantisation of h
+        b["gemm_gate_up"] = active * w13 + rows * (H * eb + sc_h) + rows * 2 * I * 4
+        b["silu_mul"] = rows * 2 * I * 4 + rows * (I * eb + sc_i)
     b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4
-    if not wide:   # one kernel holds both GEMMs
-        b["expert_ffn"] = b.pop("gemm_gate_up_swiglu") + b.pop("gemm_down")
+    if not wide:   # one kernel holds both GEMMs (gate/up with SwiGLU, then down)
+        b["expert_ffn"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i) + \
+            b.pop("gemm_down")
     b["combine"] = T * (k + S) * H * 4 + 8 * T * k + T * H * 4
     flops = 2 * T * H * E + 6 * H * I * (T * k + S * T)
     return b, active, flops
@@ -432,9 +429,9 @@ def main():
     hbm_peak, bf16_peak, peak_src = load_peaks()
     layer_bytes = method_bytes(shape, active)      # the method's bytes per step
     path_total = sum(bytes_per.values())           # + this path's wider intermediates
-    top = "expert_ffn" if stepper.fused else "gemm_gate_up_swiglu"
+    top = "expert_ffn" if stepper.fused else "gemm_gate_up"
     top_label = ("expert_ffn (gate/up + SwiGLU + down, one kernel)" if stepper.fused
-                 else "grouped_gemm gate/up + SwiGLU")
+                 else "grouped_gemm gate/up (fp32 rows; SiLU-mul is the next kernel)")
     # algorithmic bytes of the dominant launch: the weights and block scales of
     # every active group it streams (gate/up + down, or gate/up alone)
     w13_b, w2_b = expert_weight_bytes(shape)
@@ -443,11 +440,13 @@ def main():
     achieved = top_bytes / (top_ms / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168 and \
-            not stepper.wide:
+    if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168:
         with open(tpath) as f:
-            tr = json.load(f).get(top)
-        if tr:   # ncu DRAM bytes per active group (small R1 case) x this launch's groups
+            tr = json.load(f).get("grouped_gemm_gate_up_wide" if stepper.wide else top)
+        rows_per_group = T * (shape.top_k + shape.num_shared) / max(1, active)
+        if tr and (not stepper.wide or
+                   abs(rows_per_group / tr["rows_per_active_group"] - 1.0) <= 0.2):
+            # ncu DRAM bytes per active group (small R1 case) x this launch's groups
             traffic = tr["bytes_per_active_group"] * active
 
     e2e = None

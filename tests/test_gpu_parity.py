@@ -577,18 +577,22 @@ def dataclasses_replace(shape, **kw):
     return dataclasses.replace(shape, **kw)
 
 
-@pytest.mark.parametrize("name", ["r1_mini_i512", "bf16_mini", "r1_mini"])
-def test_bench_steps_equal_the_layer_call(lib, name):
-    """bench.py times the layer as C-ABI steps; they compute the layer call's bits."""
+@pytest.mark.parametrize("name,T", [("r1_mini_i512", None), ("bf16_mini", None),
+                                    ("r1_mini", None), ("r1_mini", 130)])
+def test_bench_steps_equal_the_layer_call(lib, name, T):
+    """bench.py times the layer as C-ABI steps; they compute the layer call's bits
+    (130 tokens of r1_mini average 35 rows per group: the wide-batch GEMM path)."""
     import bench
-    wl = workload(name)
+    wl = workload(name, T=T)
     layer = wl.layer()
     s = wl.shape
     ref = torch.full((s.tokens, s.hidden), float("nan"), device="cuda")
     layer.forward(wl.dev["x"], ref)
     out = torch.full_like(ref, float("nan"))
     stepper = bench.Stepper(layer, wl.dev["x"], out)
-    stepper.step()
+    assert stepper.wide == (T is not None)
+    stepper.step(record="all")
     torch.cuda.synchronize()
     assert layer.status() == 0
     assert torch.equal(out, ref)
+    assert set(stepper.kernel_ms()) == set(stepper.NAMES)
