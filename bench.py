@@ -326,6 +326,22 @@ def method_bytes(shape, active):
 
 
 # --------------------------------------------------------------- CPU oracle
+def oracle_single_thread_rate(shape, inp, log2phys, seed=0, n_tokens=None):
+    """Tokens/s of the CPU oracle with its C loops on one thread, on a few
+    tokens of the workload (a few seconds of work); the thread count is
+    restored afterwards."""
+    import oracle
+    n = n_tokens or min(shape.tokens, 4 if shape.hidden >= 7168 else 32)
+    before = oracle.num_threads()
+    oracle.set_num_threads(1)
+    try:
+        rate, dt, _, _ = oracle_sample_rate(shape, inp, log2phys, n, seed=seed, min_seconds=0.0,
+                                            max_passes=1)
+    finally:
+        oracle.set_num_threads(before)
+    return rate, n, dt
+
+
 def oracle_sample_rate(shape, inp, log2phys, n_tokens, seed=0, min_seconds=10.0, max_passes=8):
     """Tokens/s of the CPU oracle on `n_tokens` tokens of the workload,
     repeated until about `min_seconds` of CPU work (at most `max_passes`)."""
@@ -460,6 +476,10 @@ def main():
         cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{passes} pass(es) over {n} of {T} tokens of the same workload "
                          f"(routing + expert FFNs + combine in fp64), {dt:.1f} s"}
+        rate1, n1, dt1 = oracle_single_thread_rate(shape, inp, log2phys, seed=args.seed)
+        cpu["single_thread"] = {"value": rate1, "unit": "tokens/s",
+                                "sample": f"{n1} tokens, the oracle's C loops on one thread, "
+                                          f"{dt1:.1f} s"}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
