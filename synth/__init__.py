@@ -78,6 +78,9 @@ CONFIGS = {
     "r1_zipf_t1024": MoEShape("r1_zipf_t1024", tokens=1024, zipf_s=1.0,
                               balanced_perm=True, **_R1),
     "r1_prefill_t4096": MoEShape("r1_prefill_t4096", tokens=4096, **_R1),
+    # four times the prefill-sized batch: about 576 rows per routed expert,
+    # the regime where the layer's FLOPs start to weigh against its bytes
+    "r1_prefill_t16384": MoEShape("r1_prefill_t16384", tokens=16384, **_R1),
     # R1-shaped layers small enough for the oracle in seconds: several tiles
     # in every dimension and ragged tails (37 tokens, 3 k-blocks in the
     # down projection).
