@@ -32,7 +32,9 @@
 //              gate/up stage holds one 128-byte K block (gate box, up box,
 //              activation rows), a down stage two K blocks (two W2 boxes,
 //              two h boxes; one of each in the last stage when the count
-//              is odd).  Weights are row-major or 128 x 128-byte tiles.
+//              is odd).  Weights are row-major or 128 x 128-byte tiles;
+//              a unit's activation or h rows come as one box per K block
+//              (16 rows, or 32 when more than 16 are valid).
 //   warp 1     MMA issuer: tcgen05.mma (kind::f8f6f4 or kind::f16),
 //              tcgen05.commit to mbarriers; four TMEM accumulators rotate,
 //              FP8 one per K block, BF16 one per unit.
@@ -143,7 +145,9 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
     expert_ffn_kernel(const __grid_constant__ CUtensorMap tmW13,
                       const __grid_constant__ CUtensorMap tmX,
                       const __grid_constant__ CUtensorMap tmW2,
-                      const __grid_constant__ CUtensorMap tmH, const FfnArgs args) {
+                      const __grid_constant__ CUtensorMap tmH,
+                      const __grid_constant__ CUtensorMap tmX32,
+                      const __grid_constant__ CUtensorMap tmH32, const FfnArgs args) {
     extern __shared__ uint8_t dsmem[];
     __shared__ __align__(8) uint64_t full_bar[kStages];
     __shared__ __align__(8) uint64_t empty_bar[kStages];
@@ -208,6 +212,8 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
         tma_prefetch_desc(&tmX);
         tma_prefetch_desc(&tmW2);
         tma_prefetch_desc(&tmH);
+        tma_prefetch_desc(&tmX32);
+        tma_prefetch_desc(&tmH32);
     }
     pdl_wait();   // the set-up above overlaps the previous kernel's tail
     for (int i = threadIdx.x; i <= G; i += (int)blockDim.x) s_off[i] = args.offsets[i];
@@ -286,7 +292,12 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                     }
                     fence_proxy_async_global();
                 }
-                const int nbox = (u.nvalid + kBoxRows - 1) / kBoxRows;
+                // the unit's activation (or h) rows as one TMA box per K block:
+                // 16 rows, or all 32 when more than 16 are valid
+                const bool box32 = u.nvalid > kBoxRows;
+                const uint32_t abytes = (box32 ? kBN : kBoxRows) * 128;
+                const CUtensorMap *tmA = box32 ? &tmX32 : &tmX;
+                const CUtensorMap *tmHb = box32 ? &tmH32 : &tmH;
                 const int nsteps = u.down ? (KB2 + 1) / 2 : KB1;
                 const uint64_t pol_w =
                     (s_off[u.g + 1] - s_off[u.g] > kBN) ? pol_w_shared : pol_w_once;
@@ -309,8 +320,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                     // a down stage holds K blocks 2ks and (if it exists) 2ks + 1
                     const bool two = 2 * ks + 1 < KB2;
                     const uint32_t bytes =
-                        u.down ? (two ? 2u : 1u) * (kABytes + nbox * kBoxRows * 128)
-                               : 2 * kABytes + nbox * kBoxRows * 128;
+                        u.down ? (two ? 2u : 1u) * (kABytes + abytes) : 2 * kABytes + abytes;
                     mbar_arrive_expect_tx(fb, bytes);
                     if (!u.down) {
                         if (tiled) {
@@ -320,9 +330,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                             tma_load_2d(sa, &tmW13, ks * kKE, wrow, fb, pol_w);            // gate
                             tma_load_2d(sa + kABytes, &tmW13, ks * kKE, wrow + I, fb, pol_w);   // up
                         }
-                        for (int b = 0; b < nbox; ++b)
-                            tma_load_2d(sb + b * kBoxRows * 128, &tmX, ks * kKE,
-                                        u.row0 + b * kBoxRows, fb, pol_a);
+                        tma_load_2d(sb, tmA, ks * kKE, u.row0, fb, pol_a);
                     } else {
 #pragma unroll
                         for (int hk = 0; hk < 2; ++hk) {
@@ -333,9 +341,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                                             (tb_down + 2 * ks + hk) * kBM, fb, pol_w);
                             else
                                 tma_load_2d(sa + hk * kABytes, &tmW2, k0, wrow, fb, pol_w);
-                            for (int b = 0; b < nbox; ++b)
-                                tma_load_2d(sb + hk * kBBytes + b * kBoxRows * 128, &tmH, k0,
-                                            u.row0 + b * kBoxRows, fb, pol_a);
+                            tma_load_2d(sb + hk * kBBytes, tmHb, k0, u.row0, fb, pol_a);
                         }
                     }
                     issued |= 1u << stage;
@@ -738,7 +744,7 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
     });
     if (attr_rc[dev]) return MOE_ERR_CUDA;
     constexpr int kKE = FP8 ? 128 : 64;
-    CUtensorMap tmW13, tmX, tmW2, tmH;
+    CUtensorMap tmW13, tmX, tmW2, tmH, tmX32, tmH32;
     const uint64_t w13_rows = (uint64_t)groups * 2 * inter, w2_rows = (uint64_t)groups * hidden;
     const bool w_ok =
         w_tiled ? encode_2d(&tmW13, w13, FP8, kKE, w13_rows * (hidden / kKE), kBM) &&
@@ -747,7 +753,9 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
                       encode_2d(&tmW2, w2, FP8, (uint64_t)inter, w2_rows, kBM);
     if (!w_ok ||
         !encode_2d(&tmX, xp, FP8, (uint64_t)hidden, (uint64_t)rows, kBoxRows) ||
-        !encode_2d(&tmH, h, FP8, (uint64_t)inter, (uint64_t)rows, kBoxRows))
+        !encode_2d(&tmH, h, FP8, (uint64_t)inter, (uint64_t)rows, kBoxRows) ||
+        !encode_2d(&tmX32, xp, FP8, (uint64_t)hidden, (uint64_t)rows, kBN) ||
+        !encode_2d(&tmH32, h, FP8, (uint64_t)inter, (uint64_t)rows, kBN))
         return MOE_ERR_CUDA;
     if (!sched_zeroed) MOE_CUDA_TRY(cudaMemsetAsync(sched, 0, ffn_sched_bytes(groups, rows), s));
     FfnArgs a;
@@ -769,7 +777,7 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
         (int64_t)(inter / kBM + hidden / kBM) * (groups + ceil_div(rows, kBN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, units_bound);
     if (launch_dependent(expert_ffn_kernel<FP8, kEW>, dim3(grid), dim3(64 + 128 * kEW), kSmemBytes, s, tmW13,
-                         tmX, tmW2, tmH, a))
+                         tmX, tmW2, tmH, tmX32, tmH32, a))
         return MOE_ERR_CUDA;
     MOE_LAUNCH_CHECK();
     return MOE_OK;
