@@ -5,19 +5,24 @@
 
 A step is one pass of the whole hot path over one batch: routing, FP8
 quantisation of x, dispatch permutation, the expert FFN (one persistent
-kernel for decode batches and BF16 layers; gate/up GEMM, SiLU-mul +
-requantisation and down GEMM for wide FP8 batches), combine.  Inputs are seeded synthetic
+kernel for decode batches and BF16 layers; for wide FP8 batches the gate/up
+GEMM with its SwiGLU + requantisation epilogue, then the down GEMM), combine.  Inputs are seeded synthetic
 tensors of the workload's shape, resident in HBM before timing starts; the
 11 GB of expert weights streamed per step are far larger than L2, so no L2
 flush is needed between steps.
 
 Prints one JSON line (rank 0).  `value` is tokens/s over all ranks;
 `layer_roofline_frac` divides the bytes the layer must move by its definition
-by the measured HBM copy bandwidth; `roofline` describes the dominant kernel
-(the one-kernel expert FFN at decode, the gate/up GEMM for wide batches) by
-the weight bytes it streams; `e2e` is the same metric through the layer's
-public call with pinned host buffers copied in and out each step;
-`cpu_baseline` times the CPU oracle on a bounded sample of the workload.
+by the measured HBM copy bandwidth (`layer_roofline_frac_nominal`: by the
+nominal 8 TB/s, which a read-dominated stream cannot exceed); `roofline`
+describes the dominant kernel (the one-kernel expert FFN at decode, the
+gate/up GEMM for wide batches) by the weight bytes it streams; `e2e` is the
+same metric through the layer's public call with pinned host buffers copied
+in and out each step; `cpu_baseline` times the CPU oracle on a bounded
+sample of the workload.  On the default workload the line also carries
+`workloads`: the same measurements (no CPU baseline) of the 1024-token
+Zipf-skewed layer behind its balanced permutation and of the 4096-token
+layer, timed in the same process one layer at a time.
 --impl reference times the CPU oracle itself as the reference arm.
 Several GPUs run independent replicas (the layer has no exchange step on one
 node here): the timing is the max over ranks.
@@ -40,6 +45,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s at R1 shape (bs 128/1024); HBM GB/s and % of roofline"
 DEFAULT_WORKLOAD = "r1_decode_t128"
+EXTRA_WORKLOADS = ("r1_zipf_t1024", "r1_prefill_t4096")
+NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, about 8 TB/s
 
 
 def load_peaks():
@@ -147,7 +154,7 @@ class Stepper:
     """The hot path as its C-ABI steps on one stream, CUDA events around each."""
 
     NAMES_FUSED = ["route", "quant_x", "permute", "expert_ffn", "combine"]
-    NAMES_WIDE = ["route", "quant_x", "permute", "gemm_gate_up", "silu_mul", "gemm_down", "combine"]
+    NAMES_WIDE = ["route", "quant_x", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
 
     def __init__(self, layer, x, out):
         import torch
@@ -160,8 +167,8 @@ class Stepper:
         base = ws.data_ptr()
         self.p = {n: base + getattr(L, n) for n in
                   ("status", "logits", "topk_ids", "topk_w", "xq", "xs", "expert_offsets",
-                   "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "gate_up",
-                   "h", "h_scales", "y", "ffn_sched")}
+                   "src_of_row", "row_of_slot", "perm_scratch", "xp", "xp_scales", "h",
+                   "h_scales", "y", "ffn_sched")}
         self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
         rows = s.tokens * (s.top_k + s.num_shared)
         self.wide = self.fp8 and rows >= 16 * s.groups   # as moe_layer_forward decides
@@ -218,13 +225,11 @@ class Stepper:
             mark()
             self._keep_events(record, ev)
             return
-        # wide FP8 batches: the layer's gate/up GEMM, SiLU-mul and down GEMM
-        moe.grouped_gemm(cfg, G, 2 * I, H, rows, p["xp"], p["xp_scales"], p["expert_offsets"],
-                         w["w13"], w.get("w13_s"), p["gate_up"], moe.OUT_F32, p["status"],
-                         w_layout=wl)
-        mark()
-        moe.act_requant(cfg, moe.ACT_SILU_MUL, rows, p["gate_up"], p["h"], p["h_scales"],
-                        rows_dev=p["expert_offsets"] + 4 * G)
+        # wide FP8 batches: the layer's gate/up GEMM with the SwiGLU epilogue,
+        # then the down GEMM
+        moe.grouped_gemm_swiglu(cfg, G, I, H, rows, p["xp"], p["xp_scales"],
+                                p["expert_offsets"], w["w13"], w.get("w13_s"), p["h"],
+                                p["h_scales"], p["status"], w_layout=wl)
         mark()
         moe.grouped_gemm(cfg, G, H, I, rows, p["h"], p["h_scales"] if self.fp8 else None,
                          p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_F32,
@@ -258,8 +263,8 @@ class Stepper:
 
 def path_bytes(shape, offsets):
     """Bytes this path moves, per stage, given the rows per group: the method's
-    bytes plus the intermediates it keeps at higher precision (fp32 Y; the wide
-    path's fp32 gate/up rows).  Used for the per-stage split only."""
+    bytes plus the intermediate it keeps at higher precision (fp32 Y).  Used
+    for the per-stage split only."""
     T, H, I, E, S, k = (shape.tokens, shape.hidden, shape.inter, shape.num_experts,
                         shape.num_shared, shape.top_k)
     fp8 = shape.dtype == "fp8"
@@ -275,9 +280,8 @@ def path_bytes(shape, offsets):
     b["quant_x"] = (2 * T * H + T * H + T * sc_h) if fp8 else 0
     b["permute"] = 4 * T * k * 3 + rows * (H * eb + sc_h) * 2
     wide = fp8 and rows >= 16 * (E + S)
-    if wide:   # gate/up GEMM to fp32 rows, then SiLU-mul + requantisation of h
-        b["gemm_gate_up"] = active * w13 + rows * (H * eb + sc_h) + rows * 2 * I * 4
-        b["silu_mul"] = rows * 2 * I * 4 + rows * (I * eb + sc_i)
+    if wide:   # gate/up GEMM with the SwiGLU + requantisation epilogue
+        b["gemm_gate_up_swiglu"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i)
     b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4
     if not wide:   # one kernel holds both GEMMs (gate/up with SwiGLU, then down)
         b["expert_ffn"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i) + \
@@ -304,8 +308,8 @@ def method_bytes(shape, active):
     weights, x read, its FP8 codes (and row scales) written and read, the
     dispatched rows written and read, h written and read, the expert outputs Y
     as bf16 written and read, and the bf16 output.  This path's wider
-    intermediates (fp32 Y, fp32 gate/up rows of wide batches) are not counted,
-    so the layer's roofline fraction is not flattered by them."""
+    intermediate (fp32 Y) is not counted, so the layer's roofline fraction is
+    not flattered by it."""
     T, H, I, E, S, k = (shape.tokens, shape.hidden, shape.inter, shape.num_experts,
                         shape.num_shared, shape.top_k)
     fp8 = shape.dtype == "fp8"
@@ -376,6 +380,8 @@ def main():
                     help="tokens of the CPU-oracle sample (default: sized to ~10-30 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the 1024- and 4096-token layers measured after the default one")
     args = ap.parse_args()
 
     import torch
@@ -404,6 +410,30 @@ def main():
         dist.barrier()
     import moe_expert_layer_07_gb300 as moe
 
+    line = {"metric": METRIC}
+    head = measure(shape, args, world, rank, local, device,
+                   cpu=not args.no_cpu_baseline and rank == 0)
+    line.update(head)
+    if args.workload == DEFAULT_WORKLOAD and not args.no_workloads:
+        line["workloads"] = {}
+        for name in EXTRA_WORKLOADS:
+            m = measure(synth.CONFIGS[name], args, world, rank, local, device, cpu=False)
+            for k in ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling",
+                      "vs_baseline", "data", "cpu_baseline"):
+                m.pop(k, None)
+            line["workloads"][name] = m
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def measure(shape, args, world, rank, local, device, cpu):
+    """All measurements of one workload (the layer resident only meanwhile)."""
+    import torch
+    import moe_expert_layer_07_gb300 as moe
+
     inp, layer, log2phys, perm_info = setup(shape, replica_seed(args.seed, rank), device)
     T, H = shape.tokens, shape.hidden
     x = inp["x"]
@@ -413,10 +443,11 @@ def main():
         stepper.step()
     torch.cuda.synchronize()
     if layer.status() != 0:
-        raise RuntimeError(f"device status {layer.status()} after warm-up")
+        raise RuntimeError(f"device status {layer.status()} after warm-up ({shape.name})")
 
     def barrier():
         if world > 1:
+            import torch.distributed as dist
             dist.barrier()
 
     with ClockSampler(local) as clocks:
@@ -445,9 +476,8 @@ def main():
     hbm_peak, bf16_peak, peak_src = load_peaks()
     layer_bytes = method_bytes(shape, active)      # the method's bytes per step
     path_total = sum(bytes_per.values())           # + this path's wider intermediates
-    top = "expert_ffn" if stepper.fused else "gemm_gate_up"
     top_label = ("expert_ffn (gate/up + SwiGLU + down, one kernel)" if stepper.fused
-                 else "grouped_gemm gate/up (fp32 rows; SiLU-mul is the next kernel)")
+                 else "swiglu_wide gate/up GEMM (SwiGLU + FP8 requantisation epilogue)")
     # algorithmic bytes of the dominant launch: the weights and block scales of
     # every active group it streams (gate/up + down, or gate/up alone)
     w13_b, w2_b = expert_weight_bytes(shape)
@@ -458,7 +488,7 @@ def main():
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168:
         with open(tpath) as f:
-            tr = json.load(f).get("grouped_gemm_gate_up_wide" if stepper.wide else top)
+            tr = json.load(f).get("swiglu_wide" if stepper.wide else "expert_ffn")
         rows_per_group = T * (shape.top_k + shape.num_shared) / max(1, active)
         if tr and (not stepper.wide or
                    abs(rows_per_group / tr["rows_per_active_group"] - 1.0) <= 0.2):
@@ -469,26 +499,31 @@ def main():
     if not args.no_e2e:
         e2e = end_to_end(layer, shape, x, device, args.steps, args.warmup, world)
 
-    cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    cpu_line = None
+    if cpu:
         n = args.cpu_tokens or default_cpu_tokens(shape)
         rate, dt, cores, passes = oracle_sample_rate(shape, inp, log2phys, n, seed=args.seed)
-        cpu = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{passes} pass(es) over {n} of {T} tokens of the same workload "
-                         f"(routing + expert FFNs + combine in fp64), {dt:.1f} s"}
+        cpu_line = {"value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                    "sample": f"{passes} pass(es) over {n} of {T} tokens of the same workload "
+                              f"(routing + expert FFNs + combine in fp64), {dt:.1f} s"}
         rate1, n1, dt1 = oracle_single_thread_rate(shape, inp, log2phys, seed=args.seed)
-        cpu["single_thread"] = {"value": rate1, "unit": "tokens/s",
-                                "sample": f"{n1} tokens, the oracle's C loops on one thread, "
-                                          f"{dt1:.1f} s"}
+        cpu_line["single_thread"] = {"value": rate1, "unit": "tokens/s",
+                                     "sample": f"{n1} tokens, the oracle's C loops on one "
+                                               f"thread, {dt1:.1f} s"}
 
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    result = {
+        "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8e4m3" if shape.dtype == "fp8" else "bf16", "data": "synthetic",
         "config": {**workload_config(shape, world), **perm_info},
         "hbm_gbs": layer_bytes / (ms_step / 1e3) / 1e9,
         "layer_roofline_frac": (layer_bytes / (hbm_peak * 1e9)) / (ms_step / 1e3),
+        "layer_roofline_frac_nominal": (layer_bytes / (NOMINAL_HBM_GBS * 1e9)) / (ms_step / 1e3),
+        "roofline_note": "headline fractions (`layer_roofline_frac`, `roofline.frac`) are of "
+                         "the measured copy bandwidth (a read + write figure, which a "
+                         "read-dominated weight stream can exceed); the `_nominal` fractions "
+                         "are of the nominal 8 TB/s and stay below 1",
         "layer_bytes": layer_bytes,
         "path_bytes": path_total,
         "path_hbm_gbs": path_total / (ms_step / 1e3) / 1e9,
@@ -500,6 +535,8 @@ def main():
         "roofline": {"bound": "hbm", "kernel": top_label, "achieved": achieved,
                      "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
                      "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                     "peak_nominal": NOMINAL_HBM_GBS,
                      "bytes_per_unit": unit_bytes, "units": active,
                      "work_unit": "active expert group (weights + block scales)",
                      "ms_per_launch": top_ms},
@@ -508,13 +545,12 @@ def main():
         "device_status": status,
         "clocks": clocks.summary(),
         "e2e": e2e,
-        "cpu_baseline": cpu,
+        "cpu_baseline": cpu_line,
     }
-    if rank == 0:
-        print(json.dumps(line))
-    if world > 1:
-        dist.destroy_process_group()
-    return 0
+    del stepper, layer, inp, x, out
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return result
 
 
 def workload_config(shape, world):
@@ -617,18 +653,10 @@ def reference_arm(args, shape):
     oracle.build()
     device = "cuda" if torch.cuda.is_available() else "cpu"
     inp = synth.make_inputs(shape, seed=args.seed, device=device)
+    # no expert permutation: the oracle's layer is the same, bit for bit, with
+    # or without one (routing is defined on logical experts), so the reference
+    # arm runs the oracle alone on the workload's un-permuted weights
     log2phys = None
-    if shape.balanced_perm:
-        from oracle import routing as orouting
-        def bits(t):
-            return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-        bias = None if inp["e_bias"] is None else inp["e_bias"].cpu().numpy()
-        off = None if inp["logit_offset"] is None else inp["logit_offset"].cpu().numpy()
-        l = orouting.gate_logits(bits(inp["x"]), bits(inp["wg"]), off)
-        _, _, logical = orouting.route(l, shape, bias)
-        counts = np.bincount(logical.reshape(-1), minlength=shape.num_experts)
-        log2phys, p2l = balanced_perm_host(counts, shape.num_sets)
-        inp = synth.relayout_experts(inp, shape, p2l)
     npin = synth.to_numpy(inp, log2phys)
     per_step = max(1, min(shape.tokens, 2 if shape.hidden >= 7168 else shape.tokens // 4))
     rng = np.random.default_rng(args.seed)
@@ -657,14 +685,6 @@ def reference_arm(args, shape):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
-
-
-def balanced_perm_host(counts, num_sets):
-    import moe_expert_layer_07_gb300 as moe
-    from moe_expert_layer_07_gb300 import _build
-    _build.build()
-    l2p, p2l, _ = moe.balance_permutation(counts, num_sets)
-    return l2p, p2l
 
 
 if __name__ == "__main__":

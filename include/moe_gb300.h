@@ -185,7 +185,11 @@ MOE_API int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_id
  *     shape (256 experts, top 8) that is above 21824 tokens.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is looked up again when the
+ *     device's CUDA context has changed since (after a device reset the
+ *     module holding the array is reloaded elsewhere), so the call stays
+ *     valid across resets; the first call after a reset should again come
+ *     before any capture.
  *   - Every call on a device shares the one array and leaves its contents
  *     behind; nothing in it needs to start at zero (a call reads only words
  *     it wrote earlier).  Calls that overlap on the GPU (other streams, or
@@ -233,8 +237,11 @@ MOE_API int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_ou
  * moe_act_requant(SILU_MUL), without writing the fp32 gate/up rows.  A tile
  * takes 128 gate rows and the matching 128 up rows, which share one
  * activation tile (the report's "horizontal fusion" of an expert's GEMMs,
- * section "Library optimisation").  inter multiple of 128; K as in
- * moe_grouped_gemm. */
+ * section "Library optimisation").  FP8 groups averaging 16 rows or more
+ * (rows >= 16 * groups) take a second kernel with the orientation swapped:
+ * 128 token rows of one expert on the MMA's M side against those 256 weight
+ * rows on N, so each thread promotes, applies SwiGLU to and quantises one
+ * token row; same bits.  inter multiple of 128; K as in moe_grouped_gemm. */
 MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter,
                                     int32_t k_dim, int32_t rows, const void *a,
                                     const float *a_scales, const int32_t *expert_offsets,
@@ -274,6 +281,23 @@ MOE_API int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, 
                            float *h_scales, float *y, int32_t *sched, size_t sched_bytes,
                            int32_t *dev_status, void *stream);
 
+/* The experts' FFN on dispatched rows with the kernels moe_layer_forward
+ * would pick for this batch: moe_expert_ffn for BF16 layers and for FP8
+ * groups averaging fewer than 16 rows (rows < 16 * groups), otherwise
+ * moe_grouped_gemm_swiglu followed by moe_grouped_gemm (down, fp32 y).
+ * Arguments, layouts, ownership and errors as moe_expert_ffn (sched is
+ * cleared on `stream` and used only by the one-kernel path); every choice
+ * gives the same result bits.  Used by the expert-parallel step, where the
+ * rows a rank receives for its experts, and its shared-expert rows, are FFN
+ * calls of their own. */
+MOE_API int moe_experts_forward(const moe_config *cfg, int32_t groups, int32_t rows,
+                                const void *a, const float *a_scales,
+                                const int32_t *expert_offsets, const void *w13,
+                                const float *w13_scales, const void *w2,
+                                const float *w2_scales, int32_t w_layout, void *h,
+                                float *h_scales, float *y, int32_t *sched, size_t sched_bytes,
+                                int32_t *dev_status, void *stream);
+
 /* Packs an expert weight tensor W [groups, n_out, k_dim] (e4m3 for FP8
  * layers, bf16 otherwise, per cfg->dtype) from MOE_LAYOUT_ROWS into
  * MOE_LAYOUT_TILES (w_tiled, same size, device, caller-owned, must not
@@ -302,8 +326,8 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
  * on `stream`.  The experts' FFN is
  *   BF16, and FP8 with groups averaging fewer than 16 rows (decode):
  *     moe_expert_ffn (one persistent kernel);
- *   FP8, groups averaging 16 rows or more: grouped GEMM gate/up (64-row
- *     tiles, fp32 rows), SiLU-mul + requantisation, grouped GEMM down;
+ *   FP8, groups averaging 16 rows or more: moe_grouped_gemm_swiglu (its
+ *     token-rows-on-M kernel) then moe_grouped_gemm down (64-row tiles);
  * all with the same result bits (fp32 expert outputs), and
  * all intermediates inside `ws` (size from moe_workspace_size for
  * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..
@@ -315,7 +339,9 @@ MOE_API int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32
                       void *out, int32_t out_dtype, void *ws, size_t ws_bytes, void *stream);
 
 /* Byte offsets of the intermediates inside the layer workspace (host), for
- * callers that want to read routing results or rows per expert. */
+ * callers that want to read routing results or rows per expert.  gate_up is
+ * an empty region (no layer path keeps fp32 gate/up rows); it stays for
+ * layout compatibility. */
 typedef struct moe_ws_layout {
     size_t status, logits, topk_ids, topk_w, xq, xs, expert_offsets, src_of_row,
         row_of_slot, perm_scratch, xp, xp_scales, gate_up, h, h_scales, y, ffn_sched, total;
@@ -329,6 +355,13 @@ MOE_API int moe_get_device_status(const void *ws, int32_t *status /* host */);
 
 /* Static text for a MOE_OK / MOE_ERR_* code. */
 MOE_API const char *moe_status_string(int32_t code);
+
+/* What the last call on this host thread that returned MOE_ERR_CUDA failed
+ * at: the CUDA runtime or driver call and its error text (e.g.
+ * "cudaLaunchKernelEx: too many resources requested for launch").  Empty
+ * until such a failure; a later successful call does not clear it.  The
+ * pointer stays valid for the thread's lifetime. */
+MOE_API const char *moe_last_error_detail(void);
 
 /* Number of kernels moe_layer_forward enqueues for this configuration. */
 MOE_API int moe_layer_kernel_count(const moe_config *cfg, int32_t T);
@@ -403,6 +436,20 @@ MOE_API int moe_relayout_experts(const void *src, void *dst, const int32_t *src_
  * Pure host code; usable without a GPU. */
 MOE_API int expert_balance_permutation(const int64_t *counts, int32_t num_experts, int32_t num_sets,
                                int32_t *log2phys, int32_t *phys2log, double *max_over_mean);
+
+/* Host: the set imbalance of a given permutation (the figure the report,
+ * section "Load balancing across GPUs", quotes: the busiest set against the
+ * average).  Set s holds physical ids [s*m, (s+1)*m), m = E/num_sets; the
+ * load of a set is the sum of counts[e] over the logical experts e with
+ * log2phys[e] in it.
+ *   counts    host int64 [E], >= 0
+ *   log2phys  host int32 [E], a permutation of 0..E-1 (NULL = identity)
+ *   max_over_mean host, written: largest set load / mean set load (1 when
+ *             every count is 0)
+ * MOE_ERR_INVALID_ARG for a negative count, an id out of range or repeated,
+ * or E not a multiple of num_sets.  Pure host code; usable without a GPU. */
+MOE_API int expert_set_imbalance(const int64_t *counts, const int32_t *log2phys,
+                                 int32_t num_experts, int32_t num_sets, double *max_over_mean);
 
 /* Host: affinity-aware placement (SGLang/H20 article, section "Expert
  * Affinity EPLB").  From per-expert counts and the symmetric co-activation

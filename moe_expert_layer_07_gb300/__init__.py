@@ -16,10 +16,11 @@ from ._build import LIB as LIB_PATH
 __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_requant",
            "permute", "permute_workspace_size", "permute_static_scratch", "grouped_gemm", "combine", "layer_forward",
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
-           "balance_permutation", "layer_kernel_count", "MoELayer", "MoEError",
+           "last_error_detail",
+           "balance_permutation", "set_imbalance", "layer_kernel_count", "MoELayer", "MoEError",
            "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
            "count_coactivation", "affinity_permutation", "grouped_gemm_swiglu",
-           "expert_ffn", "expert_ffn_sched_bytes", "pack_expert_weights", "LAYOUT_ROWS",
+           "expert_ffn", "experts_forward", "expert_ffn_sched_bytes", "pack_expert_weights", "LAYOUT_ROWS",
            "LAYOUT_TILES",
            "SOFTMAX", "SIGMOID", "BF16", "FP8", "OUT_F32", "OUT_BF16", "ACT_IDENTITY",
            "ACT_SILU_MUL"]
@@ -34,7 +35,10 @@ LAYOUT_ROWS, LAYOUT_TILES = 0, 1
 
 class MoEError(RuntimeError):
     def __init__(self, code: int, where: str):
-        super().__init__(f"{where}: {status_string(code)} ({code})")
+        msg = f"{where}: {status_string(code)} ({code})"
+        if code == -4:   # MOE_ERR_CUDA: add what the library saw fail
+            msg += f" [{last_error_detail()}]"
+        super().__init__(msg)
         self.code = code
 
 
@@ -76,6 +80,7 @@ _SIGS = {
     "moe_get_device_status": [_P, ctypes.POINTER(ctypes.c_int32)],
     "moe_layer_kernel_count": [_CP, _I],
     "expert_balance_permutation": [_P, _I, _I, _P, _P, ctypes.POINTER(ctypes.c_double)],
+    "expert_set_imbalance": [_P, _P, _I, _I, ctypes.POINTER(ctypes.c_double)],
     "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
     "moe_permute_static_scratch": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_count_expert_rows": [_CP, _P, _P, _P],
@@ -88,6 +93,8 @@ _SIGS = {
     "moe_selftest_ffn_flag_timeout": [_P, ctypes.c_size_t, _P, _P],
     "moe_expert_ffn": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
                        ctypes.c_size_t, _P, _P],
+    "moe_experts_forward": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
+                            ctypes.c_size_t, _P, _P],
 }
 
 
@@ -111,12 +118,19 @@ def lib():
         L.moe_selftest_ffn_flag_timeout_scratch_bytes.restype = ctypes.c_size_t
         L.moe_status_string.argtypes = [ctypes.c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_last_error_detail.argtypes = []
+        L.moe_last_error_detail.restype = ctypes.c_char_p
         _lib = L
     return _lib
 
 
 def status_string(code: int) -> str:
     return lib().moe_status_string(int(code)).decode()
+
+
+def last_error_detail() -> str:
+    """What the last MOE_ERR_CUDA on this thread failed at."""
+    return lib().moe_last_error_detail().decode()
 
 
 def _check(rc: int, where: str):
@@ -237,6 +251,17 @@ def expert_ffn(cfg: Config, groups, rows, a, a_scales, expert_offsets, w13, w13_
                                 _ptr(status), _stream(stream)), "moe_expert_ffn")
 
 
+def experts_forward(cfg: Config, groups, rows, a, a_scales, expert_offsets, w13, w13_scales, w2,
+                    w2_scales, h, h_scales, y, sched, sched_bytes, status=None, stream=None,
+                    w_layout=None):
+    """The experts' FFN with the kernels the layer would pick for this batch."""
+    _check(lib().moe_experts_forward(ctypes.byref(cfg), groups, rows, _ptr(a), _ptr(a_scales),
+                                     _ptr(expert_offsets), _ptr(w13), _ptr(w13_scales), _ptr(w2),
+                                     _ptr(w2_scales), LAYOUT_ROWS if w_layout is None else w_layout,
+                                     _ptr(h), _ptr(h_scales), _ptr(y), _ptr(sched), sched_bytes,
+                                     _ptr(status), _stream(stream)), "moe_experts_forward")
+
+
 def combine(cfg: Config, T, y, row_of_slot, topk_w, expert_offsets, out, out_dtype, stream=None):
     _check(lib().moe_combine(ctypes.byref(cfg), T, _ptr(y), _ptr(row_of_slot), _ptr(topk_w),
                              _ptr(expert_offsets), _ptr(out), out_dtype, _stream(stream)),
@@ -326,6 +351,17 @@ def balance_permutation(counts, num_sets: int):
                                             p2l.ctypes.data, ctypes.byref(mom)),
            "expert_balance_permutation")
     return l2p, p2l, mom.value
+
+
+def set_imbalance(counts, log2phys, num_sets: int) -> float:
+    """Host call: largest set load / mean set load of a permutation."""
+    import numpy as np
+    c = np.ascontiguousarray(counts, dtype=np.int64)
+    l2p = None if log2phys is None else np.ascontiguousarray(log2phys, dtype=np.int32)
+    v = ctypes.c_double()
+    _check(lib().expert_set_imbalance(c.ctypes.data, None if l2p is None else l2p.ctypes.data,
+                                      len(c), num_sets, ctypes.byref(v)), "expert_set_imbalance")
+    return v.value
 
 
 class MoELayer:
@@ -456,11 +492,7 @@ class ExpertRebalancer:
         import torch
         lay, s = self.layer, self.layer.shape
         c = self.logical_counts() if counts is None else np.asarray(counts, np.int64)
-        m = s.num_experts // self.num_sets
-        loads = np.zeros(self.num_sets, np.int64)
-        for e in range(s.num_experts):
-            loads[self.log2phys[e] // m] += c[e]
-        before = float(loads.max() / loads.mean()) if loads.sum() else 1.0
+        before = set_imbalance(c, self.log2phys, self.num_sets)
         if self.coact is not None:
             new_l2p, new_p2l, after, self.last_intra_fraction = affinity_permutation(
                 c, self.coact.cpu().numpy(), self.num_sets, self.affinity_slack)

@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "route.cu", "quant.cu", "permute.cu", "gemm.cu", "combine.cu",
+SOURCES = ["api.cu", "route.cu", "quant.cu", "permute.cu", "gemm.cu", "gemm_wide.cu", "combine.cu",
            "selftest.cu", "permute_static.cu", "rebalance.cu", "ffn.cu", "pack.cu",
            "balance.cpp"]
 

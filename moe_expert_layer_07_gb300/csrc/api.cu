@@ -3,11 +3,22 @@
 // never synchronises the host (except moe_get_device_status, which exists to).
 #include <cuda_runtime.h>
 
+#include <cstdio>
 #include <mutex>
 
 #include "internal.h"
 
 namespace moe {
+
+namespace {
+thread_local char g_error_detail[256] = "";
+}
+
+int cuda_fail(const char *where, cudaError_t e) {
+    std::snprintf(g_error_detail, sizeof g_error_detail, "%s: %s", where,
+                  e == cudaSuccess ? "failed" : cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+}
 
 int check_config(const moe_config *c) {
     if (!c) return MOE_ERR_INVALID_ARG;
@@ -58,9 +69,9 @@ bool tiled_fits(int64_t groups, int64_t n_out, int64_t k_dim, bool fp8) {
     return groups * n_out * (k_dim / (fp8 ? 128 : 64)) <= INT32_MAX;
 }
 
-// Groups averaging 16 rows or more: the gate/up GEMM with 64-row tiles and a
-// separate SiLU-mul kernel beats the fused SwiGLU epilogue (whose two fp32
-// accumulators keep it at 32-row tiles); decode batches take the fused path.
+// Groups averaging 16 rows or more: FP8 batches this wide take the two-kernel
+// path (gate/up + SwiGLU with token rows on the MMA's M side, then the down
+// GEMM) instead of the one-kernel FFN.
 bool wide_rows(const moe_config *cfg, int64_t T) {
     return cfg->dtype == MOE_DTYPE_FP8_BLOCK128 &&
            total_rows(cfg, T) >= 16 * (int64_t)groups_of(cfg);
@@ -70,6 +81,26 @@ bool wide_rows(const moe_config *cfg, int64_t T) {
 // decode batches.
 bool fused_ffn(const moe_config *cfg, int64_t T) {
     return cfg->dtype != MOE_DTYPE_FP8_BLOCK128 || !wide_rows(cfg, T);
+}
+
+// The experts' FFN on dispatched rows, whichever kernels suit the batch:
+// the one-kernel FFN for BF16 and for FP8 groups averaging fewer than 16
+// rows, else the gate/up GEMM with its SwiGLU epilogue and the down GEMM.
+// All choices give the same result bits.
+int experts_forward(bool fp8, int groups, int hidden, int inter, int rows, const void *xp,
+                    const float *xp_scales, const int32_t *offsets, const void *w13,
+                    const float *w13_scales, const void *w2, const float *w2_scales,
+                    bool tiled, void *h, float *h_scales, float *y, int32_t *sched,
+                    bool sched_zeroed, int32_t *status, cudaStream_t s) {
+    if (!fp8 || (int64_t)rows < 16 * (int64_t)groups)
+        return launch_expert_ffn(fp8, groups, hidden, inter, rows, xp, xp_scales, offsets, w13,
+                                 w13_scales, w2, w2_scales, tiled, h, h_scales, y, sched,
+                                 sched_zeroed, status, s);
+    int rc = launch_grouped_gemm_swiglu(fp8, groups, inter, hidden, rows, xp, xp_scales, offsets,
+                                        w13, w13_scales, tiled, h, h_scales, status, s);
+    if (rc) return rc;
+    return launch_grouped_gemm(fp8, groups, hidden, inter, rows, h, h_scales, offsets, w2,
+                               w2_scales, tiled, y, MOE_OUT_F32, status, s);
 }
 
 int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
@@ -97,9 +128,8 @@ int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
     L->perm_scratch = take((int64_t)permute_scratch_bytes(cfg, (int)Tm));
     L->xp = take(Rt * H * (fp8 ? 1 : 2));
     L->xp_scales = take(fp8 ? 4 * Rt * (H / 128) : 0);
-    // fp32 gate/up rows exist only for batches wide enough to take the
-    // two-kernel path (see moe_layer_forward)
-    L->gate_up = take(wide_rows(cfg, Tm) ? 4 * Rt * 2 * I : 0);
+    // no layer path keeps fp32 gate/up rows (the field stays for the ABI)
+    L->gate_up = take(0);
     L->h = take(Rt * I * (fp8 ? 1 : 2));
     L->h_scales = take(fp8 ? 4 * Rt * (I / 128) : 0);
     L->y = take(4 * Rt * H);
@@ -270,6 +300,34 @@ int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const vo
                              static_cast<cudaStream_t>(stream));
 }
 
+int moe_experts_forward(const moe_config *cfg, int32_t groups, int32_t rows, const void *a,
+                        const float *a_scales, const int32_t *expert_offsets, const void *w13,
+                        const float *w13_scales, const void *w2, const float *w2_scales,
+                        int32_t w_layout, void *h, float *h_scales, float *y, int32_t *sched,
+                        size_t sched_bytes, int32_t *dev_status, void *stream) {
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (groups <= 0 || rows < 0 || !layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
+    const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
+    if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)groups * 2 * cfg->inter > INT32_MAX || (int64_t)groups * cfg->hidden > INT32_MAX)
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (w_layout == MOE_LAYOUT_TILES &&
+        (!tiled_fits(groups, 2 * (int64_t)cfg->inter, cfg->hidden, fp8) ||
+         !tiled_fits(groups, cfg->hidden, cfg->inter, fp8)))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!a || !expert_offsets || !w13 || !w2 || !h || !y || !sched ||
+        (fp8 && (!a_scales || !w13_scales || !w2_scales || !h_scales)))
+        return MOE_ERR_INVALID_ARG;
+    if (!al16(a) || !al16(w13) || !al16(w2) || !al16(h) || !al16(y)) return MOE_ERR_INVALID_ARG;
+    if (sched_bytes < ffn_sched_bytes(groups, rows)) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    return experts_forward(fp8, groups, cfg->hidden, cfg->inter, rows, a, a_scales,
+                           expert_offsets, w13, w13_scales, w2, w2_scales,
+                           w_layout == MOE_LAYOUT_TILES, h, h_scales, y, sched, false,
+                           dev_status, static_cast<cudaStream_t>(stream));
+}
+
 int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
                 const float *topk_w, const int32_t *expert_offsets, void *out, int32_t out_dtype,
                 void *stream) {
@@ -302,10 +360,9 @@ int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
 int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
     if (check_config(cfg) || T <= 0) return 0;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
-    // route, (quantise x), permute, the experts' FFN (one fused kernel; or
-    // gate/up GEMM with SwiGLU + down GEMM; or, for wide batches, GEMM +
-    // SiLU-mul + down GEMM), combine
-    const int ffn = fused_ffn(cfg, T) ? 1 : (wide_rows(cfg, T) ? 3 : 2);
+    // route, (quantise x), permute, the experts' FFN (one fused kernel, or
+    // gate/up GEMM with SwiGLU + down GEMM), combine
+    const int ffn = fused_ffn(cfg, T) ? 1 : 2;
     return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count(cfg, T) + ffn + 1;
 }
 
@@ -383,43 +440,24 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
                         reinterpret_cast<float *>(base + L.xp_scales), base + L.perm_scratch,
                         status, s);
     if (rc) return rc;
-    if (fused) {
-        rc = launch_expert_ffn(fp8, G, H, I, rows, base + L.xp,
-                               reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
-                               w->w13_scales, w->w2, w->w2_scales, tiled, base + L.h,
-                               reinterpret_cast<float *>(base + L.h_scales),
-                               reinterpret_cast<float *>(base + L.y),
-                               reinterpret_cast<int32_t *>(base + L.ffn_sched), true, status, s);
-        if (rc) return rc;
-        return launch_combine(cfg, T, base + L.y, ros, tw, offsets, out, out_dtype, s);
-    }
-    if (wide_rows(cfg, T)) {
-        rc = launch_grouped_gemm(fp8, G, 2 * I, H, rows, base + L.xp,
-                                 reinterpret_cast<const float *>(base + L.xp_scales), offsets,
-                                 w->w13, w->w13_scales, tiled, base + L.gate_up, MOE_OUT_F32,
-                                 status, s);
-        if (rc) return rc;
-        rc = launch_act_requant(cfg, MOE_ACT_SILU_MUL, rows, offsets + G, base + L.gate_up,
-                                base + L.h, reinterpret_cast<float *>(base + L.h_scales), s);
-    } else {
-        rc = launch_grouped_gemm_swiglu(fp8, G, I, H, rows, base + L.xp,
-                                        reinterpret_cast<const float *>(base + L.xp_scales),
-                                        offsets, w->w13, w->w13_scales, tiled, base + L.h,
-                                        reinterpret_cast<float *>(base + L.h_scales), status, s);
-    }
-    if (rc) return rc;
-    rc = launch_grouped_gemm(fp8, G, H, I, rows, base + L.h,
-                             reinterpret_cast<const float *>(base + L.h_scales), offsets, w->w2,
-                             w->w2_scales, tiled, base + L.y, MOE_OUT_F32, status, s);
+    // the one-kernel FFN's scheduler counters were cleared with the status word
+    rc = experts_forward(fp8, G, H, I, rows, base + L.xp,
+                         reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
+                         w->w13_scales, w->w2, w->w2_scales, tiled, base + L.h,
+                         reinterpret_cast<float *>(base + L.h_scales),
+                         reinterpret_cast<float *>(base + L.y),
+                         reinterpret_cast<int32_t *>(base + L.ffn_sched), true, status, s);
     if (rc) return rc;
     return launch_combine(cfg, T, base + L.y, ros, tw, offsets, out, out_dtype, s);
 }
+
+const char *moe_last_error_detail(void) { return g_error_detail; }
 
 int moe_get_device_status(const void *ws, int32_t *status) {
     if (!ws || !status) return MOE_ERR_INVALID_ARG;
     int32_t v = 0;
     // the status word is the first field of the layer workspace
-    if (cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    MOE_CUDA_TRY(cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost));
     *status = v;
     if (v == 0) return MOE_OK;
     return (v & MOE_DEV_TIMEOUT) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_FAULT;

@@ -246,6 +246,27 @@ struct AffinityExact {
 // co-activation kept inside sets while every set total stays within
 // max(L*, floor((1 + slack) * mean)): exhaustively for E <= 16, otherwise by
 // best-improvement swaps between sets.
+extern "C" int expert_set_imbalance(const int64_t *counts, const int32_t *log2phys,
+                                    int32_t num_experts, int32_t num_sets,
+                                    double *max_over_mean) {
+    if (!counts || !max_over_mean || num_experts <= 0 || num_sets <= 0 ||
+        num_experts % num_sets)
+        return MOE_ERR_INVALID_ARG;
+    const int E = num_experts, S = num_sets, m = E / S;
+    std::vector<int64_t> load(S, 0);
+    std::vector<char> seen(E, 0);
+    for (int e = 0; e < E; ++e) {
+        const int p = log2phys ? log2phys[e] : e;
+        if (counts[e] < 0 || p < 0 || p >= E || seen[p]) return MOE_ERR_INVALID_ARG;
+        seen[p] = 1;
+        load[p / m] += counts[e];
+    }
+    const int64_t total = std::accumulate(load.begin(), load.end(), (int64_t)0);
+    const int64_t mx = *std::max_element(load.begin(), load.end());
+    *max_over_mean = total > 0 ? (double)mx * S / (double)total : 1.0;
+    return MOE_OK;
+}
+
 extern "C" int expert_affinity_permutation(const int64_t *counts, const int64_t *coact,
                                            int32_t num_experts, int32_t num_sets,
                                            double load_slack, int32_t *log2phys,

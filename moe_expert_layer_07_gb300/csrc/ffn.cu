@@ -736,13 +736,13 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
     static int attr_rc[64];
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return cuda_fail("device ordinal beyond 63");
     std::call_once(attr_once[dev], [&] {
-        attr_rc[dev] = cudaFuncSetAttribute(expert_ffn_kernel<FP8, kEW>,
+        attr_rc[dev] = (int)cudaFuncSetAttribute(expert_ffn_kernel<FP8, kEW>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            kSmemBytes) == cudaSuccess ? 0 : 1;
+                                            kSmemBytes);
     });
-    if (attr_rc[dev]) return MOE_ERR_CUDA;
+    if (attr_rc[dev]) return cuda_fail("cudaFuncSetAttribute", (cudaError_t)attr_rc[dev]);
     constexpr int kKE = FP8 ? 128 : 64;
     CUtensorMap tmW13, tmX, tmW2, tmH, tmX32, tmH32;
     const uint64_t w13_rows = (uint64_t)groups * 2 * inter, w2_rows = (uint64_t)groups * hidden;
@@ -756,7 +756,7 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
         !encode_2d(&tmH, h, FP8, (uint64_t)inter, (uint64_t)rows, kBoxRows) ||
         !encode_2d(&tmX32, xp, FP8, (uint64_t)hidden, (uint64_t)rows, kBN) ||
         !encode_2d(&tmH32, h, FP8, (uint64_t)inter, (uint64_t)rows, kBN))
-        return MOE_ERR_CUDA;
+        return cuda_fail("cuTensorMapEncodeTiled");
     if (!sched_zeroed) MOE_CUDA_TRY(cudaMemsetAsync(sched, 0, ffn_sched_bytes(groups, rows), s));
     FfnArgs a;
     a.groups = groups;

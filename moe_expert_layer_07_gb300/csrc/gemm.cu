@@ -693,23 +693,21 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
     static int attr_rc[64];
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return cuda_fail("device ordinal beyond 63");
     std::call_once(attr_once[dev], [&] {
-        attr_rc[dev] = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            Sh::kSmemBytes) == cudaSuccess
-                           ? 0
-                           : 1;
+        attr_rc[dev] = (int)cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                            Sh::kSmemBytes);
     });
-    if (attr_rc[dev]) return MOE_ERR_CUDA;
+    if (attr_rc[dev]) return cuda_fail("cudaFuncSetAttribute", (cudaError_t)attr_rc[dev]);
     CUtensorMap tmW, tmA;
     const bool tmw_ok =
         args.w_tiled
             ? encode_2d(&tmW, w, FP8, (uint64_t)Sh::kKPerStage,
                         (uint64_t)args.groups * args.n_out * (args.k_dim / Sh::kKPerStage), kBM)
             : encode_2d(&tmW, w, FP8, (uint64_t)args.k_dim, (uint64_t)args.groups * args.n_out, kBM);
-    if (!tmw_ok) return MOE_ERR_CUDA;
+    if (!tmw_ok) return cuda_fail("cuTensorMapEncodeTiled (weights)");
     if (!encode_2d(&tmA, a, FP8, (uint64_t)args.k_dim, (uint64_t)args.rows, Sh::kABox))
-        return MOE_ERR_CUDA;
+        return cuda_fail("cuTensorMapEncodeTiled (activations)");
     const int64_t tiles_bound =
         (int64_t)(args.n_out / kBM / (SW ? 2 : 1)) * (args.groups + ceil_div(args.rows, BN));
     const int grid = (int)std::min<int64_t>((int64_t)sm_count() * kCtasPerSm, tiles_bound);
@@ -766,6 +764,11 @@ int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int r
     args.c_bf16 = !fp8;
     args.w_tiled = w_tiled;
     args.status = status;
+    // Groups averaging 16 rows or more: token rows on the MMA's M side, the
+    // gate and up rows of 128 features on N (gemm_wide.cu).
+    if (fp8 && (int64_t)rows >= 16 * (int64_t)groups)
+        return launch_swiglu_wide(groups, inter, k_dim, rows, a, a_scales, offsets, w13,
+                                  w13_scales, w_tiled, h, h_scales, status, s);
     if (fp8) return launch_impl<true, 32, 2, true>(args, a, w13, s);
     return launch_impl<false, 32, 2, true>(args, a, w13, s);
 }

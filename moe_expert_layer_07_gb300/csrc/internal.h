@@ -28,6 +28,10 @@ inline int groups_of(const moe_config *cfg) { return cfg->num_experts + cfg->num
 // Number of streaming multiprocessors of the current device (cached).
 int sm_count();
 
+// Records what failed (for moe_last_error_detail on this thread) and returns
+// MOE_ERR_CUDA.  e = cudaSuccess when the failure has no CUDA error code.
+int cuda_fail(const char *where, cudaError_t e = cudaSuccess);
+
 // ---- launchers (validated arguments; return MOE_OK or MOE_ERR_CUDA) ----
 // Weight rows the expert FFN will read first, for the gate-logit kernel to
 // prefetch into L2 while routing keeps HBM idle: the first `bytes` of every
@@ -57,6 +61,12 @@ int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int r
                                const void *a, const float *a_scales, const int32_t *offsets,
                                const void *w13, const float *w13_scales, bool w_tiled, void *h,
                                float *h_scales, int32_t *status, cudaStream_t s);
+// Wide FP8 batches (groups averaging 16 rows or more): gate/up + SwiGLU +
+// FP8 requantisation with token rows on the MMA's M side (gemm_wide.cu).
+int launch_swiglu_wide(int groups, int inter, int k_dim, int rows, const void *a,
+                       const float *a_scales, const int32_t *offsets, const void *w13,
+                       const float *w13_scales, bool w_tiled, void *h, float *h_scales,
+                       int32_t *status, cudaStream_t s);
 // The experts' FFN in one persistent kernel (FP8 or BF16): gate/up + SwiGLU
 // (+ FP8 requant), then down.  `sched` holds ffn_sched_bytes(groups, rows) bytes; it is
 // cleared on `s` unless the caller has already zeroed it in stream order.
@@ -87,7 +97,8 @@ int launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
     at[0].val.programmaticStreamSerializationAllowed = 1;
     c.attrs = at;
     c.numAttrs = 1;
-    return cudaLaunchKernelEx(&c, kernel, args...) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    const cudaError_t e = cudaLaunchKernelEx(&c, kernel, args...);
+    return e == cudaSuccess ? MOE_OK : cuda_fail("cudaLaunchKernelEx", e);
 }
 
 // Kernel launches per call, for the layer's launch count.
@@ -99,10 +110,11 @@ int permute_kernel_count(const moe_config *cfg, int T);
 #define MOE_CUDA_TRY(expr)                                   \
     do {                                                     \
         cudaError_t _e = (expr);                             \
-        if (_e != cudaSuccess) return MOE_ERR_CUDA;          \
+        if (_e != cudaSuccess) return moe::cuda_fail(#expr, _e); \
     } while (0)
 
 #define MOE_LAUNCH_CHECK()                                   \
     do {                                                     \
-        if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA; \
+        cudaError_t _e = cudaGetLastError();                 \
+        if (_e != cudaSuccess) return moe::cuda_fail("kernel launch", _e); \
     } while (0)

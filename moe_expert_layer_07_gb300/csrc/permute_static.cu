@@ -9,6 +9,8 @@
 // device array instead of a caller buffer.  The array is part of the
 // library image: every GPU that loads the library holds it until the
 // process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "internal.h"
@@ -20,22 +22,58 @@ constexpr size_t kStaticScratchBytes = size_t(1) << 20;   // 1 MiB
 
 static __device__ __align__(256) unsigned char g_permute_scratch[kStaticScratchBytes];
 
+// Identity of the current CUDA context (driver entry points looked up at run
+// time, so the library still loads where no driver is installed); 0 when it
+// cannot be told.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static GetCurrent get_current = nullptr;
+    static GetId get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrent>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetId>(p);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 // The array's device address for the current device.  In host code the
 // symbol names a host-side stand-in, never the device memory, so the address
-// is looked up once per device (with that device current) and cached.
+// is looked up (with the device current) the first time a device is used and
+// again whenever that device's context has changed since (a device reset
+// unloads the module that holds the array, and the old address would be
+// stale); where the context cannot be identified it is looked up on every call.
 int static_scratch_address(void **out) {
     static std::mutex mu;
     static void *addr[64];
-    static bool ready[64];
+    static unsigned long long ctx_of[64];
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    const cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return moe::cuda_fail("cudaGetDevice", e);
+    if (dev < 0 || dev >= 64) return moe::cuda_fail("device ordinal beyond 63");
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(mu);
-    if (!ready[dev]) {
+    if (ctx == 0 || ctx_of[dev] != ctx || !addr[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || p == nullptr)
-            return MOE_ERR_CUDA;
+        const cudaError_t es = cudaGetSymbolAddress(&p, g_permute_scratch);
+        if (es != cudaSuccess || p == nullptr) return moe::cuda_fail("cudaGetSymbolAddress", es);
         addr[dev] = p;
-        ready[dev] = true;
+        ctx_of[dev] = ctx;
     }
     *out = addr[dev];
     return MOE_OK;

@@ -455,18 +455,16 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
     static int attr_rc[64];
     int dev = 0;
     MOE_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return cuda_fail("device ordinal beyond 63");
     std::call_once(attr_once[dev], [&] {
-        attr_rc[dev] = cudaFuncSetAttribute(gate_logits_kernel<4>,
+        attr_rc[dev] = (int)cudaFuncSetAttribute(gate_logits_kernel<4>,
                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
                                cudaSuccess &&
                                cudaFuncSetAttribute(gate_logits_kernel<8>,
                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    smem) == cudaSuccess
-                           ? 0
-                           : 1;
+                                                    smem);
     });
-    if (attr_rc[dev]) return MOE_ERR_CUDA;
+    if (attr_rc[dev]) return cuda_fail("cudaFuncSetAttribute", (cudaError_t)attr_rc[dev]);
     const L2Prefetch none;
     // 8 x 8 warp tiles once the CTAs outnumber a few per SM; decode batches
     // keep 8 warps per CTA for latency hiding.  Both give the same bits.

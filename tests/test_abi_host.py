@@ -71,7 +71,7 @@ def test_layer_kernel_counts(L):
     r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
     assert moe.layer_kernel_count(r1, 128) == 7        # one-kernel FFN, 1024 slots
     assert moe.layer_kernel_count(r1, 129) == 8        # 1032 slots: count and scan apart
-    assert moe.layer_kernel_count(r1, 4096) == 10      # wide: GEMM, SiLU-mul, GEMM
+    assert moe.layer_kernel_count(r1, 4096) == 9       # wide: SwiGLU GEMM, down GEMM
     mini = moe.make_config(synth.CONFIGS["r1_mini"])   # inter 384: odd K blocks of W2
     assert moe.layer_kernel_count(mini, 37) == 7
     b16 = moe.make_config(synth.CONFIGS["bf16_mini"])   # BF16: one-kernel FFN
@@ -206,6 +206,28 @@ def test_balance_rejects_bad_arguments(L):
     c[2] = -1
     assert L.expert_balance_permutation(c.ctypes.data, 10, 5, out.ctypes.data, out.ctypes.data,
                                         None) == -1
+
+
+def test_set_imbalance_of_a_given_permutation(L):
+    """The library's set-imbalance figure against the oracle's definition, for
+    the identity, random and balanced permutations; bad tables are rejected."""
+    rng = np.random.default_rng(5)
+    for E, S in ((8, 2), (32, 4), (256, 8)):
+        counts = rng.integers(0, 1000, size=E)
+        for l2p in (None, rng.permutation(E).astype(np.int32),
+                    moe.balance_permutation(counts, S)[0]):
+            ref_perm = np.arange(E) if l2p is None else l2p
+            ref = balance.imbalance(balance.set_loads(counts, ref_perm, S))
+            assert abs(moe.set_imbalance(counts, l2p, S) - ref) < 1e-12
+    assert moe.set_imbalance(np.zeros(8, np.int64), None, 2) == 1.0
+    c = np.ones(8, np.int64)
+    bad = np.arange(8, dtype=np.int32)
+    bad[3] = 2                                    # repeated id
+    v = ctypes.c_double()
+    assert L.expert_set_imbalance(c.ctypes.data, bad.ctypes.data, 8, 2, ctypes.byref(v)) == -1
+    bad[3] = 8                                    # out of range
+    assert L.expert_set_imbalance(c.ctypes.data, bad.ctypes.data, 8, 2, ctypes.byref(v)) == -1
+    assert L.expert_set_imbalance(c.ctypes.data, None, 8, 3, ctypes.byref(v)) == -1
 
 
 def test_source_slots_apply_a_new_permutation():

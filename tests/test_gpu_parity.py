@@ -26,7 +26,10 @@ pytestmark = pytest.mark.gpu
 
 SMALL = ["tiny_bf16", "v2lite_bf16", "r1_mini", "r1_mini_zipf", "r1_mini_i512", "bf16_mini"]
 FULL = ["r1_decode_t128", "r1_zipf_t1024", "r1_prefill_t4096"]
-SAMPLE = {"r1_decode_t128": 16, "r1_zipf_t1024": 16, "r1_prefill_t4096": 16}
+# tokens of the full-size layers whose output is compared with the oracle: all
+# 128 of the decode batch (every active expert's FFN output enters some
+# token), 64 seeded tokens of the wider batches
+SAMPLE = {"r1_decode_t128": 128, "r1_zipf_t1024": 64, "r1_prefill_t4096": 64}
 
 
 @pytest.fixture(scope="module")
@@ -206,7 +209,7 @@ def run_permute(cfg, s, ids_t, x_rows, x_scales):
 
 
 @pytest.mark.parametrize("name", ["r1_mini", "bf16_mini", "v2lite_bf16", "r1_decode_t128",
-                                  "r1_prefill_t4096"])
+                                  "r1_zipf_t1024", "r1_prefill_t4096"])
 def test_permute_bit_exact(lib, name):
     wl = workload(name)
     s = wl.shape
@@ -356,6 +359,27 @@ def test_grouped_gemm_rejects_inconsistent_offsets(lib):
     assert torch.all(c == 3.0)                  # nothing was written
 
 
+def test_swiglu_wide_rejects_inconsistent_offsets(lib):
+    """The token-rows-on-M SwiGLU kernel (16+ rows per group) flags offsets that
+    run backwards or past the rows, and writes nothing."""
+    s = synth.CONFIGS["r1_mini"]
+    cfg = moe.make_config(s)
+    K, inter, rows = 128, 128, 64
+    a = torch.zeros((rows, K), dtype=torch.uint8, device="cuda")
+    asc = torch.ones((rows, 1), device="cuda")
+    w = torch.zeros((2, 2 * inter, K), dtype=torch.uint8, device="cuda")
+    wsc = torch.ones((2, 2, 1), device="cuda")
+    for bad in ([0, 40, 20], [0, 30, 70]):      # decreasing; past the rows
+        h = torch.full((rows, inter), 7, dtype=torch.uint8, device="cuda")
+        hs = torch.full((rows, 1), 3.0, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        off = torch.tensor(bad, dtype=torch.int32, device="cuda")
+        moe.grouped_gemm_swiglu(cfg, 2, inter, K, rows, a, asc, off, w, wsc, h, hs, st)
+        torch.cuda.synchronize()
+        assert int(st.item()) & moe.DEV_BAD_OFFSETS
+        assert torch.all(h == 7) and torch.all(hs == 3.0)
+
+
 # ------------------------------------------------------------------ combine
 @pytest.mark.parametrize("out_bf16", [False, True])
 def test_combine(lib, out_bf16):
@@ -423,7 +447,10 @@ def test_layer_parity_full_size(lib, name):
     assert layer.status() == 0
     print(f"{name}: max|gpu-oracle|/rms over {len(tokens)} tokens = {rel:.2e}")
     if s.balanced_perm:
+        # the report (section "Load balancing across GPUs") brings the sets
+        # within 5% of each other with the balanced grouping
         assert wl.imbalance <= wl.naive_imbalance
+        assert wl.imbalance <= 1.05
         print(f"{name}: set imbalance balanced {wl.imbalance:.4f}, contiguous {wl.naive_imbalance:.4f}")
 
 
@@ -526,13 +553,17 @@ def test_bounded_wait_reports_timeout_and_context_survives(lib):
 
 @pytest.mark.parametrize("fp8,inter,K,counts", [
     (True, 384, 1024, GEMM_ROWS), (True, 2048, 7168, [3, 0, 17, 40, 128, 1]),
+    (True, 384, 1024, [127, 128, 129, 0, 255, 256, 300, 1, 520, 33]),
+    (True, 2048, 7168, [150, 130, 120, 0, 140, 600, 7]),
     (True, 384, 1024, [0, 1, 15, 16, 17, 3, 9, 2, 0, 5, 31]),
     (True, 2048, 7168, [2, 0, 9, 1, 14, 3]),
     (False, 384, 512, GEMM_ROWS)])
 def test_swiglu_epilogue_equals_gemm_then_silu_requant(lib, fp8, inter, K, counts):
-    """The fused gate/up + SwiGLU kernel gives the bits of the two-kernel path,
-    for groups averaging 16 rows or more (the first two cases, where the plain
-    GEMM takes 64-row tiles) and fewer (the next two)."""
+    """The fused gate/up + SwiGLU kernels give the bits of the two-kernel path,
+    for groups averaging 16 rows or more (the first four cases: the
+    token-rows-on-M kernel, with ragged 128-row token tiles, empty groups and
+    a group of 600 rows; the plain GEMM takes 64-row tiles there) and fewer
+    (the next two: 32-row activation tiles)."""
     s = synth.CONFIGS["r1_mini" if fp8 else "bf16_mini"]
     cfg = moe.make_config(s)
     counts = np.array(counts)

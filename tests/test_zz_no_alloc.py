@@ -39,11 +39,21 @@ def _outputs(shape, T):
                 st=torch.zeros(1, dtype=torch.int32, device="cuda"))
 
 
-@pytest.mark.parametrize("name,T", [("r1_mini", 37), ("r1_decode_t128", 128)])
+# up to 1024 routed slots the dispatch counts and scans in one CTA; above it
+# (129 and 1024 tokens at the R1 shape, and 21824, where the per-chunk counts,
+# chunk bases and per-slot ranks fill the 1 MiB array exactly) it takes the
+# multi-chunk kernels, whose scratch all lives in the static array
+@pytest.mark.parametrize("name,T", [("r1_mini", 37), ("r1_decode_t128", 128),
+                                    ("r1_decode_t128", 129), ("r1_decode_t128", 1024),
+                                    ("r1_decode_t128", 21824)])
 def test_static_scratch_permute_matches_workspace_permute(lib, name, T):
     shape = synth.CONFIGS[name]
     cfg = moe.make_config(shape, max_tokens=T)
     k, E, H = shape.top_k, shape.num_experts, shape.hidden
+    if T > 1024:
+        assert moe.permute_workspace_size(cfg, T) > moe.permute_workspace_size(cfg, 128)
+    if T == 21824:
+        assert moe.permute_workspace_size(cfg, T) == lib.moe_permute_static_scratch_capacity()
     for call in range(2):   # two calls in a row: the second reuses the scratch
         g = torch.Generator(device="cuda").manual_seed(100 + call)
         # k distinct experts per token, skewed towards low ids on the second call
