@@ -219,7 +219,9 @@ MOE_API size_t moe_permute_static_scratch_capacity(void);
  * rows sit on the MMA's M side and the few token rows of an expert on its
  * N side (the SGLang/H20 article, section "SwapAB GEMM": map the token
  * dimension to the fine-grained side of the MMA for small, variable rows
- * per expert). */
+ * per expert).  FP8 groups averaging 16 rows or more with fp32 C and N a
+ * multiple of 256 swap back: 128 token rows on M against 256 output columns
+ * on N; same bits. */
 MOE_API int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32_t k_dim,
                      int32_t rows, const void *a, const float *a_scales,
                      const int32_t *expert_offsets, const void *w, const float *w_scales,

@@ -683,6 +683,21 @@ bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint6
     return r == CUDA_SUCCESS;
 }
 
+// Row-major fp32 [outer, inner] matrix, box of 32 columns (128 bytes) x
+// box_rows, 128-byte swizzle (for TMA stores of fp32 tiles).
+bool encode_2d_f32(CUtensorMap *m, void *base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
+    auto enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {inner * 4};
+    cuuint32_t box[2] = {32, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 namespace {
 
 template <bool FP8, int BN, int STAGES, bool SW = false, int EW = 1>
@@ -739,8 +754,13 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     args.w_tiled = w_tiled;
     args.status = status;
     // Decode-sized groups (a few rows each) stream best with 32-row tiles;
-    // larger groups re-read each weight tile fewer times with 64-row tiles.
+    // larger groups take 128 token rows against 256 output columns per tile
+    // (gemm_wide.cu: one weight-tile read per 128 rows of an expert), or,
+    // for bf16 C or widths that are not a multiple of 256, 64-row tiles.
     const bool wide = (int64_t)rows >= 16 * (int64_t)groups;
+    if (fp8 && wide && n_out % 256 == 0 && c_dtype == MOE_OUT_F32)
+        return launch_gemm_wide(groups, n_out, k_dim, rows, a, a_scales, offsets, w, w_scales,
+                                w_tiled, static_cast<float *>(c), status, s);
     if (fp8) return wide ? launch_impl<true, 64, 3, false, 2>(args, a, w, s)
                          : launch_impl<true, 32, 4>(args, a, w, s);
     return launch_impl<false, 32, 4>(args, a, w, s);

@@ -67,6 +67,12 @@ int launch_swiglu_wide(int groups, int inter, int k_dim, int rows, const void *a
                        const float *a_scales, const int32_t *offsets, const void *w13,
                        const float *w13_scales, bool w_tiled, void *h, float *h_scales,
                        int32_t *status, cudaStream_t s);
+// Wide FP8 batches, fp32 C with n_out a multiple of 256: the same kernel
+// with a plain epilogue (TMA stores of 32 x 32 fp32 blocks).
+int launch_gemm_wide(int groups, int n_out, int k_dim, int rows, const void *a,
+                     const float *a_scales, const int32_t *offsets, const void *w,
+                     const float *w_scales, bool w_tiled, float *c, int32_t *status,
+                     cudaStream_t s);
 // The experts' FFN in one persistent kernel (FP8 or BF16): gate/up + SwiGLU
 // (+ FP8 requant), then down.  `sched` holds ffn_sched_bytes(groups, rows) bytes; it is
 // cleared on `s` unless the caller has already zeroed it in stream order.

@@ -13,4 +13,8 @@ namespace moe {
 bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint64_t outer,
                uint32_t box_rows);
 
+// Tensor map of a row-major fp32 [outer, inner] matrix with a box of 32
+// columns (128 bytes) x box_rows and 128-byte swizzle, for TMA stores.
+bool encode_2d_f32(CUtensorMap *m, void *base, uint64_t inner, uint64_t outer, uint32_t box_rows);
+
 }  // namespace moe

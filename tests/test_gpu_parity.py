@@ -304,15 +304,18 @@ def test_grouped_gemm(lib, fp8, N, K, out_bf16):
 WIDE_ROWS = [0, 1, 127, 128, 129, 0, 255, 64, 300, 17]
 
 
-def test_grouped_gemm_tile_variants_agree(lib):
-    """The 32- and 64-row activation tiles (chosen by rows per group) promote
-    per K block in the same order: the same bits, within the oracle's
-    tolerance.  Empty groups appended to the same problem move it between
-    the variants."""
+@pytest.mark.parametrize("N,K,counts", [(384, 1024, WIDE_ROWS), (512, 1024, WIDE_ROWS),
+                                         (7168, 2048, [150, 130, 120, 0, 140, 600, 7])])
+def test_grouped_gemm_tile_variants_agree(lib, N, K, counts):
+    """The kernels chosen by rows per group promote per K block in the same
+    order: the same bits, within the oracle's tolerance.  Empty groups
+    appended to the same problem move it between them: 32-row activation
+    tiles for few rows per group; for 16 or more, 128 token rows against 256
+    output columns when N is a multiple of 256 (512, and the R1 down
+    projection's 7168 with ragged 128-row token tiles), else 64-row tiles."""
     s = synth.CONFIGS["r1_mini"]
     cfg = moe.make_config(s)
-    N, K = 384, 1024
-    counts = np.array(WIDE_ROWS)
+    counts = np.array(counts)
     rows = int(counts.sum())
     g = torch.Generator(device="cuda").manual_seed(11)
     a32 = torch.randn(rows, K, device="cuda", generator=g)
@@ -323,7 +326,7 @@ def test_grouped_gemm_tile_variants_agree(lib):
     w, wsc = synth.block_quantize_e4m3(
         torch.randn(len(counts), N, K, device="cuda", generator=g) * 0.05)
     outs = []
-    for extra in (0, 40, 70):   # 102, 20 and 13 rows per group: 64, 64 and 32-row tiles
+    for extra in (0, 40, 70):   # WIDE_ROWS: 102, 20 and 13 rows per group
         G = len(counts) + extra
         off = np.concatenate([[0], np.cumsum(np.concatenate([counts, np.zeros(extra, int)]))])
         wpad = torch.cat([w, torch.zeros((extra, N, K), dtype=w.dtype, device="cuda")])
