@@ -17,7 +17,7 @@ __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_
            "permute", "permute_workspace_size", "permute_static_scratch", "grouped_gemm", "combine", "layer_forward",
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
            "last_error_detail",
-           "balance_permutation", "set_imbalance", "layer_kernel_count", "MoELayer", "MoEError",
+           "balance_permutation", "set_imbalance", "rebalance_due", "layer_kernel_count", "MoELayer", "MoEError",
            "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
            "count_coactivation", "affinity_permutation", "grouped_gemm_swiglu",
            "expert_ffn", "experts_forward", "expert_ffn_sched_bytes", "pack_expert_weights", "LAYOUT_ROWS",
@@ -364,6 +364,17 @@ def set_imbalance(counts, log2phys, num_sets: int) -> float:
     return v.value
 
 
+def rebalance_due(batches: int, every, max_imbalance, check_every: int, imbalance) -> bool:
+    """The periodic re-balancing policy: due after `every` counted batches, or,
+    with max_imbalance set, when imbalance() (called only on every
+    check_every-th batch) exceeds it."""
+    if every is not None and batches >= every:
+        return True
+    if max_imbalance is not None and batches % check_every == 0:
+        return imbalance() > max_imbalance
+    return False
+
+
 class MoELayer:
     """One MoE layer: device weights, a workspace and the forward call.
 
@@ -437,10 +448,12 @@ class MoELayer:
 
 class ExpertRebalancer:
     """Continuous load balancing of one MoELayer: counts each batch's rows per
-    expert on the device, and on request derives a new balanced permutation
-    from the counts and re-lays the expert weights into it on a side stream
-    (report "21K output tokens/s DeepSeek inference on MI300X with Expert
-    Parallelism", section "Load balancing across GPUs").
+    expert on the device, and -- on request (rebalance) or by the periodic
+    policy of step() -- derives a new balanced permutation from the counts
+    and re-lays the expert weights into it on a side stream (report "21K
+    output tokens/s DeepSeek inference on MI300X with Expert Parallelism",
+    section "Load balancing across GPUs": activation frequencies are
+    re-measured at regular intervals and the permutation renewed).
 
     The layer's output does not change when its experts move: routing is
     defined on logical ids and each expert's rows are computed the same way
@@ -449,15 +462,33 @@ class ExpertRebalancer:
 
     _BLOCKS = ("w13", "w13_s", "w2", "w2_s")
 
-    def __init__(self, layer: MoELayer, num_sets: int, affinity_slack: float | None = None):
+    def __init__(self, layer: MoELayer, num_sets: int, affinity_slack: float | None = None,
+                 every: int | None = None, max_imbalance: float | None = None,
+                 check_every: int = 1):
         """affinity_slack: None for plain balancing; a value (e.g. 0.05) to
         also track co-activation and place co-selected experts together with
-        set totals allowed up to (1 + slack) x the mean."""
+        set totals allowed up to (1 + slack) x the mean.
+
+        The periodic policy of step() (the report's re-measurement "at
+        regular intervals"): every -- re-balance after this many counted
+        batches; max_imbalance -- re-balance as soon as the counts since the
+        last re-balance put the busiest set above this multiple of the mean
+        under the current permutation, looked at every check_every batches
+        (the look reads the counts to the host)."""
         import numpy as np
         import torch
+        if every is not None and every < 1:
+            raise ValueError("every must be at least 1")
+        if max_imbalance is not None and max_imbalance < 1.0:
+            raise ValueError("max_imbalance is a max / mean ratio, at least 1")
+        if check_every < 1:
+            raise ValueError("check_every must be at least 1")
         self.layer = layer
         self.num_sets = num_sets
         self.affinity_slack = affinity_slack
+        self.every, self.max_imbalance, self.check_every = every, max_imbalance, check_every
+        self.batches = 0          # batches counted since the last re-balance
+        self.history = []         # (batches counted, imbalance before, after) per re-balance
         s = layer.shape
         dev = layer._keep["w13"].device
         self.counts = torch.zeros(s.num_experts, dtype=torch.int64, device=dev)
@@ -483,6 +514,25 @@ class ExpertRebalancer:
     def logical_counts(self):
         """Rows per logical expert since the last re-balance (synchronous read)."""
         return self.counts.cpu().numpy()[self.log2phys]
+
+    def current_imbalance(self) -> float:
+        """Busiest set / mean set of the counts since the last re-balance under
+        the current permutation (synchronous read)."""
+        return set_imbalance(self.logical_counts(), self.log2phys, self.num_sets)
+
+    def step(self, T=None, stream=None):
+        """Counts the batch the layer just ran and applies the periodic policy
+        given at construction.  Returns (imbalance before, after) when it
+        re-balanced, else None."""
+        self.observe(T, stream)
+        self.batches += 1
+        if not rebalance_due(self.batches, self.every, self.max_imbalance, self.check_every,
+                             self.current_imbalance):
+            return None
+        n = self.batches
+        before, after = self.rebalance()
+        self.history.append((n, before, after))
+        return before, after
 
     def rebalance(self, counts=None):
         """New permutation from the counts; weights re-laid on a side stream,
@@ -521,6 +571,7 @@ class ExpertRebalancer:
             if self.coact is not None:
                 self.coact.zero_()
         cur.wait_stream(self.side)
+        self.batches = 0
         for key in self._BLOCKS:   # old buffers stay valid until the copy is done
             if lay._keep.get(key) is not None:
                 lay._keep[key].record_stream(self.side)

@@ -2,6 +2,7 @@
 // device status.  Every entry point validates before enqueuing anything and
 // never synchronises the host (except moe_get_device_status, which exists to).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdio>
 #include <mutex>
@@ -9,6 +10,18 @@
 #include "internal.h"
 
 namespace moe {
+
+namespace {
+// An NVTX range around each entry point (and each step of the layer call),
+// so that a profiler's timeline names the library's calls; without a tool
+// attached a push/pop is a call to an empty function.
+struct Range {
+    explicit Range(const char *name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range &) = delete;
+    Range &operator=(const Range &) = delete;
+};
+}  // namespace
 
 namespace {
 thread_local char g_error_detail[256] = "";
@@ -161,6 +174,7 @@ int moe_route(const moe_config *cfg, int32_t T, const void *x, const void *w_gat
               const float *e_bias, const float *logit_offset, const int32_t *log2phys,
               float *logits, int32_t *topk_ids, float *topk_w, int32_t *dev_status,
               void *stream) {
+    Range range("moe_route");
     int rc = check_config(cfg);
     if (rc) return rc;
     if (T < 0) return MOE_ERR_INVALID_ARG;
@@ -174,6 +188,7 @@ int moe_route(const moe_config *cfg, int32_t T, const void *x, const void *w_gat
 
 int moe_act_requant(const moe_config *cfg, int32_t mode, int32_t rows, const int32_t *rows_dev,
                     const void *in, void *out, float *out_scales, void *stream) {
+    Range range("moe_act_requant");
     int rc = check_config(cfg);
     if (rc) return rc;
     if (rows < 0 || (mode != MOE_ACT_IDENTITY && mode != MOE_ACT_SILU_MUL))
@@ -199,6 +214,7 @@ int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_ids, const
                 const float *x_scales, int32_t *expert_offsets, int32_t *src_of_row,
                 int32_t *row_of_slot, void *xp, float *xp_scales, void *ws, size_t ws_bytes,
                 int32_t *dev_status, void *stream) {
+    Range range("moe_permute");
     int rc = check_config(cfg);
     if (rc) return rc;
     if (T < 0 || !expert_offsets) return MOE_ERR_INVALID_ARG;
@@ -219,6 +235,7 @@ int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32
                      const int32_t *expert_offsets, const void *w, const float *w_scales,
                      int32_t w_layout, void *c, int32_t c_dtype, int32_t *dev_status,
                      void *stream) {
+    Range range("moe_grouped_gemm");
     int rc = check_config(cfg);
     if (rc) return rc;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
@@ -245,6 +262,7 @@ int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter
                             const int32_t *expert_offsets, const void *w13,
                             const float *w13_scales, int32_t w_layout, void *h, float *h_scales,
                             int32_t *dev_status, void *stream) {
+    Range range("moe_grouped_gemm_swiglu");
     int rc = check_config(cfg);
     if (rc) return rc;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
@@ -276,6 +294,7 @@ int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const vo
                    const float *w13_scales, const void *w2, const float *w2_scales,
                    int32_t w_layout, void *h, float *h_scales, float *y, int32_t *sched,
                    size_t sched_bytes, int32_t *dev_status, void *stream) {
+    Range range("moe_expert_ffn");
     int rc = check_config(cfg);
     if (rc) return rc;
     if (groups <= 0 || rows < 0 || !layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
@@ -305,6 +324,7 @@ int moe_experts_forward(const moe_config *cfg, int32_t groups, int32_t rows, con
                         const float *w13_scales, const void *w2, const float *w2_scales,
                         int32_t w_layout, void *h, float *h_scales, float *y, int32_t *sched,
                         size_t sched_bytes, int32_t *dev_status, void *stream) {
+    Range range("moe_experts_forward");
     int rc = check_config(cfg);
     if (rc) return rc;
     if (groups <= 0 || rows < 0 || !layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
@@ -331,6 +351,7 @@ int moe_experts_forward(const moe_config *cfg, int32_t groups, int32_t rows, con
 int moe_combine(const moe_config *cfg, int32_t T, const void *y, const int32_t *row_of_slot,
                 const float *topk_w, const int32_t *expert_offsets, void *out, int32_t out_dtype,
                 void *stream) {
+    Range range("moe_combine");
     int rc = check_config(cfg);
     if (rc) return rc;
     if (T < 0 || (out_dtype != MOE_OUT_F32 && out_dtype != MOE_OUT_BF16)) return MOE_ERR_INVALID_ARG;
@@ -368,6 +389,7 @@ int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
 
 int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, const void *x,
                       void *out, int32_t out_dtype, void *ws, size_t ws_bytes, void *stream) {
+    Range range("moe_layer_forward");
     int rc = check_config(cfg);
     if (rc) return rc;
     if (!w || !ws || T < 0 || T > cfg->max_tokens) return MOE_ERR_INVALID_ARG;
@@ -424,8 +446,11 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
         pf.bytes = H < 1536 ? H : 1536;
         pf.tiled = tiled;
     }
-    rc = launch_route(cfg, T, x, w->w_gate, w->e_bias, w->logit_offset, w->log2phys, logits, ids,
-                      tw, status, s, fused ? &pf : nullptr);
+    {
+        Range r("route");
+        rc = launch_route(cfg, T, x, w->w_gate, w->e_bias, w->logit_offset, w->log2phys, logits,
+                          ids, tw, status, s, fused ? &pf : nullptr);
+    }
     if (rc) return rc;
     const void *rows_src = x;
     const float *rows_scales = nullptr;
@@ -436,11 +461,15 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
         rows_src = base + L.xq;
         rows_scales = reinterpret_cast<const float *>(base + L.xs);
     }
-    rc = launch_permute(cfg, T, ids, rows_src, rows_scales, offsets, src, ros, base + L.xp,
-                        reinterpret_cast<float *>(base + L.xp_scales), base + L.perm_scratch,
-                        status, s);
+    {
+        Range r("dispatch");
+        rc = launch_permute(cfg, T, ids, rows_src, rows_scales, offsets, src, ros, base + L.xp,
+                            reinterpret_cast<float *>(base + L.xp_scales), base + L.perm_scratch,
+                            status, s);
+    }
     if (rc) return rc;
     // the one-kernel FFN's scheduler counters were cleared with the status word
+    Range r_ffn("experts");
     rc = experts_forward(fp8, G, H, I, rows, base + L.xp,
                          reinterpret_cast<const float *>(base + L.xp_scales), offsets, w->w13,
                          w->w13_scales, w->w2, w->w2_scales, tiled, base + L.h,

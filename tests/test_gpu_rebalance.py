@@ -122,3 +122,48 @@ def test_coactivation_counts_equal_the_oracle(lib):
     torch.cuda.synchronize()
     assert torch.equal(out, out_b) and layer.status() == 0
     assert 0.0 <= reb.last_intra_fraction <= 1.0
+
+
+def test_periodic_rebalance_retightens_a_drifting_stream(lib):
+    """A stream whose expert popularity drifts (a new seeded Zipf order every
+    three batches): the every-3-batches policy re-balances at the end of each
+    phase.  Each re-balance brings the phase's counts from their imbalance
+    under the old permutation down to the balanced partition's, and the layer
+    gives the same bits for the same batch before and after each move."""
+    shape = synth.CONFIGS["r1_mini_zipf"]
+    inp = synth.make_inputs(shape, seed=0, device="cuda")
+    layer = moe.MoELayer(shape, inp)
+    reb = moe.ExpertRebalancer(layer, shape.num_sets, every=3)
+    offset = layer._keep["logit_offset"]          # the prior the layer routes with
+    T, H = shape.tokens, shape.hidden
+    out = torch.empty((T, H), device="cuda")
+    g = torch.Generator(device="cuda").manual_seed(77)
+    befores, afters = [], []
+    for phase in range(3):
+        offset.copy_(synth.zipf_logit_offset(shape, 100 + phase, "cuda"))
+        for b in range(3):
+            x = torch.randn((T, H), device="cuda", generator=g).to(torch.bfloat16)
+            layer.forward(x, out)
+            counted = reb.logical_counts() + np.bincount(
+                _oracle_phys_ids(shape, {**inp, "logit_offset": offset}, x)[1].reshape(-1),
+                minlength=shape.num_experts)
+            prev_l2p = reb.log2phys.copy()
+            res = reb.step()
+            assert (res is not None) == (b == 2)
+        before, after = res
+        # the policy's figures are those of the phase's counts
+        assert before == pytest.approx(moe.set_imbalance(counted, prev_l2p, shape.num_sets))
+        assert after == pytest.approx(moe.set_imbalance(counted, reb.log2phys, shape.num_sets))
+        _, _, best = moe.balance_permutation(counted, shape.num_sets)
+        assert after == pytest.approx(best) and after <= before
+        ref = out.clone()
+        layer.forward(x, out)                       # the same batch after the move
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref) and layer.status() == 0
+        befores.append(before)
+        afters.append(after)
+    assert [h[0] for h in reb.history] == [3, 3, 3]
+    # after the first phase the stream drifts: the old placement no longer fits
+    assert all(b > a for b, a in zip(befores[1:], afters[1:]))
+    print(f"set imbalance per phase, before -> after: "
+          f"{[(round(b, 3), round(a, 3)) for b, a in zip(befores, afters)]}")
