@@ -171,7 +171,7 @@ class Stepper:
                    "h_scales", "y", "ffn_sched")}
         self.perm_bytes = moe.permute_workspace_size(layer.cfg, s.tokens)
         rows = s.tokens * (s.top_k + s.num_shared)
-        self.wide = self.fp8 and rows >= 16 * s.groups   # as moe_layer_forward decides
+        self.wide = self.fp8 and rows >= 32 * s.groups   # as moe_layer_forward decides
         self.fused = not self.wide   # as moe_layer_forward decides
         self.NAMES = self.NAMES_FUSED if self.fused else self.NAMES_WIDE
         self.sched_bytes = moe.expert_ffn_sched_bytes(s.groups, rows)
@@ -279,7 +279,7 @@ def path_bytes(shape, offsets):
     b["route"] = 2 * T * H + 2 * E * H + 4 * T * E * 2 + 8 * T * k
     b["quant_x"] = (2 * T * H + T * H + T * sc_h) if fp8 else 0
     b["permute"] = 4 * T * k * 3 + rows * (H * eb + sc_h) * 2
-    wide = fp8 and rows >= 16 * (E + S)
+    wide = fp8 and rows >= 32 * (E + S)
     if wide:   # gate/up GEMM with the SwiGLU + requantisation epilogue
         b["gemm_gate_up_swiglu"] = active * w13 + rows * (H * eb + sc_h) + rows * (I * eb + sc_i)
     b["gemm_down"] = active * w2 + rows * (I * eb + sc_i) + rows * H * 4

@@ -285,7 +285,7 @@ MOE_API int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, 
 
 /* The experts' FFN on dispatched rows with the kernels moe_layer_forward
  * would pick for this batch: moe_expert_ffn for BF16 layers and for FP8
- * groups averaging fewer than 16 rows (rows < 16 * groups), otherwise
+ * groups averaging fewer than 32 rows (rows < 32 * groups), otherwise
  * moe_grouped_gemm_swiglu followed by moe_grouped_gemm (down, fp32 y).
  * Arguments, layouts, ownership and errors as moe_expert_ffn (sched is
  * cleared on `stream` and used only by the one-kernel path); every choice
@@ -326,9 +326,9 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
 /* ---- the whole layer -------------------------------------------------------------
  * route -> (FP8: quantise x) -> permute -> the experts' FFN -> combine, all
  * on `stream`.  The experts' FFN is
- *   BF16, and FP8 with groups averaging fewer than 16 rows (decode):
+ *   BF16, and FP8 with groups averaging fewer than 32 rows (decode):
  *     moe_expert_ffn (one persistent kernel);
- *   FP8, groups averaging 16 rows or more: moe_grouped_gemm_swiglu (its
+ *   FP8, groups averaging 32 rows or more: moe_grouped_gemm_swiglu (its
  *     token-rows-on-M kernel) then moe_grouped_gemm down (64-row tiles);
  * all with the same result bits (fp32 expert outputs), and
  * all intermediates inside `ws` (size from moe_workspace_size for

@@ -82,12 +82,16 @@ bool tiled_fits(int64_t groups, int64_t n_out, int64_t k_dim, bool fp8) {
     return groups * n_out * (k_dim / (fp8 ? 128 : 64)) <= INT32_MAX;
 }
 
-// Groups averaging 16 rows or more: FP8 batches this wide take the two-kernel
-// path (gate/up + SwiGLU with token rows on the MMA's M side, then the down
-// GEMM) instead of the one-kernel FFN.
+// Rows per group from which FP8 batches take the wide GEMMs (gate/up + SwiGLU
+// with token rows on the MMA's M side, then the down GEMM) instead of the
+// one-kernel FFN.  Same-box timings of both on the same R1 rows (identical
+// bits): FFN / GEMMs 1.665 / 1.860 ms at 16 rows per group, 1.800 / 1.898 at
+// 26.9, 2.042 / 1.924 at 35.9.
+constexpr int64_t kWideRowsPerGroup = 32;
+
 bool wide_rows(const moe_config *cfg, int64_t T) {
     return cfg->dtype == MOE_DTYPE_FP8_BLOCK128 &&
-           total_rows(cfg, T) >= 16 * (int64_t)groups_of(cfg);
+           total_rows(cfg, T) >= kWideRowsPerGroup * (int64_t)groups_of(cfg);
 }
 
 // Both expert GEMMs run in one persistent kernel for BF16 layers and FP8
@@ -97,7 +101,7 @@ bool fused_ffn(const moe_config *cfg, int64_t T) {
 }
 
 // The experts' FFN on dispatched rows, whichever kernels suit the batch:
-// the one-kernel FFN for BF16 and for FP8 groups averaging fewer than 16
+// the one-kernel FFN for BF16 and for FP8 groups averaging fewer than 32
 // rows, else the gate/up GEMM with its SwiGLU epilogue and the down GEMM.
 // All choices give the same result bits.
 int experts_forward(bool fp8, int groups, int hidden, int inter, int rows, const void *xp,
@@ -105,7 +109,7 @@ int experts_forward(bool fp8, int groups, int hidden, int inter, int rows, const
                     const float *w13_scales, const void *w2, const float *w2_scales,
                     bool tiled, void *h, float *h_scales, float *y, int32_t *sched,
                     bool sched_zeroed, int32_t *status, cudaStream_t s) {
-    if (!fp8 || (int64_t)rows < 16 * (int64_t)groups)
+    if (!fp8 || (int64_t)rows < kWideRowsPerGroup * (int64_t)groups)
         return launch_expert_ffn(fp8, groups, hidden, inter, rows, xp, xp_scales, offsets, w13,
                                  w13_scales, w2, w2_scales, tiled, h, h_scales, y, sched,
                                  sched_zeroed, status, s);
