@@ -38,6 +38,24 @@ def test_every_declared_symbol_is_exported(L):
         assert hasattr(L, n), f"{n} declared in the header but not exported"
 
 
+def test_error_detail_is_a_thread_local_text(L):
+    """moe_last_error_detail names the CUDA call behind a MOE_ERR_CUDA; a thread
+    that has seen none reads an empty text (argument errors do not set it)."""
+    import threading
+    cfg = moe.make_config(synth.CONFIGS["r1_mini"])
+    seen = []
+
+    def fresh_thread():
+        assert L.moe_route(ctypes.byref(cfg), 4, None, None, None, None, None, None, None, None,
+                           None, None) == -1
+        seen.append(moe.last_error_detail())
+
+    t = threading.Thread(target=fresh_thread)
+    t.start()
+    t.join()
+    assert seen == [""]
+
+
 def test_status_strings(L):
     assert moe.status_string(0) == "ok"
     for code in (-1, -2, -3, -4, -5, -6):
@@ -154,6 +172,18 @@ def test_bad_arguments_are_rejected_before_launch(L):
                             fake, 0, fake, fake, fake, fake, need, None, None) == -1
     assert L.moe_expert_ffn(ctypes.byref(r1), 257, 0, None, None, None, None, None, None, None,
                             0, None, None, None, None, 0, None, None) == 0
+    # the experts' FFN with the layer's choice of kernels: the same checks
+    fwd = lambda c, groups, rows, nbytes, layout=0: L.moe_experts_forward(
+        ctypes.byref(c), groups, rows, fake, fake, fake, fake, fake, fake, fake, layout, fake,
+        fake, fake, fake, nbytes, None, None)
+    assert fwd(r1, 257, 1152, need - 4) == -3
+    assert fwd(r1, 0, 10, need) == -1
+    assert fwd(r1, 2000, 10, 1 << 20) == -2
+    assert fwd(r1, 257, 1152, need, layout=5) == -1
+    assert L.moe_experts_forward(ctypes.byref(r1), 257, 1152, fake, None, fake, fake, fake, fake,
+                                 fake, 0, fake, fake, fake, fake, need, None, None) == -1
+    assert L.moe_experts_forward(ctypes.byref(r1), 257, 0, None, None, None, None, None, None,
+                                 None, 0, None, None, None, None, 0, None, None) == 0
     # the FFN flag self-test needs its scratch
     n = L.moe_selftest_ffn_flag_timeout_scratch_bytes()
     assert 0 < n < (1 << 20)

@@ -55,6 +55,35 @@ def test_logits_one_hot_and_ragged_hidden(oracle_lib):
         assert np.array_equal(l[0], w[:, h])
 
 
+def test_logits_summation_order_by_absorption(oracle_lib):
+    """The fixed summation order, pinned by fp32 absorption (2^24 + 1 rounds to
+    2^24): each case's value is worked out by hand for the order the routing
+    reading fixes -- hidden index h in lane slice (h/8) mod 32, each slice
+    summed in increasing h, the 32 slices meeting in an xor butterfly
+    (16, 8, 4, 2, 1) -- and differs under the plausible alternatives."""
+    H, big = 1024, 2.0 ** 24
+
+    def logit(products):
+        x = np.zeros((1, H), np.float32)
+        w = np.zeros((1, H), np.float32)
+        for h, p in products.items():
+            x[0, h], w[0, h] = 1.0, p        # bf16-exact values
+        return float(routing.gate_logits(_bits(x), _bits(w))[0, 0])
+
+    # three slices (lanes 0, 1, 2): the butterfly adds lane 2 to lane 0 (2^24 - 2^24)
+    # before lane 1 joins: 1; summed in increasing h it would be (2^24 + 1) - 2^24 = 0
+    assert logit({0: big, 8: 1.0, 16: -big}) == 1.0
+    # one slice, increasing h: 2^24 absorbs each 1; in decreasing h, 1 + 1 + 2^24
+    assert logit({0: big, 1: 1.0, 2: 1.0}) == big
+    assert logit({2: big, 1: 1.0, 0: 1.0}) == big + 2.0
+    # slices of 8 consecutive elements: h = 0, 1 share lane 0 (the 1 is absorbed)
+    # and h = 32 is lane 4: 0; with h mod 32 lanes, h = 0 and 32 would cancel in
+    # lane 0 and the 1 would survive in lane 1
+    assert logit({0: big, 1: 1.0, 32: -big}) == 0.0
+    # h = 256 returns to lane 0 after h = 0..255: (2^24 + 1) absorbed, then -2^24
+    assert logit({0: big, 256: 1.0, 512: -big}) == 0.0
+
+
 def test_logits_within_fp32_bound_of_fp64_dot(oracle_lib):
     rng = np.random.default_rng(2)
     T, E, H = 6, 16, 7168
