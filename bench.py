@@ -153,8 +153,9 @@ def setup(shape, seed, device):
 class Stepper:
     """The hot path as its C-ABI steps on one stream, CUDA events around each."""
 
-    NAMES_FUSED = ["route", "quant_x", "permute", "expert_ffn", "combine"]
-    NAMES_WIDE = ["route", "quant_x", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
+    # "route" includes the FP8 quantisation of x (done by the selection kernel)
+    NAMES_FUSED = ["route", "permute", "expert_ffn", "combine"]
+    NAMES_WIDE = ["route", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
 
     def __init__(self, layer, x, out):
         import torch
@@ -180,7 +181,7 @@ class Stepper:
         self.events = []
         self.top_events = []
 
-    TOP = 3   # stage index of the dominant kernel (expert FFN, or the gate/up GEMM alone)
+    TOP = 2   # stage index of the dominant kernel (expert FFN, or the gate/up GEMM alone)
 
     def step(self, record=None):
         """One pass of the layer.  record="all": CUDA events between all stages
@@ -202,11 +203,13 @@ class Stepper:
                 ev.append(e)
 
         mark()
-        moe.route(cfg, T, self.x, w["wg"], w.get("e_bias"), w.get("logit_offset"),
-                  w.get("log2phys"), p["logits"], p["topk_ids"], p["topk_w"], p["status"])
-        mark()
         if self.fp8:
-            moe.act_requant(cfg, moe.ACT_IDENTITY, T, self.x, p["xq"], p["xs"])
+            moe.route_quantize(cfg, T, self.x, w["wg"], w.get("e_bias"), w.get("logit_offset"),
+                               w.get("log2phys"), p["logits"], p["topk_ids"], p["topk_w"],
+                               p["xq"], p["xs"], p["status"])
+        else:
+            moe.route(cfg, T, self.x, w["wg"], w.get("e_bias"), w.get("logit_offset"),
+                      w.get("log2phys"), p["logits"], p["topk_ids"], p["topk_w"], p["status"])
         mark()
         moe.permute(cfg, T, p["topk_ids"], p["xq"] if self.fp8 else self.x,
                     p["xs"] if self.fp8 else None, p["expert_offsets"], p["src_of_row"],

@@ -132,6 +132,20 @@ MOE_API int moe_route(const moe_config *cfg, int32_t T, const void *x, const voi
               float *logits, int32_t *topk_ids, float *topk_w,
               int32_t *dev_status, void *stream);
 
+/* moe_route followed by the FP8 quantisation of x (moe_act_requant with
+ * MOE_ACT_IDENTITY) in the launches of moe_route alone: the selection kernel
+ * quantises each token's row while the gate logits are computed.  The same
+ * results, bit for bit, as the two calls.  FP8 layers only (else
+ * MOE_ERR_INVALID_ARG).  xq e4m3 [T, hidden] and xs fp32 [T, hidden/128]
+ * (device, caller-owned); other arguments as moe_route.  x must not change
+ * until the call's kernels have run (it is read while the logits are
+ * computed). */
+MOE_API int moe_route_quantize(const moe_config *cfg, int32_t T, const void *x, const void *w_gate,
+                               const float *e_bias, const float *logit_offset,
+                               const int32_t *log2phys, float *logits, int32_t *topk_ids,
+                               float *topk_w, void *xq, float *xs, int32_t *dev_status,
+                               void *stream);
+
 /* ---- activation quantisation ----------------------------------------------
  * mode MOE_ACT_IDENTITY (FP8 layers): in bf16 [rows, H] -> out e4m3 [rows, H]
  *   and out_scales fp32 [rows, H/128]: per row and 128-column group,
@@ -324,7 +338,8 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
                 int32_t out_dtype, void *stream);
 
 /* ---- the whole layer -------------------------------------------------------------
- * route -> (FP8: quantise x) -> permute -> the experts' FFN -> combine, all
+ * route (FP8: with the quantisation of x, as moe_route_quantize) -> permute
+ * -> the experts' FFN -> combine, all
  * on `stream`.  The experts' FFN is
  *   BF16, and FP8 with groups averaging fewer than 32 rows (decode):
  *     moe_expert_ffn (one persistent kernel);

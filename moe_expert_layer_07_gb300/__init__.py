@@ -13,7 +13,8 @@ import os
 
 from ._build import LIB as LIB_PATH
 
-__all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "act_requant",
+__all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "route_quantize",
+           "act_requant",
            "permute", "permute_workspace_size", "permute_static_scratch", "grouped_gemm", "combine", "layer_forward",
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
            "last_error_detail",
@@ -70,6 +71,7 @@ _CP = ctypes.POINTER(Config)
 _SIGS = {
     "moe_route": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_act_requant": [_CP, _I, _I, _P, _P, _P, _P, _P],
+    "moe_route_quantize": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute_workspace_size": [_CP, _I, ctypes.POINTER(ctypes.c_size_t)],
     "moe_permute": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
     "moe_grouped_gemm": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P],
@@ -172,6 +174,15 @@ def route(cfg: Config, T, x, w_gate, e_bias, logit_offset, log2phys, logits, top
     _check(lib().moe_route(ctypes.byref(cfg), T, _ptr(x), _ptr(w_gate), _ptr(e_bias),
                            _ptr(logit_offset), _ptr(log2phys), _ptr(logits), _ptr(topk_ids),
                            _ptr(topk_w), _ptr(status), _stream(stream)), "moe_route")
+
+
+def route_quantize(cfg: Config, T, x, w_gate, e_bias, logit_offset, log2phys, logits, topk_ids,
+                   topk_w, xq, xs, status=None, stream=None):
+    """moe_route and the FP8 quantisation of x in the selection kernel (FP8 layers)."""
+    _check(lib().moe_route_quantize(ctypes.byref(cfg), T, _ptr(x), _ptr(w_gate), _ptr(e_bias),
+                                    _ptr(logit_offset), _ptr(log2phys), _ptr(logits),
+                                    _ptr(topk_ids), _ptr(topk_w), _ptr(xq), _ptr(xs),
+                                    _ptr(status), _stream(stream)), "moe_route_quantize")
 
 
 def act_requant(cfg: Config, mode, rows, inp, out, out_scales=None, rows_dev=None, stream=None):

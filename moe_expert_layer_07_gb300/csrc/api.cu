@@ -190,6 +190,23 @@ int moe_route(const moe_config *cfg, int32_t T, const void *x, const void *w_gat
                         topk_w, dev_status, static_cast<cudaStream_t>(stream));
 }
 
+int moe_route_quantize(const moe_config *cfg, int32_t T, const void *x, const void *w_gate,
+                       const float *e_bias, const float *logit_offset, const int32_t *log2phys,
+                       float *logits, int32_t *topk_ids, float *topk_w, void *xq, float *xs,
+                       int32_t *dev_status, void *stream) {
+    Range range("moe_route_quantize");
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (cfg->dtype != MOE_DTYPE_FP8_BLOCK128 || T < 0) return MOE_ERR_INVALID_ARG;
+    if (T == 0) return MOE_OK;
+    if (!x || !w_gate || !logits || !topk_ids || !topk_w || !xq || !xs) return MOE_ERR_INVALID_ARG;
+    if (!al16(x) || !al16(w_gate) || !al16(xq)) return MOE_ERR_INVALID_ARG;
+    if (e_bias && cfg->scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+    return launch_route(cfg, T, x, w_gate, e_bias, logit_offset, log2phys, logits, topk_ids,
+                        topk_w, dev_status, static_cast<cudaStream_t>(stream), nullptr,
+                        static_cast<uint8_t *>(xq), xs);
+}
+
 int moe_act_requant(const moe_config *cfg, int32_t mode, int32_t rows, const int32_t *rows_dev,
                     const void *in, void *out, float *out_scales, void *stream) {
     Range range("moe_act_requant");
@@ -385,10 +402,11 @@ int moe_workspace_size(const moe_config *cfg, size_t *bytes) {
 int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
     if (check_config(cfg) || T <= 0) return 0;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
-    // route, (quantise x), permute, the experts' FFN (one fused kernel, or
-    // gate/up GEMM with SwiGLU + down GEMM), combine
+    // route (with the FP8 quantisation of x), permute, the experts' FFN (one
+    // fused kernel, or gate/up GEMM with SwiGLU + down GEMM), combine
+    (void)fp8;
     const int ffn = fused_ffn(cfg, T) ? 1 : 2;
-    return route_kernel_count() + (fp8 ? 1 : 0) + permute_kernel_count(cfg, T) + ffn + 1;
+    return route_kernel_count() + permute_kernel_count(cfg, T) + ffn + 1;
 }
 
 int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, const void *x,
@@ -450,21 +468,17 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
         pf.bytes = H < 1536 ? H : 1536;
         pf.tiled = tiled;
     }
+    // FP8: the selection kernel also quantises x (while the logits run)
+    const void *rows_src = fp8 ? static_cast<const void *>(base + L.xq) : x;
+    const float *rows_scales = fp8 ? reinterpret_cast<const float *>(base + L.xs) : nullptr;
     {
         Range r("route");
         rc = launch_route(cfg, T, x, w->w_gate, w->e_bias, w->logit_offset, w->log2phys, logits,
-                          ids, tw, status, s, fused ? &pf : nullptr);
+                          ids, tw, status, s, fused ? &pf : nullptr,
+                          fp8 ? base + L.xq : nullptr,
+                          fp8 ? reinterpret_cast<float *>(base + L.xs) : nullptr);
     }
     if (rc) return rc;
-    const void *rows_src = x;
-    const float *rows_scales = nullptr;
-    if (fp8) {
-        rc = launch_act_requant(cfg, MOE_ACT_IDENTITY, T, nullptr, x, base + L.xq,
-                                reinterpret_cast<float *>(base + L.xs), s);
-        if (rc) return rc;
-        rows_src = base + L.xq;
-        rows_scales = reinterpret_cast<const float *>(base + L.xs);
-    }
     {
         Range r("dispatch");
         rc = launch_permute(cfg, T, ids, rows_src, rows_scales, offsets, src, ros, base + L.xp,

@@ -42,10 +42,13 @@ struct L2Prefetch {
     int hidden = 0, inter = 0, groups = 0, units = 0, bytes = 0;
     int tiled = 0;                  // MOE_LAYOUT_TILES: the K prefix of a row block is contiguous
 };
+// With xq and xs (FP8 layers), the selection kernel also quantises x
+// (e4m3 [T, H] + scales [T, H/128]) while the logits are computed.
 int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate,
                  const float *e_bias, const float *logit_offset, const int32_t *log2phys,
                  float *logits, int32_t *topk_ids, float *topk_w, int32_t *status,
-                 cudaStream_t s, const L2Prefetch *pf = nullptr);
+                 cudaStream_t s, const L2Prefetch *pf = nullptr, uint8_t *xq = nullptr,
+                 float *xs = nullptr);
 int launch_act_requant(const moe_config *cfg, int mode, int rows, const int32_t *rows_dev,
                        const void *in, void *out, float *out_scales, cudaStream_t s);
 size_t permute_scratch_bytes(const moe_config *cfg, int T);

@@ -22,4 +22,46 @@ __device__ __forceinline__ uint8_t fp8_code(float v, float scale) {
     return (uint8_t)__nv_cvt_float_to_fp8(__fdiv_rn(v, scale), __NV_SATFINITE, __NV_E4M3);
 }
 
+// FP8 quantisation of one 256-column segment of a bf16 row by one warp:
+// lanes 0-15 take 128-column group 2 seg, lanes 16-31 group 2 seg + 1, 8
+// consecutive values per lane.  Each group's scale is its amax / 448 and each
+// value's code e4m3_rn_sat(v / scale) (IEEE division).  Columns at or past H
+// (a multiple of 128) are skipped.
+__device__ __forceinline__ void quant_row_segment(const uint16_t *__restrict__ in_row,
+                                                  uint8_t *__restrict__ out_row,
+                                                  float *__restrict__ scales_row, int seg,
+                                                  int lane, int H) {
+    const int col = seg * 256 + lane * 8;
+    const bool active = col < H;
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (active) v = *reinterpret_cast<const uint4 *>(in_row + col);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {   // bf16 -> fp32 is exact: the bits move up 16 places
+        f[2 * j] = __uint_as_float(w[j] << 16);
+        f[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    const float sc = fp8_group_scale(amax);
+    if (!active) return;
+    uint32_t q[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const uint16_t lo = (uint16_t)__nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(f[4 * h], sc), __fdiv_rn(f[4 * h + 1], sc)), __NV_SATFINITE,
+            __NV_E4M3);
+        const uint16_t hi = (uint16_t)__nv_cvt_float2_to_fp8x2(
+            make_float2(__fdiv_rn(f[4 * h + 2], sc), __fdiv_rn(f[4 * h + 3], sc)), __NV_SATFINITE,
+            __NV_E4M3);
+        q[h] = (uint32_t)lo | ((uint32_t)hi << 16);
+    }
+    *reinterpret_cast<uint2 *>(out_row + col) = make_uint2(q[0], q[1]);
+    if ((lane & 15) == 0) scales_row[col / 128] = sc;
+}
+
 }  // namespace moe

@@ -16,9 +16,6 @@
 namespace moe {
 namespace {
 
-__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
-
 // two fp32 -> two e4m3 codes (round to nearest even, saturate to +-448)
 __device__ __forceinline__ uint16_t e4m3x2(float lo, float hi) {
     return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
@@ -38,26 +35,7 @@ __global__ void __launch_bounds__(256)
     const int seg = (int)(warp % segs);
     const int nrows = rows_dev ? min(rows, max(0, *rows_dev)) : rows;
     if (row >= nrows) return;
-    const int col = seg * 256 + lane * 8;
-    const bool active = col < H;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (active) v = *reinterpret_cast<const uint4 *>(in + row * H + col);
-    const float f[8] = {bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y),
-                        bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w)};
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-#pragma unroll
-    for (int o = 8; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sc = fp8_group_scale(amax);
-    if (!active) return;
-    uint2 q;
-    q.x = (uint32_t)e4m3x2(__fdiv_rn(f[0], sc), __fdiv_rn(f[1], sc)) |
-          ((uint32_t)e4m3x2(__fdiv_rn(f[2], sc), __fdiv_rn(f[3], sc)) << 16);
-    q.y = (uint32_t)e4m3x2(__fdiv_rn(f[4], sc), __fdiv_rn(f[5], sc)) |
-          ((uint32_t)e4m3x2(__fdiv_rn(f[6], sc), __fdiv_rn(f[7], sc)) << 16);
-    *reinterpret_cast<uint2 *>(out + row * H + col) = q;
-    if ((lane & 15) == 0) scales[row * (H / 128) + col / 128] = sc;
+    quant_row_segment(in + row * H, out + row * H, scales + row * (H / 128), seg, lane, H);
 }
 
 // One warp per (row, 128-wide group of h); each lane 4 consecutive values.

@@ -27,6 +27,7 @@
 #include <mutex>
 
 #include "internal.h"
+#include "numerics.cuh"
 #include "ptx.cuh"
 
 namespace moe {
@@ -214,6 +215,11 @@ struct SelectArgs {
     int32_t *ids;
     float *w;
     int32_t *status;
+    // optional: the FP8 quantisation of x (xq e4m3 [T, H], xs [T, H/128])
+    const uint16_t *x;
+    uint8_t *xq;
+    float *xs;
+    int H;
 };
 
 // warp-wide arg-max with ties to the lower index; every lane gets the result
@@ -239,6 +245,16 @@ template <int PL>   // experts per lane of warp 0: e = q*32 + lane, q < PL
 __global__ void __launch_bounds__(kSelThreads) route_select_kernel(const SelectArgs a) {
     __shared__ float sh_l[PL * 32], sh_s[PL * 32], sh_sel[PL * 32];
     ptx::pdl_launch_dependents();
+    if (a.xq && (int)blockIdx.x < a.T) {
+        // this token's row of x to FP8, while the gate logits are still being
+        // computed: x is the call's input (complete before the logit kernel,
+        // a full-dependency launch, started), not a previous kernel's output
+        const size_t t0 = blockIdx.x;
+        const int segs = (a.H + 255) / 256;
+        for (int seg = threadIdx.x >> 5; seg < segs; seg += kSelThreads / 32)
+            quant_row_segment(a.x + t0 * a.H, a.xq + t0 * a.H, a.xs + t0 * (a.H / 128), seg,
+                              threadIdx.x & 31, a.H);
+    }
     ptx::pdl_wait();   // logits of the previous kernel
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x;
@@ -446,7 +462,7 @@ int route_kernel_count() { return 2; }
 int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate,
                  const float *e_bias, const float *logit_offset, const int32_t *log2phys,
                  float *logits, int32_t *topk_ids, float *topk_w, int32_t *status,
-                 cudaStream_t s, const L2Prefetch *pf) {
+                 cudaStream_t s, const L2Prefetch *pf, uint8_t *xq, float *xs) {
     if (T == 0) return MOE_OK;
     const int E = cfg->num_experts, H = cfg->hidden;
     const dim3 grid((unsigned)ceil_div(T, kCT), (unsigned)ceil_div(E, kCE));
@@ -457,12 +473,12 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
     MOE_CUDA_TRY(cudaGetDevice(&dev));
     if (dev < 0 || dev >= 64) return cuda_fail("device ordinal beyond 63");
     std::call_once(attr_once[dev], [&] {
-        attr_rc[dev] = (int)cudaFuncSetAttribute(gate_logits_kernel<4>,
-                                            cudaFuncAttributeMaxDynamicSharedMemorySize, smem) ==
-                               cudaSuccess &&
-                               cudaFuncSetAttribute(gate_logits_kernel<8>,
-                                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                    smem);
+        cudaError_t e = cudaFuncSetAttribute(gate_logits_kernel<4>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(gate_logits_kernel<8>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        attr_rc[dev] = (int)e;
     });
     if (attr_rc[dev]) return cuda_fail("cudaFuncSetAttribute", (cudaError_t)attr_rc[dev]);
     const L2Prefetch none;
@@ -497,6 +513,10 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
     a.ids = topk_ids;
     a.w = topk_w;
     a.status = status;
+    a.x = static_cast<const uint16_t *>(x);
+    a.xq = xq;
+    a.xs = xs;
+    a.H = H;
     const int pl = (int)ceil_div(E, 32);
     int rc;
     if (pl <= 1) rc = launch_select<1>(a, s);

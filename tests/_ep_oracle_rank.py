@@ -29,16 +29,26 @@ class OracleRank:
         logits = orouting.gate_logits(x_bits, n["wg_bits"], n.get("logit_offset"))
         phys, w, _ = orouting.route(logits, s, n.get("e_bias"), n.get("log2phys"))
         off, src, ros = opermute.permute(phys, E, S)
-        xq, xs = oquant.quant_groups_fp8(oquant.bf16_from_bits(x_bits))
         tok = opermute.token_of_slot(src, T, k)
+        if self.fp8:
+            xq, xs = oquant.quant_groups_fp8(oquant.bf16_from_bits(x_bits))
+            rows = dict(xp=torch.from_numpy(np.ascontiguousarray(xq[tok])),
+                        xps=torch.from_numpy(np.ascontiguousarray(xs[tok])))
+        else:   # bf16 rows travel as their bytes
+            xq, xs = np.ascontiguousarray(x_bits, np.uint16), None
+            rows = dict(xp=torch.from_numpy(np.ascontiguousarray(xq[tok]).view(np.uint8)))
         d = dict(ids=phys, w=w, ros=ros, src=src, xq=xq, xs=xs,
-                 xp=torch.from_numpy(np.ascontiguousarray(xq[tok])),
-                 xps=torch.from_numpy(np.ascontiguousarray(xs[tok])),
-                 y=torch.zeros((len(src), s.hidden), dtype=torch.float64))
+                 y=torch.zeros((len(src), s.hidden), dtype=torch.float64), **rows)
         return StepState(T=T, offsets=off, tensors=d)
+
+    @property
+    def fp8(self):
+        return self.shape.dtype == "fp8"
 
     def new_rows(self, nrows):
         H = self.shape.hidden
+        if not self.fp8:
+            return {"xp": torch.empty((nrows, 2 * H), dtype=torch.uint8)}
         return {"xp": torch.empty((nrows, H), dtype=torch.uint8),
                 "xps": torch.empty((nrows, H // 128), dtype=torch.float32)}
 
@@ -49,15 +59,18 @@ class OracleRank:
         return st.tensors["y"][:R]
 
     def local_experts(self, plan, local_ids, bufs):
-        self.received = {"local_ids": local_ids.copy(), "xp": bufs["xp"].numpy().copy(),
-                         "xps": bufs["xps"].numpy().copy()}
+        xp = bufs["xp"].numpy()
+        if not self.fp8:
+            xp = np.ascontiguousarray(xp).view(np.uint16)
+        xps = bufs["xps"].numpy() if self.fp8 else None
+        self.received = {"local_ids": local_ids.copy(), "xp": xp.copy(),
+                         "xps": None if xps is None else xps.copy()}
         n, H = len(local_ids), self.shape.hidden
         y = np.zeros((n, H), dtype=np.float64)
-        xp, xps = bufs["xp"].numpy(), bufs["xps"].numpy()
         for j in np.unique(local_ids):
             rows = np.nonzero(local_ids == j)[0]
             e = plan.rank * plan.m + int(j)                   # physical expert
-            y[rows] = self._ffn(e, xp[rows], xps[rows])
+            y[rows] = self._ffn(e, xp[rows], None if xps is None else xps[rows])
         return torch.from_numpy(y)
 
     def finish(self, st, out):
@@ -72,6 +85,8 @@ class OracleRank:
 
     def _ffn(self, e, xq, xs):
         n = self.np
+        if not self.fp8:
+            return olayer.expert_ffn(self.shape, xq, n["w13"][e], n["w2"][e])
         return olayer.expert_ffn(self.shape, xq, n["w13"][e], n["w2"][e], n["w13_s"][e],
                                  n["w2_s"][e], xs)
 

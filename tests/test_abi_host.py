@@ -84,14 +84,14 @@ def test_workspace_size_r1_decode(L):
 
 
 def test_layer_kernel_counts(L):
-    # route (2) + quantise x + permute (2 for at most 1024 routed slots, else 3)
-    # + experts' FFN + combine
+    # route (2, the FP8 quantisation of x inside) + permute (2 for at most 1024
+    # routed slots, else 3) + experts' FFN + combine
     r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
-    assert moe.layer_kernel_count(r1, 128) == 7        # one-kernel FFN, 1024 slots
-    assert moe.layer_kernel_count(r1, 129) == 8        # 1032 slots: count and scan apart
-    assert moe.layer_kernel_count(r1, 4096) == 9       # wide: SwiGLU GEMM, down GEMM
+    assert moe.layer_kernel_count(r1, 128) == 6        # one-kernel FFN, 1024 slots
+    assert moe.layer_kernel_count(r1, 129) == 7        # 1032 slots: count and scan apart
+    assert moe.layer_kernel_count(r1, 4096) == 8       # wide: SwiGLU GEMM, down GEMM
     mini = moe.make_config(synth.CONFIGS["r1_mini"])   # inter 384: odd K blocks of W2
-    assert moe.layer_kernel_count(mini, 37) == 7
+    assert moe.layer_kernel_count(mini, 37) == 6
     b16 = moe.make_config(synth.CONFIGS["bf16_mini"])   # BF16: one-kernel FFN
     assert moe.layer_kernel_count(b16, 29) == 6
     assert moe.layer_kernel_count(r1, 0) == 0
@@ -133,8 +133,14 @@ def test_bad_arguments_are_rejected_before_launch(L):
     need = moe.permute_workspace_size(cfg, 37)
     assert L.moe_permute(ctypes.byref(cfg), 37, fake, fake, fake, fake, fake, fake, fake, fake,
                          fake, need - 1, None, None) == -3
-    # identity quantisation needs an FP8 layer; unknown enums
+    # identity quantisation (alone or with routing) needs an FP8 layer; unknown enums
     b16 = moe.make_config(synth.CONFIGS["bf16_mini"])
+    assert L.moe_route_quantize(ctypes.byref(b16), 4, fake, fake, None, None, None, fake, fake,
+                                fake, fake, fake, None, None) == -1
+    assert L.moe_route_quantize(ctypes.byref(cfg), 4, fake, fake, None, None, None, fake, fake,
+                                fake, None, fake, None, None) == -1
+    assert L.moe_route_quantize(ctypes.byref(cfg), 0, None, None, None, None, None, None, None,
+                                None, None, None, None, None) == 0
     assert L.moe_act_requant(ctypes.byref(b16), moe.ACT_IDENTITY, 4, None, fake, fake, fake,
                              None) == -1
     assert L.moe_act_requant(ctypes.byref(cfg), 7, 4, None, fake, fake, fake, None) == -1

@@ -85,12 +85,13 @@ def _run(name, world, ranges):
         return dict(results)
 
 
-@pytest.mark.parametrize("world,ranges", [(2, [(0, 20), (20, 37)]),
-                                          (4, [(0, 1), (1, 12), (12, 30), (30, 37)])])
-def test_expert_parallel_step_matches_the_oracle(oracle_lib, world, ranges):
+@pytest.mark.parametrize("name,world,ranges", [
+    ("r1_mini", 2, [(0, 20), (20, 37)]),
+    ("r1_mini", 4, [(0, 1), (1, 12), (12, 30), (30, 37)]),
+    ("bf16_mini", 2, [(0, 11), (11, 29)])])        # BF16, two shared experts, top-3
+def test_expert_parallel_step_matches_the_oracle(oracle_lib, name, world, ranges):
     from oracle import layer as olayer
     from oracle import permute as opermute
-    name = "r1_mini"
     res = _run(name, world, ranges)
     shape, npin = _inputs(name, world)
     full = olayer.layer_forward(shape, npin)      # routing of every token, all outputs
@@ -115,18 +116,22 @@ def test_expert_parallel_step_matches_the_oracle(oracle_lib, world, ranges):
             for j in range(m):
                 e = r * m + j
                 tt, _ = np.nonzero(ids_s == e)          # slot order: t, then j
-                exp_codes.append(full["xq"][sa + tt])
-                exp_scales.append(full["xs"][sa + tt])
+                if shape.dtype == "fp8":
+                    exp_codes.append(full["xq"][sa + tt])
+                    exp_scales.append(full["xs"][sa + tt])
+                else:
+                    exp_codes.append(npin["x_bits"][sa + tt])
                 exp_ids.append(np.full(len(tt), j, np.int32))
         rec = got["received"]
         assert np.array_equal(rec["local_ids"], np.concatenate(exp_ids))
         assert np.array_equal(rec["xp"], np.concatenate(exp_codes))
-        assert np.array_equal(rec["xps"], np.concatenate(exp_scales))
+        if shape.dtype == "fp8":
+            assert np.array_equal(rec["xps"], np.concatenate(exp_scales))
         # the rank's output against the oracle layer on its tokens
         ref = full["out"][a:b]
         err = np.abs(got["out"] - ref).max()
         rms = np.sqrt(np.mean(full["out"] ** 2))
-        assert err <= FP8_TOL * rms
+        assert err <= (FP8_TOL if shape.dtype == "fp8" else 5e-3) * rms
         assert err <= 1e-9 * rms    # same computation, different summation of rows
     # the balanced permutation spreads the routed rows evenly over the ranks
     loads = [int(res[r]["recv"].sum()) for r in range(world)]

@@ -7,7 +7,8 @@ has drained, so no kernel ever waits on another rank's kernel.
 Every rank's output must equal the single-GPU layer (moe_layer_forward) on
 the same tokens bit for bit: a row's FFN result does not depend on which
 rows share its tile, whether the rank's expert groups take the one-kernel
-FFN (few rows per group) or the wide GEMMs (37 tokens against 200 below).
+FFN (few rows per group) or the wide GEMMs (37 tokens against 200 below),
+and in a BF16 layer with two shared experts.
 """
 import threading
 
@@ -83,9 +84,10 @@ def _balanced(shape, inp):
     return counts
 
 
-@pytest.mark.parametrize("T,world", [(37, 2), (37, 4), (200, 2)])
-def test_expert_parallel_ranks_equal_the_single_gpu_layer(lib, T, world):
-    shape = synth.CONFIGS["r1_mini"].with_tokens(T)
+@pytest.mark.parametrize("name,T,world", [("r1_mini", 37, 2), ("r1_mini", 37, 4),
+                                          ("r1_mini", 200, 2), ("bf16_mini", 29, 2)])
+def test_expert_parallel_ranks_equal_the_single_gpu_layer(lib, name, T, world):
+    shape = synth.CONFIGS[name].with_tokens(T)
     inp = synth.make_inputs(shape, seed=5, device="cuda")
     # one balanced expert set per rank, weights re-laid in that order
     l2p, p2l, _ = moe.balance_permutation(_balanced(shape, inp), world)
@@ -130,3 +132,52 @@ def test_expert_parallel_ranks_equal_the_single_gpu_layer(lib, T, world):
         for s in range(world):
             assert np.array_equal(recs[r]["recv_counts"][s], recs[s]["send_counts"][r])
     assert ref_layer.status() == 0
+
+
+def _nccl_rank(port, results):
+    import os
+    import torch
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    torch.cuda.set_device(0)
+    dist.init_process_group("nccl", rank=0, world_size=1)
+    try:
+        import moe_expert_layer_07_gb300 as moe
+        import synth
+        from moe_expert_layer_07_gb300 import _build
+        from moe_expert_layer_07_gb300.ep import DistExchange, EPPlan, GpuRank, ep_forward, split_weights
+        _build.build()
+        shape = synth.CONFIGS["r1_mini"]
+        inp = synth.make_inputs(shape, seed=6, device="cuda")
+        plan = EPPlan(shape.num_experts, 1, 0)
+        ops = GpuRank(shape, split_weights(inp, plan, shape.num_shared), plan)
+        out = torch.full((shape.tokens, shape.hidden), float("nan"), device="cuda")
+        rec = ep_forward(ops, plan, DistExchange(device="cuda"), inp["x"], out)
+        ref = torch.full_like(out, float("nan"))
+        moe.MoELayer(shape, inp).forward(inp["x"], ref)
+        torch.cuda.synchronize()
+        results["equal"] = bool(torch.equal(out, ref))
+        results["rows"] = (rec["rows_sent"], rec["rows_received"])
+        results["status"] = int(ops.status.item())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_dist_exchange_over_nccl_single_rank(lib):
+    """ep_forward over a real NCCL process group (one rank, one GPU: each
+    all-to-all is a copy to itself) gives the single-GPU layer's bits; the
+    calls are those a multi-GPU run makes."""
+    import os
+    import torch.multiprocessing as mp
+    port = 29700 + os.getpid() % 1000
+    ctx = mp.get_context("spawn")
+    with ctx.Manager() as m:
+        results = m.dict()
+        p = ctx.Process(target=_nccl_rank, args=(port, results))
+        p.start()
+        p.join(timeout=600)
+        assert p.exitcode == 0
+        res = dict(results)
+    assert res["equal"] and res["status"] == 0
+    s = synth.CONFIGS["r1_mini"]
+    assert res["rows"] == (s.tokens * s.top_k, s.tokens * s.top_k)

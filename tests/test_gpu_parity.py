@@ -123,6 +123,39 @@ def test_quant_x_bit_exact(lib, name):
     assert fp8_codes_equal(q, rq) and np.array_equal(sc, rs)
 
 
+@pytest.mark.parametrize("name,T", [("r1_mini", None), ("r1_decode_t128", None),
+                                    ("r1_prefill_t4096", None), ("r1_mini", 1)])
+def test_route_quantize_equals_route_then_quantize(lib, name, T):
+    """Routing with the x quantisation in the selection kernel (the layer's own
+    launch sequence) gives the bits of moe_route followed by moe_act_requant."""
+    wl = workload(name, T=T)
+    s = wl.shape
+    T = s.tokens
+    cfg = moe.make_config(s)
+    dev = wl.dev
+    l2p = None if wl.log2phys is None else torch.as_tensor(wl.log2phys, device="cuda")
+    outs = []
+    for fused in (False, True):
+        logits = torch.full((T, s.num_experts), float("nan"), device="cuda")
+        ids = torch.full((T, s.top_k), -7, dtype=torch.int32, device="cuda")
+        w = torch.full((T, s.top_k), float("nan"), device="cuda")
+        xq = torch.full((T, s.hidden), 0x55, dtype=torch.uint8, device="cuda")
+        xs = torch.full((T, s.hidden // 128), -1.0, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if fused:
+            moe.route_quantize(cfg, T, dev["x"], dev["wg"], dev["e_bias"], dev["logit_offset"],
+                               l2p, logits, ids, w, xq, xs, st)
+        else:
+            moe.route(cfg, T, dev["x"], dev["wg"], dev["e_bias"], dev["logit_offset"], l2p,
+                      logits, ids, w, st)
+            moe.act_requant(cfg, moe.ACT_IDENTITY, T, dev["x"], xq, xs)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        outs.append((logits, ids, w, xq, xs))
+    for a, b in zip(*outs):
+        assert torch.equal(a, b)
+
+
 def test_quant_x_ties_zeros_and_extremes(lib):
     s = synth.CONFIGS["r1_mini"]
     H = s.hidden
