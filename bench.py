@@ -432,6 +432,40 @@ def main():
     return 0
 
 
+_READ_STREAM = {}
+
+
+def read_stream_gbs(layer, device):
+    """This GPU's read-only HBM rate, GB/s: the library's stream-read utility
+    over the layer's gate/up weights (several GB, far beyond L2), best of five
+    passes; measured once per process.  None when the weights fit in L2."""
+    import torch
+    import moe_expert_layer_07_gb300 as moe
+    if "gbs" in _READ_STREAM:
+        return _READ_STREAM["gbs"]
+    w = layer._keep["w13"]
+    g = moe.stream_read_granule()
+    nbytes = (w.numel() * w.element_size()) // g * g
+    if nbytes < (1 << 30):
+        return None
+    st = torch.zeros(1, dtype=torch.int32, device=device)
+    for _ in range(3):
+        moe.stream_read(w, nbytes, st)
+    best = None
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        moe.stream_read(w, nbytes, st)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    if int(st.item()) != 0:
+        return None
+    _READ_STREAM["gbs"] = nbytes / (best * 1e-3) / 1e9
+    return _READ_STREAM["gbs"]
+
+
 def measure(shape, args, world, rank, local, device, cpu):
     """All measurements of one workload (the layer resident only meanwhile)."""
     import torch
@@ -501,6 +535,7 @@ def measure(shape, args, world, rank, local, device, cpu):
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(layer, shape, x, device, args.steps, args.warmup, world)
+    read_gbs = read_stream_gbs(layer, device)
 
     cpu_line = None
     if cpu:
@@ -523,10 +558,15 @@ def measure(shape, args, world, rank, local, device, cpu):
         "hbm_gbs": layer_bytes / (ms_step / 1e3) / 1e9,
         "layer_roofline_frac": (layer_bytes / (hbm_peak * 1e9)) / (ms_step / 1e3),
         "layer_roofline_frac_nominal": (layer_bytes / (NOMINAL_HBM_GBS * 1e9)) / (ms_step / 1e3),
+        "read_stream_gbs": read_gbs,
+        "layer_roofline_frac_read_stream": (None if not read_gbs else
+                                            (layer_bytes / (read_gbs * 1e9)) / (ms_step / 1e3)),
         "roofline_note": "headline fractions (`layer_roofline_frac`, `roofline.frac`) are of "
                          "the measured copy bandwidth (a read + write figure, which a "
-                         "read-dominated weight stream can exceed); the `_nominal` fractions "
-                         "are of the nominal 8 TB/s and stay below 1",
+                         "read-dominated weight stream can exceed); the `_read_stream` "
+                         "fractions are of this GPU's read-only rate measured in this run "
+                         "(`read_stream_gbs`: the library's stream-read utility over the "
+                         "layer's weights); the `_nominal` fractions are of the nominal 8 TB/s",
         "layer_bytes": layer_bytes,
         "path_bytes": path_total,
         "path_hbm_gbs": path_total / (ms_step / 1e3) / 1e9,
@@ -540,6 +580,8 @@ def measure(shape, args, world, rank, local, device, cpu):
                      "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
                      "frac_nominal": achieved / NOMINAL_HBM_GBS,
                      "peak_nominal": NOMINAL_HBM_GBS,
+                     "frac_read_stream": None if not read_gbs else achieved / read_gbs,
+                     "peak_read_stream": read_gbs,
                      "bytes_per_unit": unit_bytes, "units": active,
                      "work_unit": "active expert group (weights + block scales)",
                      "ms_per_launch": top_ms},

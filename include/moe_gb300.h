@@ -383,6 +383,18 @@ MOE_API const char *moe_last_error_detail(void);
 /* Number of kernels moe_layer_forward enqueues for this configuration. */
 MOE_API int moe_layer_kernel_count(const moe_config *cfg, int32_t T);
 
+/* Measurement utility (no counterpart on the pages): streams `bytes` of device
+ * memory at `src` through shared memory and discards them, so that the time
+ * of the call (timed by the caller with events on `stream`) gives this GPU's
+ * read-only HBM rate -- the denominator for kernels bound by streaming
+ * weights, which a copy (read + write) figure understates.  One CTA per SM,
+ * 64 KB bulk copies, a 3-deep ring.  src 16-byte aligned; bytes a multiple
+ * of moe_stream_read_granule() (else MOE_ERR_INVALID_ARG); nothing is written
+ * to global memory.  A bounded wait that expires sets MOE_DEV_TIMEOUT in
+ * *dev_status (may be NULL). */
+MOE_API size_t moe_stream_read_granule(void);
+MOE_API int moe_stream_read(const void *src, size_t bytes, int32_t *dev_status, void *stream);
+
 /* Self-test of the bounded waits (no counterpart on the pages: a robustness
  * check of this library).  Launches one warp that waits on a completed
  * mbarrier (must succeed) and on one nothing arrives on (must give up after

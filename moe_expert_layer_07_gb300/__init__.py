@@ -17,7 +17,7 @@ __all__ = ["Config", "Weights", "WsLayout", "lib", "make_config", "route", "rout
            "act_requant",
            "permute", "permute_workspace_size", "permute_static_scratch", "grouped_gemm", "combine", "layer_forward",
            "workspace_size", "workspace_layout", "get_device_status", "status_string",
-           "last_error_detail",
+           "last_error_detail", "stream_read", "stream_read_granule",
            "balance_permutation", "set_imbalance", "rebalance_due", "layer_kernel_count", "MoELayer", "MoEError",
            "count_expert_rows", "relayout_experts", "source_slots", "ExpertRebalancer",
            "count_coactivation", "affinity_permutation", "grouped_gemm_swiglu",
@@ -97,6 +97,7 @@ _SIGS = {
                        ctypes.c_size_t, _P, _P],
     "moe_experts_forward": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
                             ctypes.c_size_t, _P, _P],
+    "moe_stream_read": [_P, ctypes.c_size_t, _P, _P],
 }
 
 
@@ -114,6 +115,8 @@ def lib():
             fn.restype = ctypes.c_int
         L.moe_permute_static_scratch_capacity.argtypes = []
         L.moe_permute_static_scratch_capacity.restype = ctypes.c_size_t
+        L.moe_stream_read_granule.argtypes = []
+        L.moe_stream_read_granule.restype = ctypes.c_size_t
         L.moe_expert_ffn_sched_bytes.argtypes = [_I, _I]
         L.moe_expert_ffn_sched_bytes.restype = ctypes.c_size_t
         L.moe_selftest_ffn_flag_timeout_scratch_bytes.argtypes = []
@@ -320,6 +323,16 @@ def source_slots(old_log2phys, new_phys2log, num_experts: int, groups: int):
     old = np.asarray(old_log2phys, dtype=np.int64)
     new = np.asarray(new_phys2log, dtype=np.int64)
     return np.concatenate([old[new], np.arange(num_experts, groups)]).astype(np.int32)
+
+
+def stream_read(src, nbytes: int, status=None, stream=None):
+    """Reads nbytes of device memory at src through shared memory (a timing utility)."""
+    _check(lib().moe_stream_read(_ptr(src), nbytes, _ptr(status), _stream(stream)),
+           "moe_stream_read")
+
+
+def stream_read_granule() -> int:
+    return int(lib().moe_stream_read_granule())
 
 
 def workspace_size(cfg: Config) -> int:

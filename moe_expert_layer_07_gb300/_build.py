@@ -18,7 +18,7 @@ BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "route.cu", "quant.cu", "permute.cu", "gemm.cu", "gemm_wide.cu", "combine.cu",
-           "selftest.cu", "permute_static.cu", "rebalance.cu", "ffn.cu", "pack.cu",
+           "selftest.cu", "stream_read.cu", "permute_static.cu", "rebalance.cu", "ffn.cu", "pack.cu",
            "balance.cpp"]
 
 

@@ -190,6 +190,13 @@ def test_bad_arguments_are_rejected_before_launch(L):
                                  fake, 0, fake, fake, fake, fake, need, None, None) == -1
     assert L.moe_experts_forward(ctypes.byref(r1), 257, 0, None, None, None, None, None, None,
                                  None, 0, None, None, None, None, 0, None, None) == 0
+    # the read-stream utility: aligned, whole granules
+    g = L.moe_stream_read_granule()
+    assert g == 65536
+    assert L.moe_stream_read(None, g, None, None) == -1
+    assert L.moe_stream_read(P(0x1008), g, None, None) == -1
+    assert L.moe_stream_read(fake, g + 16, None, None) == -1
+    assert L.moe_stream_read(fake, 0, None, None) == 0
     # the FFN flag self-test needs its scratch
     n = L.moe_selftest_ffn_flag_timeout_scratch_bytes()
     assert 0 < n < (1 << 20)

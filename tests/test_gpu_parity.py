@@ -573,6 +573,23 @@ def test_layer_back_to_back_calls_bit_identical(lib, name, T):
         assert torch.equal(o, outs[0])
 
 
+def test_stream_read_utility(lib):
+    """The read-stream utility bench.py uses for the read-only HBM rate: a
+    1 GiB pass ends with a clear status at a plausible rate (1 to 10 TB/s)."""
+    nbytes = 1 << 30
+    buf = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.stream_read(buf, nbytes, st)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    moe.stream_read(buf, nbytes, st)
+    b.record()
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    gbs = nbytes / (a.elapsed_time(b) * 1e-3) / 1e9
+    assert 1000 < gbs < 10000, gbs
+
+
 def test_bounded_wait_reports_timeout_and_context_survives(lib):
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     res = torch.zeros(1, dtype=torch.int32, device="cuda")
