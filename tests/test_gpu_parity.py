@@ -105,6 +105,29 @@ def test_route_with_random_permutation(lib):
     assert np.array_equal(ids, phys) and np.array_equal(ids, wl.log2phys[logical])
 
 
+@pytest.mark.parametrize("name", ["r1_mini", "bf16_mini", "tiny_bf16"])
+def test_route_ties_go_to_the_lower_index(lib, name):
+    """Every odd expert's gate row (and bias) copies the even expert below it,
+    so scores tie in pairs: the selection, group scores and slot order must
+    break every tie toward the lower index, as the oracle does."""
+    shape = synth.CONFIGS[name]
+    wl = Workload(shape, seed=7)
+    for key in ("wg", "e_bias", "logit_offset"):
+        if wl.dev.get(key) is not None:
+            t = wl.dev[key].clone()
+            t[1::2] = t[0::2]
+            wl.dev[key] = t
+    wl._np = None
+    logits, ids, w, st = run_route(wl)
+    assert st == 0
+    assert np.array_equal(logits[:, 1::2], logits[:, 0::2])   # the ties are real
+    n = wl.np
+    ref_l = orouting.gate_logits(n["x_bits"], n["wg_bits"], n["logit_offset"])
+    phys, ref_w, _ = orouting.route(ref_l, shape, n["e_bias"], n.get("log2phys"))
+    assert np.array_equal(ids, phys)
+    np.testing.assert_allclose(w, ref_w, rtol=W_RTOL)
+
+
 # ------------------------------------------------------------ quantisation
 def _quant_x(cfg, x, T, H):
     q = torch.empty((T, H), dtype=torch.uint8, device="cuda")
