@@ -155,7 +155,10 @@ class Stepper:
 
     # "route" includes the FP8 quantisation of x (done by the selection kernel)
     NAMES_FUSED = ["route", "permute", "expert_ffn", "combine"]
-    NAMES_WIDE = ["route", "permute", "gemm_gate_up_swiglu", "gemm_down", "combine"]
+    # wide FP8 batches: the one-kernel FFN on the groups of at most 32 rows, the
+    # two GEMMs on the others (as moe_layer_forward splits them)
+    NAMES_WIDE = ["route", "permute", "expert_ffn", "gemm_gate_up_swiglu", "gemm_down", "combine"]
+    SMALL_GROUP_ROWS = 32
 
     def __init__(self, layer, x, out):
         import torch
@@ -181,7 +184,21 @@ class Stepper:
         self.events = []
         self.top_events = []
 
-    TOP = 2   # stage index of the dominant kernel (expert FFN, or the gate/up GEMM alone)
+    # stage index of the dominant kernel: the expert FFN, or, in wide batches,
+    # whichever of the FFN and the gate/up GEMM takes longer (set_top)
+    TOP = 2
+
+    def set_top(self):
+        """Picks the longest expert stage from a pass with events between all stages."""
+        if self.fused:
+            return
+        self.events = []
+        for _ in range(3):
+            self.step(record="all")
+        self.torch.cuda.synchronize()
+        kms = self.kernel_ms()
+        self.TOP = 2 if kms["expert_ffn"] >= kms["gemm_gate_up_swiglu"] else 3
+        self.events = []
 
     def step(self, record=None):
         """One pass of the layer.  record="all": CUDA events between all stages
@@ -228,15 +245,21 @@ class Stepper:
             mark()
             self._keep_events(record, ev)
             return
-        # wide FP8 batches: the layer's gate/up GEMM with the SwiGLU epilogue,
-        # then the down GEMM
+        # wide FP8 batches: the groups of few rows in the one-kernel FFN, then the
+        # layer's gate/up GEMM with the SwiGLU epilogue and the down GEMM on the rest
+        small = self.SMALL_GROUP_ROWS
+        moe.expert_ffn(cfg, G, rows, p["xp"], p["xp_scales"], p["expert_offsets"], w["w13"],
+                       w.get("w13_s"), w["w2"], w.get("w2_s"), p["h"], p["h_scales"], p["y"],
+                       p["ffn_sched"], self.sched_bytes, p["status"], w_layout=wl,
+                       max_group_rows=small)
+        mark()
         moe.grouped_gemm_swiglu(cfg, G, I, H, rows, p["xp"], p["xp_scales"],
                                 p["expert_offsets"], w["w13"], w.get("w13_s"), p["h"],
-                                p["h_scales"], p["status"], w_layout=wl)
+                                p["h_scales"], p["status"], w_layout=wl, min_group_rows=small + 1)
         mark()
         moe.grouped_gemm(cfg, G, H, I, rows, p["h"], p["h_scales"] if self.fp8 else None,
                          p["expert_offsets"], w["w2"], w.get("w2_s"), p["y"], moe.OUT_F32,
-                         p["status"], w_layout=wl)
+                         p["status"], w_layout=wl, min_group_rows=small + 1)
         mark()
         moe.combine(cfg, T, p["y"], p["row_of_slot"], p["topk_w"], p["expert_offsets"], self.out,
                     moe.OUT_F32)
@@ -479,6 +502,7 @@ def measure(shape, args, world, rank, local, device, cpu):
     for _ in range(args.warmup):
         stepper.step()
     torch.cuda.synchronize()
+    stepper.set_top()
     if layer.status() != 0:
         raise RuntimeError(f"device status {layer.status()} after warm-up ({shape.name})")
 
@@ -513,24 +537,37 @@ def measure(shape, args, world, rank, local, device, cpu):
     hbm_peak, bf16_peak, peak_src = load_peaks()
     layer_bytes = method_bytes(shape, active)      # the method's bytes per step
     path_total = sum(bytes_per.values())           # + this path's wider intermediates
-    top_label = ("expert_ffn (gate/up + SwiGLU + down, one kernel)" if stepper.fused
-                 else "swiglu_wide gate/up GEMM (SwiGLU + FP8 requantisation epilogue)")
-    # algorithmic bytes of the dominant launch: the weights and block scales of
-    # every active group it streams (gate/up + down, or gate/up alone)
+    # the dominant launch and the active groups it streams: the one-kernel FFN
+    # (all groups, or in wide batches those of at most 32 rows) moves every
+    # weight and block scale of its groups once; the wide gate/up GEMM (groups
+    # of more than 32 rows) their gate/up weights
+    counts = np.diff(offsets)
+    small = Stepper.SMALL_GROUP_ROWS
+    if stepper.fused:
+        top_groups, top_label = counts > 0, "expert_ffn (gate/up + SwiGLU + down, one kernel)"
+    elif stepper.TOP == 2:
+        top_groups = (counts > 0) & (counts <= small)
+        top_label = (f"expert_ffn on the groups of at most {small} rows (gate/up + SwiGLU + "
+                     "down, one kernel)")
+    else:
+        top_groups = counts > small
+        top_label = (f"swiglu_wide gate/up GEMM on the groups of more than {small} rows "
+                     "(SwiGLU + FP8 requantisation epilogue)")
+    top_ffn = stepper.fused or stepper.TOP == 2
+    top_units = int(top_groups.sum())
     w13_b, w2_b = expert_weight_bytes(shape)
-    unit_bytes = w13_b + w2_b if stepper.fused else w13_b
-    top_bytes = active * unit_bytes
+    unit_bytes = w13_b + w2_b if top_ffn else w13_b
+    top_bytes = top_units * unit_bytes
     achieved = top_bytes / (top_ms / 1e3) / 1e9
     traffic = None
     tpath = os.path.join(ROOT, "profiles", "traffic.json")
     if os.path.exists(tpath) and shape.dtype == "fp8" and shape.hidden == 7168:
         with open(tpath) as f:
-            tr = json.load(f).get("swiglu_wide" if stepper.wide else "expert_ffn")
-        rows_per_group = T * (shape.top_k + shape.num_shared) / max(1, active)
-        if tr and (not stepper.wide or
-                   abs(rows_per_group / tr["rows_per_active_group"] - 1.0) <= 0.2):
+            tr = json.load(f).get("expert_ffn" if top_ffn else "swiglu_wide")
+        rows_per_group = counts[top_groups].sum() / max(1, top_units)
+        if tr and (top_ffn or abs(rows_per_group / tr["rows_per_active_group"] - 1.0) <= 0.2):
             # ncu DRAM bytes per active group (small R1 case) x this launch's groups
-            traffic = tr["bytes_per_active_group"] * active
+            traffic = tr["bytes_per_active_group"] * top_units
 
     e2e = None
     if not args.no_e2e:
@@ -582,7 +619,7 @@ def measure(shape, args, world, rank, local, device, cpu):
                      "peak_nominal": NOMINAL_HBM_GBS,
                      "frac_read_stream": None if not read_gbs else achieved / read_gbs,
                      "peak_read_stream": read_gbs,
-                     "bytes_per_unit": unit_bytes, "units": active,
+                     "bytes_per_unit": unit_bytes, "units": top_units,
                      "work_unit": "active expert group (weights + block scales)",
                      "ms_per_launch": top_ms},
         "tensor_pipe_frac_of_bf16x2": (flops / (ms_step / 1e3)) / (2 * bf16_peak * 1e12),

@@ -216,6 +216,17 @@ MOE_API int moe_permute_static_scratch(const moe_config *cfg, int32_t T, const i
                                        int32_t *dev_status, void *stream);
 MOE_API size_t moe_permute_static_scratch_capacity(void);
 
+/* ---- group row windows --------------------------------------------------------
+ * moe_grouped_gemm, moe_grouped_gemm_swiglu and moe_expert_ffn take a window
+ * min_group_rows <= n <= max_group_rows: only the groups whose row count n
+ * (expert_offsets[g+1] - expert_offsets[g]) lies in it are computed; the
+ * output rows of the other groups are not written.  0 and INT32_MAX select
+ * every group; min_group_rows < 0 is MOE_ERR_INVALID_ARG.  A batch can so
+ * send its groups of few rows to one kernel and the rest to another: the
+ * layer, for wide FP8 batches, runs moe_expert_ffn on the groups of at most
+ * 32 rows and the two GEMMs on the others.  Results are bit-identical to a
+ * call over every group. */
+
 /* ---- grouped GEMM -----------------------------------------------------------
  * For every group g and row r in [expert_offsets[g], expert_offsets[g+1]):
  *   C[r, n] = sum_k A[r, k] * W[g, n, k]
@@ -239,8 +250,8 @@ MOE_API size_t moe_permute_static_scratch_capacity(void);
 MOE_API int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32_t k_dim,
                      int32_t rows, const void *a, const float *a_scales,
                      const int32_t *expert_offsets, const void *w, const float *w_scales,
-                     int32_t w_layout, void *c, int32_t c_dtype, int32_t *dev_status,
-                     void *stream);
+                     int32_t w_layout, void *c, int32_t c_dtype, int32_t min_group_rows,
+                     int32_t max_group_rows, int32_t *dev_status, void *stream);
 
 /* Grouped GEMM with the SwiGLU epilogue (gate/up GEMM and SiLU-mul fused):
  * for the rows r of group g, with W13[g] = [W_gate; W_up] ([2*inter, K]),
@@ -262,7 +273,8 @@ MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32
                                     int32_t k_dim, int32_t rows, const void *a,
                                     const float *a_scales, const int32_t *expert_offsets,
                                     const void *w13, const float *w13_scales, int32_t w_layout,
-                                    void *h, float *h_scales, int32_t *dev_status,
+                                    void *h, float *h_scales, int32_t min_group_rows,
+                                    int32_t max_group_rows, int32_t *dev_status,
                                     void *stream);
 
 /* ---- the experts' FFN in one kernel ------------------------------------------
@@ -295,15 +307,17 @@ MOE_API int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, 
                            const void *w13, const float *w13_scales, const void *w2,
                            const float *w2_scales, int32_t w_layout, void *h,
                            float *h_scales, float *y, int32_t *sched, size_t sched_bytes,
+                           int32_t min_group_rows, int32_t max_group_rows,
                            int32_t *dev_status, void *stream);
 
 /* The experts' FFN on dispatched rows with the kernels moe_layer_forward
  * would pick for this batch: moe_expert_ffn for BF16 layers and for FP8
- * groups averaging fewer than 32 rows (rows < 32 * groups), otherwise
- * moe_grouped_gemm_swiglu followed by moe_grouped_gemm (down, fp32 y).
- * Arguments, layouts, ownership and errors as moe_expert_ffn (sched is
- * cleared on `stream` and used only by the one-kernel path); every choice
- * gives the same result bits.  Used by the expert-parallel step, where the
+ * groups averaging fewer than 32 rows (rows < 32 * groups); otherwise
+ * moe_expert_ffn on the groups of at most 32 rows, then
+ * moe_grouped_gemm_swiglu and moe_grouped_gemm (down, fp32 y) on the groups
+ * of more (row windows above).  Arguments, layouts, ownership and errors as
+ * moe_expert_ffn over every group (sched is cleared on `stream`); every
+ * choice gives the same result bits.  Used by the expert-parallel step, where the
  * rows a rank receives for its experts, and its shared-expert rows, are FFN
  * calls of their own. */
 MOE_API int moe_experts_forward(const moe_config *cfg, int32_t groups, int32_t rows,
@@ -343,8 +357,10 @@ MOE_API int moe_combine(const moe_config *cfg, int32_t T, const void *y, const i
  * on `stream`.  The experts' FFN is
  *   BF16, and FP8 with groups averaging fewer than 32 rows (decode):
  *     moe_expert_ffn (one persistent kernel);
- *   FP8, groups averaging 32 rows or more: moe_grouped_gemm_swiglu (its
- *     token-rows-on-M kernel) then moe_grouped_gemm down (64-row tiles);
+ *   FP8, groups averaging 32 rows or more: moe_expert_ffn on the groups of
+ *     at most 32 rows, then moe_grouped_gemm_swiglu (its token-rows-on-M
+ *     kernel) and moe_grouped_gemm down (the same orientation when hidden is
+ *     a multiple of 256, else 64-row tiles) on the others;
  * all with the same result bits (fp32 expert outputs), and
  * all intermediates inside `ws` (size from moe_workspace_size for
  * cfg->max_tokens).  x bf16 [T, H]; out fp32 or bf16 [T, H].  T may be 0..

@@ -74,7 +74,7 @@ _SIGS = {
     "moe_route_quantize": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute_workspace_size": [_CP, _I, ctypes.POINTER(ctypes.c_size_t)],
     "moe_permute": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
-    "moe_grouped_gemm": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _P, _P],
+    "moe_grouped_gemm": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _P],
     "moe_combine": [_CP, _I, _P, _P, _P, _P, _P, _I, _P],
     "moe_workspace_size": [_CP, ctypes.POINTER(ctypes.c_size_t)],
     "moe_layer_forward": [_CP, ctypes.POINTER(Weights), _I, _P, _P, _I, _P, ctypes.c_size_t, _P],
@@ -86,7 +86,8 @@ _SIGS = {
     "moe_selftest_bounded_wait": [_P, ctypes.c_int64, _P, _P],
     "moe_permute_static_scratch": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_count_expert_rows": [_CP, _P, _P, _P],
-    "moe_grouped_gemm_swiglu": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P],
+    "moe_grouped_gemm_swiglu": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I, _P,
+                                _P],
     "moe_pack_expert_weights": [_CP, _I, _I, _I, _P, _P, _P],
     "moe_count_coactivation": [_CP, _I, _P, _P, _P, _P],
     "expert_affinity_permutation": [_P, _P, _I, _I, ctypes.c_double, _P, _P,
@@ -94,7 +95,7 @@ _SIGS = {
     "moe_relayout_experts": [_P, _P, _P, _I, ctypes.c_int64, _P, _P],
     "moe_selftest_ffn_flag_timeout": [_P, ctypes.c_size_t, _P, _P],
     "moe_expert_ffn": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
-                       ctypes.c_size_t, _P, _P],
+                       ctypes.c_size_t, _I, _I, _P, _P],
     "moe_experts_forward": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
                             ctypes.c_size_t, _P, _P],
     "moe_stream_read": [_P, ctypes.c_size_t, _P, _P],
@@ -219,22 +220,30 @@ def permute_static_scratch(cfg: Config, T, topk_ids, x_rows, x_scales, expert_of
            "moe_permute_static_scratch")
 
 
+# group row window [min_group_rows, max_group_rows] of the expert entry points: all groups
+ALL_ROWS = 0x7FFFFFFF
+
+
 def grouped_gemm(cfg: Config, groups, n_out, k_dim, rows, a, a_scales, expert_offsets, w,
-                 w_scales, c, c_dtype, status=None, stream=None, w_layout=None):
+                 w_scales, c, c_dtype, status=None, stream=None, w_layout=None,
+                 min_group_rows=0, max_group_rows=ALL_ROWS):
     _check(lib().moe_grouped_gemm(ctypes.byref(cfg), groups, n_out, k_dim, rows, _ptr(a),
                                   _ptr(a_scales), _ptr(expert_offsets), _ptr(w), _ptr(w_scales),
                                   LAYOUT_ROWS if w_layout is None else w_layout, _ptr(c),
-                                  c_dtype, _ptr(status), _stream(stream)),
+                                  c_dtype, min_group_rows, max_group_rows, _ptr(status),
+                                  _stream(stream)),
            "moe_grouped_gemm")
 
 
 def grouped_gemm_swiglu(cfg: Config, groups, inter, k_dim, rows, a, a_scales, expert_offsets,
-                        w13, w13_scales, h, h_scales, status=None, stream=None, w_layout=None):
+                        w13, w13_scales, h, h_scales, status=None, stream=None, w_layout=None,
+                        min_group_rows=0, max_group_rows=ALL_ROWS):
     _check(lib().moe_grouped_gemm_swiglu(ctypes.byref(cfg), groups, inter, k_dim, rows, _ptr(a),
                                          _ptr(a_scales), _ptr(expert_offsets), _ptr(w13),
                                          _ptr(w13_scales),
                                          LAYOUT_ROWS if w_layout is None else w_layout, _ptr(h),
-                                         _ptr(h_scales), _ptr(status), _stream(stream)),
+                                         _ptr(h_scales), min_group_rows, max_group_rows,
+                                         _ptr(status), _stream(stream)),
            "moe_grouped_gemm_swiglu")
 
 
@@ -256,13 +265,14 @@ def expert_ffn_sched_bytes(groups, rows) -> int:
 
 def expert_ffn(cfg: Config, groups, rows, a, a_scales, expert_offsets, w13, w13_scales, w2,
                w2_scales, h, h_scales, y, sched, sched_bytes, status=None, stream=None,
-               w_layout=None):
-    """Both expert GEMMs with SwiGLU between them, one persistent kernel (FP8)."""
+               w_layout=None, min_group_rows=0, max_group_rows=ALL_ROWS):
+    """Both expert GEMMs with SwiGLU between them, one persistent kernel (FP8 or BF16)."""
     _check(lib().moe_expert_ffn(ctypes.byref(cfg), groups, rows, _ptr(a), _ptr(a_scales),
                                 _ptr(expert_offsets), _ptr(w13), _ptr(w13_scales), _ptr(w2),
                                 _ptr(w2_scales), LAYOUT_ROWS if w_layout is None else w_layout,
                                 _ptr(h), _ptr(h_scales), _ptr(y), _ptr(sched), sched_bytes,
-                                _ptr(status), _stream(stream)), "moe_expert_ffn")
+                                min_group_rows, max_group_rows, _ptr(status), _stream(stream)),
+           "moe_expert_ffn")
 
 
 def experts_forward(cfg: Config, groups, rows, a, a_scales, expert_offsets, w13, w13_scales, w2,

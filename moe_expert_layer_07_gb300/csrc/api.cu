@@ -100,10 +100,18 @@ bool fused_ffn(const moe_config *cfg, int64_t T) {
     return cfg->dtype != MOE_DTYPE_FP8_BLOCK128 || !wide_rows(cfg, T);
 }
 
+// In batches that take the wide GEMMs, the groups with at most this many
+// rows still go to the one-kernel FFN: one 32-row activation tile streams
+// their weights once, where a 128-row token tile of the wide kernels would
+// be at most a quarter full.
+constexpr int kFfnGroupRowsInWide = 32;
+
 // The experts' FFN on dispatched rows, whichever kernels suit the batch:
 // the one-kernel FFN for BF16 and for FP8 groups averaging fewer than 32
-// rows, else the gate/up GEMM with its SwiGLU epilogue and the down GEMM.
-// All choices give the same result bits.
+// rows; else (FP8) the gate/up GEMM with its SwiGLU epilogue and the down
+// GEMM, with token rows on the MMA's M side, for the groups of more than 32
+// rows, and the one-kernel FFN for the others (the two sets of groups read
+// disjoint weights and rows).  All choices give the same result bits.
 int experts_forward(bool fp8, int groups, int hidden, int inter, int rows, const void *xp,
                     const float *xp_scales, const int32_t *offsets, const void *w13,
                     const float *w13_scales, const void *w2, const float *w2_scales,
@@ -113,11 +121,17 @@ int experts_forward(bool fp8, int groups, int hidden, int inter, int rows, const
         return launch_expert_ffn(fp8, groups, hidden, inter, rows, xp, xp_scales, offsets, w13,
                                  w13_scales, w2, w2_scales, tiled, h, h_scales, y, sched,
                                  sched_zeroed, status, s);
-    int rc = launch_grouped_gemm_swiglu(fp8, groups, inter, hidden, rows, xp, xp_scales, offsets,
-                                        w13, w13_scales, tiled, h, h_scales, status, s);
+    int rc = launch_expert_ffn(fp8, groups, hidden, inter, rows, xp, xp_scales, offsets, w13,
+                               w13_scales, w2, w2_scales, tiled, h, h_scales, y, sched,
+                               sched_zeroed, status, s, 0, kFfnGroupRowsInWide);
+    if (rc) return rc;
+    rc = launch_grouped_gemm_swiglu(fp8, groups, inter, hidden, rows, xp, xp_scales, offsets, w13,
+                                    w13_scales, tiled, h, h_scales, status, s,
+                                    kFfnGroupRowsInWide + 1);
     if (rc) return rc;
     return launch_grouped_gemm(fp8, groups, hidden, inter, rows, h, h_scales, offsets, w2,
-                               w2_scales, tiled, y, MOE_OUT_F32, status, s);
+                               w2_scales, tiled, y, MOE_OUT_F32, status, s,
+                               kFfnGroupRowsInWide + 1);
 }
 
 int layout(const moe_config *cfg, int64_t Tm, moe_ws_layout *L) {
@@ -254,13 +268,14 @@ int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_ids, const
 int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32_t k_dim,
                      int32_t rows, const void *a, const float *a_scales,
                      const int32_t *expert_offsets, const void *w, const float *w_scales,
-                     int32_t w_layout, void *c, int32_t c_dtype, int32_t *dev_status,
-                     void *stream) {
+                     int32_t w_layout, void *c, int32_t c_dtype, int32_t min_group_rows,
+                     int32_t max_group_rows, int32_t *dev_status, void *stream) {
     Range range("moe_grouped_gemm");
     int rc = check_config(cfg);
     if (rc) return rc;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
-    if (groups <= 0 || rows < 0 || n_out <= 0 || k_dim <= 0) return MOE_ERR_INVALID_ARG;
+    if (groups <= 0 || rows < 0 || n_out <= 0 || k_dim <= 0 || min_group_rows < 0)
+        return MOE_ERR_INVALID_ARG;
     if (!layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
     if (c_dtype != MOE_OUT_F32 && c_dtype != MOE_OUT_BF16) return MOE_ERR_INVALID_ARG;
     if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -275,19 +290,21 @@ int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32
     if (!al16(a) || !al16(w) || !al16(c)) return MOE_ERR_INVALID_ARG;
     return launch_grouped_gemm(fp8, groups, n_out, k_dim, rows, a, a_scales, expert_offsets, w,
                                w_scales, w_layout == MOE_LAYOUT_TILES, c, c_dtype, dev_status,
-                               static_cast<cudaStream_t>(stream));
+                               static_cast<cudaStream_t>(stream), min_group_rows, max_group_rows);
 }
 
 int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter, int32_t k_dim,
                             int32_t rows, const void *a, const float *a_scales,
                             const int32_t *expert_offsets, const void *w13,
                             const float *w13_scales, int32_t w_layout, void *h, float *h_scales,
+                            int32_t min_group_rows, int32_t max_group_rows,
                             int32_t *dev_status, void *stream) {
     Range range("moe_grouped_gemm_swiglu");
     int rc = check_config(cfg);
     if (rc) return rc;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
-    if (groups <= 0 || rows < 0 || inter <= 0 || k_dim <= 0) return MOE_ERR_INVALID_ARG;
+    if (groups <= 0 || rows < 0 || inter <= 0 || k_dim <= 0 || min_group_rows < 0)
+        return MOE_ERR_INVALID_ARG;
     if (!layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
     if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (inter % 128 || k_dim % (fp8 ? 128 : 64)) return MOE_ERR_UNSUPPORTED_SHAPE;
@@ -302,7 +319,8 @@ int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter
     return launch_grouped_gemm_swiglu(fp8, groups, inter, k_dim, rows, a, a_scales,
                                       expert_offsets, w13, w13_scales,
                                       w_layout == MOE_LAYOUT_TILES, h, h_scales, dev_status,
-                                      static_cast<cudaStream_t>(stream));
+                                      static_cast<cudaStream_t>(stream), min_group_rows,
+                                      max_group_rows);
 }
 
 size_t moe_expert_ffn_sched_bytes(int32_t groups, int32_t rows) {
@@ -314,11 +332,13 @@ int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const vo
                    const float *a_scales, const int32_t *expert_offsets, const void *w13,
                    const float *w13_scales, const void *w2, const float *w2_scales,
                    int32_t w_layout, void *h, float *h_scales, float *y, int32_t *sched,
-                   size_t sched_bytes, int32_t *dev_status, void *stream) {
+                   size_t sched_bytes, int32_t min_group_rows, int32_t max_group_rows,
+                   int32_t *dev_status, void *stream) {
     Range range("moe_expert_ffn");
     int rc = check_config(cfg);
     if (rc) return rc;
-    if (groups <= 0 || rows < 0 || !layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
+    if (groups <= 0 || rows < 0 || !layout_ok(w_layout) || min_group_rows < 0)
+        return MOE_ERR_INVALID_ARG;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
     if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
     if ((int64_t)groups * 2 * cfg->inter > INT32_MAX || (int64_t)groups * cfg->hidden > INT32_MAX)
@@ -337,7 +357,7 @@ int moe_expert_ffn(const moe_config *cfg, int32_t groups, int32_t rows, const vo
                              expert_offsets,
                              w13, w13_scales, w2, w2_scales, w_layout == MOE_LAYOUT_TILES, h,
                              h_scales, y, sched, false, dev_status,
-                             static_cast<cudaStream_t>(stream));
+                             static_cast<cudaStream_t>(stream), min_group_rows, max_group_rows);
 }
 
 int moe_experts_forward(const moe_config *cfg, int32_t groups, int32_t rows, const void *a,
@@ -405,7 +425,8 @@ int moe_layer_kernel_count(const moe_config *cfg, int32_t T) {
     // route (with the FP8 quantisation of x), permute, the experts' FFN (one
     // fused kernel, or gate/up GEMM with SwiGLU + down GEMM), combine
     (void)fp8;
-    const int ffn = fused_ffn(cfg, T) ? 1 : 2;
+    // wide batches: the FFN kernel for groups of few rows, the two GEMMs for the rest
+    const int ffn = fused_ffn(cfg, T) ? 1 : 3;
     return route_kernel_count() + permute_kernel_count(cfg, T) + ffn + 1;
 }
 
@@ -438,9 +459,9 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     int32_t *status = reinterpret_cast<int32_t *>(base + L.status);
     const bool fused = T > 0 && fused_ffn(cfg, T);
     const int rows = (int)total_rows(cfg, T);
-    // status word (and, for the fused FFN, its scheduler counters) cleared
-    const size_t clear = fused ? L.ffn_sched + ffn_sched_bytes(groups_of(cfg), rows)
-                               : sizeof(int32_t);
+    // status word and the one-kernel FFN's scheduler counters (every path
+    // runs that kernel, for all groups or for the groups with few rows)
+    const size_t clear = L.ffn_sched + ffn_sched_bytes(groups_of(cfg), rows);
     MOE_CUDA_TRY(cudaMemsetAsync(status, 0, clear, s));
     if (T == 0) return MOE_OK;
 

@@ -99,6 +99,7 @@ struct FfnArgs {
     float *y;                  // [rows, hidden]
     int32_t *sched;            // [0] next unit; [1 + j] finished gate/up tiles of activation tile j
     int w_tiled;               // W13, W2 in MOE_LAYOUT_TILES
+    int min_rows, max_rows;    // groups whose row count lies outside are skipped
     int32_t *status;
 };
 
@@ -223,13 +224,18 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
         if (a < 0 || b < a || b > args.rows) s_bad = 1;
     }
     __syncthreads();
+    // activation tiles of group g; none for groups outside the row window
+    auto ntiles_of = [&](int g) {
+        const int n = s_off[g + 1] - s_off[g];
+        return (n < args.min_rows || n > args.max_rows) ? 0 : (n + kBN - 1) / kBN;
+    };
     if (warp == 0) {   // activation-tile prefix over groups: lane L owns a contiguous run
         const int per = (G + 31) / 32;
         const int g0 = lane * per;
         int local = 0;
         for (int q = 0; q < per; ++q) {
             const int g = g0 + q;
-            if (g < G) local += (s_off[g + 1] - s_off[g] + kBN - 1) / kBN;
+            if (g < G) local += ntiles_of(g);
         }
         int incl = local;
 #pragma unroll
@@ -242,7 +248,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
             const int g = g0 + q;
             if (g < G) {
                 s_nt[g] = run;
-                run += (s_off[g + 1] - s_off[g] + kBN - 1) / kBN;
+                run += ntiles_of(g);
             }
         }
         if (lane == 31) s_nt[G] = incl;
@@ -727,7 +733,8 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
                     const float *xp_scales, const int32_t *offsets, const void *w13,
                     const float *w13_scales, const void *w2, const float *w2_scales,
                     bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
-                    bool sched_zeroed, int32_t *status, cudaStream_t s) {
+                    bool sched_zeroed, int32_t *status, cudaStream_t s, int min_rows,
+                    int max_rows) {
     if (rows == 0) return MOE_OK;
     // two epilogue warpgroups: FP8 promotes every K block, and more warps per
     // SM sub-partition hide those latencies (BF16: neutral to slightly faster)
@@ -772,6 +779,8 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
     a.y = y;
     a.sched = sched;
     a.w_tiled = w_tiled;
+    a.min_rows = min_rows;
+    a.max_rows = max_rows;
     a.status = status;
     const int64_t units_bound =
         (int64_t)(inter / kBM + hidden / kBM) * (groups + ceil_div(rows, kBN));
@@ -789,10 +798,11 @@ int launch_expert_ffn(bool fp8, int groups, int hidden, int inter, int rows, con
                       const float *xp_scales, const int32_t *offsets, const void *w13,
                       const float *w13_scales, const void *w2, const float *w2_scales,
                       bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
-                      bool sched_zeroed, int32_t *status, cudaStream_t s) {
+                      bool sched_zeroed, int32_t *status, cudaStream_t s, int min_rows,
+                      int max_rows) {
     auto f = fp8 ? launch_ffn_impl<true> : launch_ffn_impl<false>;
     return f(groups, hidden, inter, rows, xp, xp_scales, offsets, w13, w13_scales, w2, w2_scales,
-             w_tiled, h, h_scales, y, sched, sched_zeroed, status, s);
+             w_tiled, h, h_scales, y, sched, sched_zeroed, status, s, min_rows, max_rows);
 }
 
 }  // namespace moe

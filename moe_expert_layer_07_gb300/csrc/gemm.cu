@@ -111,6 +111,7 @@ struct GemmArgs {
     float *h_scales;  // SwiGLU + FP8: [rows, n_out/256]
     int c_bf16;
     int w_tiled;      // W in MOE_LAYOUT_TILES
+    int min_rows, max_rows;   // groups whose row count lies outside are skipped
     int32_t *status;
 };
 
@@ -216,13 +217,18 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
         if (a < 0 || b < a || b > args.rows) s_bad = 1;
     }
     __syncthreads();
+    // token tiles of group g; none for groups outside the row window
+    auto ntiles_of = [&](int g) {
+        const int n = s_off[g + 1] - s_off[g];
+        return (n < args.min_rows || n > args.max_rows) ? 0 : (n + BN - 1) / BN;
+    };
     if (warp == 0) {   // tile prefix over groups: lane L owns a contiguous run
         const int per = (G + 31) / 32;
         const int g0 = lane * per;
         int local = 0;
         for (int q = 0; q < per; ++q) {
             const int g = g0 + q;
-            if (g < G) local += MT * ((s_off[g + 1] - s_off[g] + BN - 1) / BN);
+            if (g < G) local += MT * ntiles_of(g);
         }
         int incl = local;
 #pragma unroll
@@ -235,7 +241,7 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
             const int g = g0 + q;
             if (g < G) {
                 s_tiles[g] = run;
-                run += MT * ((s_off[g + 1] - s_off[g] + BN - 1) / BN);
+                run += MT * ntiles_of(g);
             }
         }
         if (lane == 31) s_tiles[G] = incl;
@@ -738,7 +744,7 @@ int launch_impl(const GemmArgs &args, const void *a, const void *w, cudaStream_t
 int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, const void *a,
                         const float *a_scales, const int32_t *offsets, const void *w,
                         const float *w_scales, bool w_tiled, void *c, int c_dtype,
-                        int32_t *status, cudaStream_t s) {
+                        int32_t *status, cudaStream_t s, int min_rows, int max_rows) {
     if (rows == 0) return MOE_OK;
     GemmArgs args;
     args.groups = groups;
@@ -752,6 +758,8 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     args.h_scales = nullptr;
     args.c_bf16 = c_dtype == MOE_OUT_BF16;
     args.w_tiled = w_tiled;
+    args.min_rows = min_rows;
+    args.max_rows = max_rows;
     args.status = status;
     // Decode-sized groups (a few rows each) stream best with 32-row tiles;
     // larger groups take 128 token rows against 256 output columns per tile
@@ -760,7 +768,7 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     const bool wide = (int64_t)rows >= 16 * (int64_t)groups;
     if (fp8 && wide && n_out % 256 == 0 && c_dtype == MOE_OUT_F32)
         return launch_gemm_wide(groups, n_out, k_dim, rows, a, a_scales, offsets, w, w_scales,
-                                w_tiled, static_cast<float *>(c), status, s);
+                                w_tiled, static_cast<float *>(c), status, s, min_rows, max_rows);
     if (fp8) return wide ? launch_impl<true, 64, 3, false, 2>(args, a, w, s)
                          : launch_impl<true, 32, 4>(args, a, w, s);
     return launch_impl<false, 32, 4>(args, a, w, s);
@@ -769,7 +777,8 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
 int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int rows,
                                const void *a, const float *a_scales, const int32_t *offsets,
                                const void *w13, const float *w13_scales, bool w_tiled, void *h,
-                               float *h_scales, int32_t *status, cudaStream_t s) {
+                               float *h_scales, int32_t *status, cudaStream_t s, int min_rows,
+                               int max_rows) {
     if (rows == 0) return MOE_OK;
     GemmArgs args;
     args.groups = groups;
@@ -783,12 +792,15 @@ int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int r
     args.h_scales = h_scales;
     args.c_bf16 = !fp8;
     args.w_tiled = w_tiled;
+    args.min_rows = min_rows;
+    args.max_rows = max_rows;
     args.status = status;
     // Groups averaging 16 rows or more: token rows on the MMA's M side, the
     // gate and up rows of 128 features on N (gemm_wide.cu).
     if (fp8 && (int64_t)rows >= 16 * (int64_t)groups)
         return launch_swiglu_wide(groups, inter, k_dim, rows, a, a_scales, offsets, w13,
-                                  w13_scales, w_tiled, h, h_scales, status, s);
+                                  w13_scales, w_tiled, h, h_scales, status, s, min_rows,
+                                  max_rows);
     if (fp8) return launch_impl<true, 32, 2, true>(args, a, w13, s);
     return launch_impl<false, 32, 2, true>(args, a, w13, s);
 }

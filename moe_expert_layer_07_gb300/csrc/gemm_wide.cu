@@ -91,6 +91,7 @@ struct WideArgs {
     float *h_scales;         // SwiGLU: [rows, n_out / 256]
     float *c;                // plain: [rows, n_out] fp32
     int w_tiled;             // W in MOE_LAYOUT_TILES
+    int min_rows, max_rows;  // groups whose row count lies outside are skipped
     int32_t *status;
 };
 
@@ -187,13 +188,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (a < 0 || b < a || b > args.rows) s_bad = 1;
     }
     __syncthreads();
+    // token tiles of group g; none for groups outside the row window
+    auto mtiles_of = [&](int g) {
+        const int n = s_off[g + 1] - s_off[g];
+        return (n < args.min_rows || n > args.max_rows) ? 0 : (n + kTM - 1) / kTM;
+    };
     if (warp == 0 && !s_bad) {   // tile prefix over groups: lane L owns a contiguous run
         const int per = (G + 31) / 32;
         const int g0 = lane * per;
         int local = 0;
         for (int q = 0; q < per; ++q) {
             const int g = g0 + q;
-            if (g < G) local += NT * ((s_off[g + 1] - s_off[g] + kTM - 1) / kTM);
+            if (g < G) local += NT * mtiles_of(g);
         }
         int incl = local;
 #pragma unroll
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int g = g0 + q;
             if (g < G) {
                 s_tiles[g] = run;
-                run += NT * ((s_off[g + 1] - s_off[g] + kTM - 1) / kTM);
+                run += NT * mtiles_of(g);
             }
         }
         if (lane == 31) s_tiles[G] = incl;
@@ -531,6 +537,8 @@ WideArgs wide_args(int groups, int n_out, int k_dim, int rows, const float *a_sc
     args.h_scales = nullptr;
     args.c = nullptr;
     args.w_tiled = w_tiled;
+    args.min_rows = 0;
+    args.max_rows = 0x7fffffff;
     args.status = status;
     return args;
 }
@@ -540,10 +548,12 @@ WideArgs wide_args(int groups, int n_out, int k_dim, int rows, const float *a_sc
 int launch_swiglu_wide(int groups, int inter, int k_dim, int rows, const void *a,
                        const float *a_scales, const int32_t *offsets, const void *w13,
                        const float *w13_scales, bool w_tiled, void *h, float *h_scales,
-                       int32_t *status, cudaStream_t s) {
+                       int32_t *status, cudaStream_t s, int min_rows, int max_rows) {
     if (rows == 0) return MOE_OK;
     WideArgs args = wide_args(groups, 2 * inter, k_dim, rows, a_scales, offsets, w13_scales,
                               w_tiled, status);
+    args.min_rows = min_rows;
+    args.max_rows = max_rows;
     args.h = static_cast<uint8_t *>(h);
     args.h_scales = h_scales;
     return launch_wide<true>(args, a, w13, s);
@@ -552,10 +562,12 @@ int launch_swiglu_wide(int groups, int inter, int k_dim, int rows, const void *a
 int launch_gemm_wide(int groups, int n_out, int k_dim, int rows, const void *a,
                      const float *a_scales, const int32_t *offsets, const void *w,
                      const float *w_scales, bool w_tiled, float *c, int32_t *status,
-                     cudaStream_t s) {
+                     cudaStream_t s, int min_rows, int max_rows) {
     if (rows == 0) return MOE_OK;
     WideArgs args =
         wide_args(groups, n_out, k_dim, rows, a_scales, offsets, w_scales, w_tiled, status);
+    args.min_rows = min_rows;
+    args.max_rows = max_rows;
     args.c = c;
     return launch_wide<false>(args, a, w, s);
 }

@@ -56,26 +56,34 @@ int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const 
                    const float *x_scales, int32_t *offsets, int32_t *src_of_row,
                    int32_t *row_of_slot, void *xp, float *xp_scales, void *ws,
                    int32_t *status, cudaStream_t s);
+// Row windows: every expert launcher below processes only the groups whose
+// row count n satisfies min_rows <= n <= max_rows (the others' rows of its
+// outputs are left as they are), so that groups of few and of many rows can
+// go to different kernels of one batch.
+constexpr int kAllRows = 0x7fffffff;
 int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, const void *a,
                         const float *a_scales, const int32_t *offsets, const void *w,
                         const float *w_scales, bool w_tiled, void *c, int c_dtype,
-                        int32_t *status, cudaStream_t s);
+                        int32_t *status, cudaStream_t s, int min_rows = 0,
+                        int max_rows = kAllRows);
 int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int rows,
                                const void *a, const float *a_scales, const int32_t *offsets,
                                const void *w13, const float *w13_scales, bool w_tiled, void *h,
-                               float *h_scales, int32_t *status, cudaStream_t s);
+                               float *h_scales, int32_t *status, cudaStream_t s,
+                               int min_rows = 0, int max_rows = kAllRows);
 // Wide FP8 batches (groups averaging 16 rows or more): gate/up + SwiGLU +
 // FP8 requantisation with token rows on the MMA's M side (gemm_wide.cu).
 int launch_swiglu_wide(int groups, int inter, int k_dim, int rows, const void *a,
                        const float *a_scales, const int32_t *offsets, const void *w13,
                        const float *w13_scales, bool w_tiled, void *h, float *h_scales,
-                       int32_t *status, cudaStream_t s);
+                       int32_t *status, cudaStream_t s, int min_rows = 0,
+                       int max_rows = kAllRows);
 // Wide FP8 batches, fp32 C with n_out a multiple of 256: the same kernel
 // with a plain epilogue (TMA stores of 32 x 32 fp32 blocks).
 int launch_gemm_wide(int groups, int n_out, int k_dim, int rows, const void *a,
                      const float *a_scales, const int32_t *offsets, const void *w,
                      const float *w_scales, bool w_tiled, float *c, int32_t *status,
-                     cudaStream_t s);
+                     cudaStream_t s, int min_rows = 0, int max_rows = kAllRows);
 // The experts' FFN in one persistent kernel (FP8 or BF16): gate/up + SwiGLU
 // (+ FP8 requant), then down.  `sched` holds ffn_sched_bytes(groups, rows) bytes; it is
 // cleared on `s` unless the caller has already zeroed it in stream order.
@@ -84,7 +92,8 @@ int launch_expert_ffn(bool fp8, int groups, int hidden, int inter, int rows, con
                       const float *xp_scales, const int32_t *offsets, const void *w13,
                       const float *w13_scales, const void *w2, const float *w2_scales,
                       bool w_tiled, void *h, float *h_scales, float *y, int32_t *sched,
-                      bool sched_zeroed, int32_t *status, cudaStream_t s);
+                      bool sched_zeroed, int32_t *status, cudaStream_t s, int min_rows = 0,
+                      int max_rows = kAllRows);
 int launch_combine(const moe_config *cfg, int T, const void *y, const int32_t *row_of_slot,
                    const float *topk_w, const int32_t *offsets, void *out, int out_dtype,
                    cudaStream_t s);

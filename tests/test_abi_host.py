@@ -89,7 +89,7 @@ def test_layer_kernel_counts(L):
     r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
     assert moe.layer_kernel_count(r1, 128) == 6        # one-kernel FFN, 1024 slots
     assert moe.layer_kernel_count(r1, 129) == 7        # 1032 slots: count and scan apart
-    assert moe.layer_kernel_count(r1, 4096) == 8       # wide: SwiGLU GEMM, down GEMM
+    assert moe.layer_kernel_count(r1, 4096) == 9       # wide: FFN (small groups), 2 GEMMs
     mini = moe.make_config(synth.CONFIGS["r1_mini"])   # inter 384: odd K blocks of W2
     assert moe.layer_kernel_count(mini, 37) == 6
     b16 = moe.make_config(synth.CONFIGS["bf16_mini"])   # BF16: one-kernel FFN
@@ -113,15 +113,21 @@ def test_bad_arguments_are_rejected_before_launch(L):
     bad.hidden = 1000
     assert L.moe_route(ctypes.byref(bad), 4, fake, fake, None, None, None, fake, fake, fake,
                        None, None) == -2
+    ALL = moe.ALL_ROWS
     assert L.moe_grouped_gemm(ctypes.byref(cfg), 3, 200, 128, 10, fake, fake, fake, fake, fake,
-                              0, fake, 0, None, None) == -2
+                              0, fake, 0, 0, ALL, None, None) == -2
     assert L.moe_grouped_gemm(ctypes.byref(cfg), 2000, 128, 128, 10, fake, fake, fake, fake,
-                              fake, 0, fake, 0, None, None) == -2
+                              fake, 0, fake, 0, 0, ALL, None, None) == -2
     # unknown weight layout
     assert L.moe_grouped_gemm(ctypes.byref(cfg), 3, 256, 128, 10, fake, fake, fake, fake, fake,
-                              7, fake, 0, None, None) == -1
+                              7, fake, 0, 0, ALL, None, None) == -1
     assert L.moe_grouped_gemm_swiglu(ctypes.byref(cfg), 3, 256, 128, 10, fake, fake, fake, fake,
-                                     fake, 2, fake, fake, None, None) == -1
+                                     fake, 2, fake, fake, 0, ALL, None, None) == -1
+    # a group row window that starts below zero
+    assert L.moe_grouped_gemm(ctypes.byref(cfg), 3, 256, 128, 10, fake, fake, fake, fake, fake,
+                              0, fake, 0, -1, ALL, None, None) == -1
+    assert L.moe_grouped_gemm_swiglu(ctypes.byref(cfg), 3, 256, 128, 10, fake, fake, fake, fake,
+                                     fake, 0, fake, fake, -1, ALL, None, None) == -1
     # packing: shapes and overlap
     assert L.moe_pack_expert_weights(ctypes.byref(cfg), 2, 200, 128, fake, P(0x100000),
                                      None) == -2
@@ -165,19 +171,21 @@ def test_bad_arguments_are_rejected_before_launch(L):
                                16, None) == -3
     # the one-kernel expert FFN: enough scratch, known layouts
     r1 = moe.make_config(synth.CONFIGS["r1_decode_t128"])
-    ffn = lambda c, groups, rows, nbytes, layout=0: L.moe_expert_ffn(
+    ffn = lambda c, groups, rows, nbytes, layout=0, lo=0: L.moe_expert_ffn(
         ctypes.byref(c), groups, rows, fake, fake, fake, fake, fake, fake, fake, layout, fake,
-        fake, fake, fake, nbytes, None, None)
+        fake, fake, fake, nbytes, lo, moe.ALL_ROWS, None, None)
     need = moe.expert_ffn_sched_bytes(257, 1152)
     assert need == 4 * (1 + 257 + 36)
     assert ffn(r1, 257, 1152, need - 4) == -3
     assert ffn(r1, 0, 10, need) == -1
     assert ffn(r1, 2000, 10, 1 << 20) == -2
     assert ffn(r1, 257, 1152, need, layout=5) == -1
+    assert ffn(r1, 257, 1152, need, lo=-3) == -1
     assert L.moe_expert_ffn(ctypes.byref(r1), 257, 1152, P(0x1001), fake, fake, fake, fake, fake,
-                            fake, 0, fake, fake, fake, fake, need, None, None) == -1
+                            fake, 0, fake, fake, fake, fake, need, 0, moe.ALL_ROWS, None,
+                            None) == -1
     assert L.moe_expert_ffn(ctypes.byref(r1), 257, 0, None, None, None, None, None, None, None,
-                            0, None, None, None, None, 0, None, None) == 0
+                            0, None, None, None, None, 0, 0, moe.ALL_ROWS, None, None) == 0
     # the experts' FFN with the layer's choice of kernels: the same checks
     fwd = lambda c, groups, rows, nbytes, layout=0: L.moe_experts_forward(
         ctypes.byref(c), groups, rows, fake, fake, fake, fake, fake, fake, fake, layout, fake,

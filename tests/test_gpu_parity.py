@@ -684,11 +684,64 @@ def dataclasses_replace(shape, **kw):
     return dataclasses.replace(shape, **kw)
 
 
+@pytest.mark.parametrize("name,T", [("r1_mini_zipf", None), ("r1_mini", 130), ("bf16_mini", None)])
+def test_group_row_windows_partition_the_groups(lib, name, T):
+    """The group row windows of the expert entry points: the one-kernel FFN on
+    the groups of at most X rows, then the gate/up and down GEMMs on the
+    others, give the bits of the FFN over every group; a windowed call leaves
+    the other groups' rows as they were.  (130 tokens of r1_mini: the GEMMs
+    take their token-rows-on-M kernels; the others their 32/64-row tiles.)"""
+    wl = workload(name, T=T)
+    layer = wl.layer()
+    s = wl.shape
+    out = torch.empty((s.tokens, s.hidden), device="cuda")
+    layer.forward(wl.dev["x"], out)   # routing and dispatch into the workspace
+    torch.cuda.synchronize()
+    cfg, w, wlay = layer.cfg, layer._keep, layer.expert_layout
+    G, H, I = s.groups, s.hidden, s.inter
+    rows = s.tokens * (s.top_k + s.num_shared)
+    L, base = layer.layout, layer.ws.data_ptr()
+    fp8 = s.dtype == "fp8"
+    xp, xps, off = base + L.xp, (base + L.xp_scales) if fp8 else None, base + L.expert_offsets
+    offs = to_np(layer.view("expert_offsets", torch.int32, (G + 1,)))
+    counts = np.diff(offs)
+    X = int(np.median(counts[counts > 0]))
+    assert (counts > X).any() and ((counts > 0) & (counts <= X)).any()
+    nb = moe.expert_ffn_sched_bytes(G, rows)
+    small = np.zeros(rows, bool)
+    for g in np.nonzero(counts <= X)[0]:
+        small[offs[g]:offs[g + 1]] = True
+    small_t = torch.as_tensor(small, device="cuda")
+
+    def run_ffn(**kw):
+        h = torch.zeros((rows, I), dtype=torch.uint8 if fp8 else torch.bfloat16, device="cuda")
+        hs = torch.zeros((rows, I // 128), device="cuda") if fp8 else None
+        y = torch.full((rows, H), float("nan"), device="cuda")
+        sched = torch.zeros(nb // 4 + 1, dtype=torch.int32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        moe.expert_ffn(cfg, G, rows, xp, xps, off, w["w13"], w.get("w13_s"), w["w2"],
+                       w.get("w2_s"), h, hs, y, sched, nb, st, w_layout=wlay, **kw)
+        return h, hs, y, st
+
+    _, _, y_all, st0 = run_ffn()
+    h, hs, y, st = run_ffn(max_group_rows=X)
+    torch.cuda.synchronize()
+    assert torch.isnan(y[~small_t]).all() and torch.equal(y[small_t], y_all[small_t])
+    moe.grouped_gemm_swiglu(cfg, G, I, H, rows, xp, xps, off, w["w13"], w.get("w13_s"), h, hs, st,
+                            w_layout=wlay, min_group_rows=X + 1)
+    moe.grouped_gemm(cfg, G, H, I, rows, h, hs, off, w["w2"], w.get("w2_s"), y, moe.OUT_F32, st,
+                     w_layout=wlay, min_group_rows=X + 1)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0 and int(st0.item()) == 0
+    assert torch.equal(y, y_all)
+
+
 @pytest.mark.parametrize("name,T", [("r1_mini_i512", None), ("bf16_mini", None),
                                     ("r1_mini", None), ("r1_mini", 130)])
 def test_bench_steps_equal_the_layer_call(lib, name, T):
     """bench.py times the layer as C-ABI steps; they compute the layer call's bits
-    (130 tokens of r1_mini average 35 rows per group: the wide-batch GEMM path)."""
+    (130 tokens of r1_mini average 35 rows per group: the wide-batch path, the
+    one-kernel FFN on the groups of at most 32 rows and the GEMMs on the rest)."""
     import bench
     wl = workload(name, T=T)
     layer = wl.layer()
