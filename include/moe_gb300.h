@@ -177,6 +177,11 @@ MOE_API int moe_act_requant(const moe_config *cfg, int32_t mode, int32_t rows,
  *   xp         [R_tot, H] gathered rows (e4m3 or bf16), xp_scales fp32
  *              [R_tot, H/128] (FP8 only)
  *   ws         scratch of moe_permute_workspace_size bytes
+ *   copy_max_group_rows  the rows of groups with more rows than this get their
+ *              src_of_row / row_of_slot entries but are not copied into xp /
+ *              xp_scales (a GEMM that gathers them from the token rows,
+ *              moe_grouped_gemm_swiglu_gather, reads them there); INT32_MAX
+ *              copies every row, < 0 is MOE_ERR_INVALID_ARG.
  * (report, sections "Overview" and "Compute-communication overlap": the
  * dispatch that carries each token to its experts.) */
 MOE_API int moe_permute_workspace_size(const moe_config *cfg, int32_t T, size_t *bytes /* host */);
@@ -184,13 +189,13 @@ MOE_API int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_id
                 const void *x_rows, const float *x_scales,
                 int32_t *expert_offsets, int32_t *src_of_row, int32_t *row_of_slot,
                 void *xp, float *xp_scales, void *ws, size_t ws_bytes,
-                int32_t *dev_status, void *stream);
+                int32_t copy_max_group_rows, int32_t *dev_status, void *stream);
 
 /* moe_permute without a workspace argument.  The pages have no counterpart:
  * this entry serves callers that cannot allocate device memory, such as a
  * plugin inside a framework that owns every device allocation, or a
  * runtime held to a fixed, pre-reserved memory budget.  Arguments and
- * results are those of moe_permute minus ws/ws_bytes.
+ * results are those of moe_permute minus ws/ws_bytes, copying every row.
  *   - Scratch lives in a static device array inside the library, 1 MiB per
  *     device (moe_permute_static_scratch_capacity()), held by every GPU that
  *     loads the library until the process exits.  A call whose scratch need
@@ -277,7 +282,36 @@ MOE_API int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32
                                     int32_t max_group_rows, int32_t *dev_status,
                                     void *stream);
 
-/* ---- the experts' FFN in one kernel ------------------------------------------
+/* moe_grouped_gemm_swiglu without materialised activation rows: the rows of
+ * each group are gathered from the token rows of x by the tensor cores' copy
+ * engine (TMA tile::gather4, four rows per copy, straight into the MMA's
+ * swizzled operand layout), the f1 row gather of the report's fused MoE
+ * kernel (section "Library optimisation").  Row r (in expert_offsets' row
+ * numbering) is token t(r) of slot src_of_row[r]: routed slots t*top_k + j
+ * give t, the shared experts' slots T*top_k + i*T + t give t (moe_permute's
+ * tables).  FP8 layers only (else MOE_ERR_INVALID_ARG).
+ *   x_rows   e4m3 [T, k_dim] and x_scales fp32 [T, k_dim/128]: the token rows
+ *            (moe_route_quantize's xq / xs)
+ *   src_of_row int32 [rows]
+ * Other arguments, results (h, h_scales rows in dispatch order) and the group
+ * row window as moe_grouped_gemm_swiglu, whose token-rows-on-M kernel this is
+ * (used for every batch size); the same result bits as that call on the
+ * rows moe_permute gathers.  Not the layer's path: each gather4 moves 512
+ * bytes, and the 32 of them a 128-row tile needs per 128-byte K block make
+ * the copies, not the MMAs or the promotion, set the pace (same box, R1
+ * layer: gate/up 1.87 -> 3.72 ms at 4096 tokens, against a 48 us saving in
+ * the dispatch). */
+MOE_API int moe_grouped_gemm_swiglu_gather(const moe_config *cfg, int32_t groups, int32_t inter,
+                                           int32_t k_dim, int32_t rows, const void *x_rows,
+                                           const float *x_scales, int32_t T,
+                                           const int32_t *src_of_row,
+                                           const int32_t *expert_offsets, const void *w13,
+                                           const float *w13_scales, int32_t w_layout, void *h,
+                                           float *h_scales, int32_t min_group_rows,
+                                           int32_t max_group_rows, int32_t *dev_status,
+                                           void *stream);
+
+/* ---- the experts' FFN in one kernel ------------------------------------------/* ---- the experts' FFN in one kernel ------------------------------------------
  * For the rows r of every group g (offsets as in moe_grouped_gemm):
  *   g, u = A[r] W13[g]^T     (W13 [groups, 2*inter, hidden], A [rows, hidden];
  *                             FP8: e4m3 with block scales w13_scales fp32

@@ -73,7 +73,9 @@ _SIGS = {
     "moe_act_requant": [_CP, _I, _I, _P, _P, _P, _P, _P],
     "moe_route_quantize": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
     "moe_permute_workspace_size": [_CP, _I, ctypes.POINTER(ctypes.c_size_t)],
-    "moe_permute": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P, _P],
+    "moe_permute": [_CP, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _I, _P, _P],
+    "moe_grouped_gemm_swiglu_gather": [_CP, _I, _I, _I, _I, _P, _P, _I, _P, _P, _P, _P, _I, _P,
+                                       _P, _I, _I, _P, _P],
     "moe_grouped_gemm": [_CP, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _I, _I, _I, _P, _P],
     "moe_combine": [_CP, _I, _P, _P, _P, _P, _P, _I, _P],
     "moe_workspace_size": [_CP, ctypes.POINTER(ctypes.c_size_t)],
@@ -202,11 +204,12 @@ def permute_workspace_size(cfg: Config, T: int) -> int:
 
 
 def permute(cfg: Config, T, topk_ids, x_rows, x_scales, expert_offsets, src_of_row,
-            row_of_slot, xp, xp_scales, ws, ws_bytes, status=None, stream=None):
+            row_of_slot, xp, xp_scales, ws, ws_bytes, status=None, stream=None,
+            copy_max_group_rows=0x7FFFFFFF):
     _check(lib().moe_permute(ctypes.byref(cfg), T, _ptr(topk_ids), _ptr(x_rows), _ptr(x_scales),
                              _ptr(expert_offsets), _ptr(src_of_row), _ptr(row_of_slot),
-                             _ptr(xp), _ptr(xp_scales), _ptr(ws), ws_bytes, _ptr(status),
-                             _stream(stream)), "moe_permute")
+                             _ptr(xp), _ptr(xp_scales), _ptr(ws), ws_bytes, copy_max_group_rows,
+                             _ptr(status), _stream(stream)), "moe_permute")
 
 
 def permute_static_scratch(cfg: Config, T, topk_ids, x_rows, x_scales, expert_offsets,
@@ -245,6 +248,18 @@ def grouped_gemm_swiglu(cfg: Config, groups, inter, k_dim, rows, a, a_scales, ex
                                          _ptr(h_scales), min_group_rows, max_group_rows,
                                          _ptr(status), _stream(stream)),
            "moe_grouped_gemm_swiglu")
+
+
+def grouped_gemm_swiglu_gather(cfg: Config, groups, inter, k_dim, rows, x_rows, x_scales, T,
+                               src_of_row, expert_offsets, w13, w13_scales, h, h_scales,
+                               status=None, stream=None, w_layout=None, min_group_rows=0,
+                               max_group_rows=ALL_ROWS):
+    """The gate/up GEMM with SwiGLU on rows gathered from the token rows of x (FP8)."""
+    _check(lib().moe_grouped_gemm_swiglu_gather(
+        ctypes.byref(cfg), groups, inter, k_dim, rows, _ptr(x_rows), _ptr(x_scales), T,
+        _ptr(src_of_row), _ptr(expert_offsets), _ptr(w13), _ptr(w13_scales),
+        LAYOUT_ROWS if w_layout is None else w_layout, _ptr(h), _ptr(h_scales), min_group_rows,
+        max_group_rows, _ptr(status), _stream(stream)), "moe_grouped_gemm_swiglu_gather")
 
 
 def pack_expert_weights(cfg: Config, w, out=None, stream=None):

@@ -248,11 +248,11 @@ int moe_permute_workspace_size(const moe_config *cfg, int32_t T, size_t *bytes) 
 int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_ids, const void *x_rows,
                 const float *x_scales, int32_t *expert_offsets, int32_t *src_of_row,
                 int32_t *row_of_slot, void *xp, float *xp_scales, void *ws, size_t ws_bytes,
-                int32_t *dev_status, void *stream) {
+                int32_t copy_max_group_rows, int32_t *dev_status, void *stream) {
     Range range("moe_permute");
     int rc = check_config(cfg);
     if (rc) return rc;
-    if (T < 0 || !expert_offsets) return MOE_ERR_INVALID_ARG;
+    if (T < 0 || !expert_offsets || copy_max_group_rows < 0) return MOE_ERR_INVALID_ARG;
     const bool fp8 = cfg->dtype == MOE_DTYPE_FP8_BLOCK128;
     if (T > 0 && (!topk_ids || !x_rows || !src_of_row || !row_of_slot || !xp ||
                   (fp8 && (!x_scales || !xp_scales))))
@@ -262,7 +262,7 @@ int moe_permute(const moe_config *cfg, int32_t T, const int32_t *topk_ids, const
         return MOE_ERR_WORKSPACE_TOO_SMALL;
     return launch_permute(cfg, T, topk_ids, x_rows, x_scales, expert_offsets, src_of_row,
                           row_of_slot, xp, xp_scales, ws, dev_status,
-                          static_cast<cudaStream_t>(stream));
+                          static_cast<cudaStream_t>(stream), copy_max_group_rows);
 }
 
 int moe_grouped_gemm(const moe_config *cfg, int32_t groups, int32_t n_out, int32_t k_dim,
@@ -321,6 +321,38 @@ int moe_grouped_gemm_swiglu(const moe_config *cfg, int32_t groups, int32_t inter
                                       w_layout == MOE_LAYOUT_TILES, h, h_scales, dev_status,
                                       static_cast<cudaStream_t>(stream), min_group_rows,
                                       max_group_rows);
+}
+
+int moe_grouped_gemm_swiglu_gather(const moe_config *cfg, int32_t groups, int32_t inter,
+                                   int32_t k_dim, int32_t rows, const void *x_rows,
+                                   const float *x_scales, int32_t T, const int32_t *src_of_row,
+                                   const int32_t *expert_offsets, const void *w13,
+                                   const float *w13_scales, int32_t w_layout, void *h,
+                                   float *h_scales, int32_t min_group_rows,
+                                   int32_t max_group_rows, int32_t *dev_status, void *stream) {
+    Range range("moe_grouped_gemm_swiglu_gather");
+    int rc = check_config(cfg);
+    if (rc) return rc;
+    if (cfg->dtype != MOE_DTYPE_FP8_BLOCK128) return MOE_ERR_INVALID_ARG;
+    if (groups <= 0 || rows < 0 || T < 0 || inter <= 0 || k_dim <= 0 || min_group_rows < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (!layout_ok(w_layout)) return MOE_ERR_INVALID_ARG;
+    if (groups > 1024) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (inter % 128 || k_dim % 128 || k_dim > 7168) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)groups * 2 * inter > INT32_MAX) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (w_layout == MOE_LAYOUT_TILES && !tiled_fits(groups, 2 * (int64_t)inter, k_dim, true))
+        return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (T == 0) return MOE_ERR_INVALID_ARG;   // rows to fill but no token rows
+    if (!x_rows || !x_scales || !src_of_row || !expert_offsets || !w13 || !w13_scales || !h ||
+        !h_scales)
+        return MOE_ERR_INVALID_ARG;
+    if (!al16(x_rows) || !al16(w13) || !al16(h)) return MOE_ERR_INVALID_ARG;
+    return launch_swiglu_wide_gather(groups, inter, k_dim, rows, x_rows, x_scales, T,
+                                     cfg->top_k, src_of_row, expert_offsets, w13, w13_scales,
+                                     w_layout == MOE_LAYOUT_TILES, h, h_scales, dev_status,
+                                     static_cast<cudaStream_t>(stream), min_group_rows,
+                                     max_group_rows);
 }
 
 size_t moe_expert_ffn_sched_bytes(int32_t groups, int32_t rows) {

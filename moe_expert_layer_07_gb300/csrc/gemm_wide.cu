@@ -30,7 +30,10 @@
 // 128 x 256 fp32 accumulators fill the SM), 10 warps:
 //   warp 0      TMA producer: per K block two 16 KB boxes of weight rows
 //               (row-major weights, or two contiguous 16 KB tiles of packed
-//               weights) and ceil(rows/32) 32-row activation boxes.
+//               weights) and ceil(rows/32) 32-row activation boxes -- or, in
+//               the SwiGLU kernel's gather mode, ceil(rows/4) gather4 copies
+//               of token rows of x straight into the tile's swizzled rows
+//               (the row gather of the dispatch, without materialised rows).
 //   warp 1      MMA issuer (one thread); the accumulator alternates between
 //               the two TMEM buffers per K block; completion via tcgen05.commit.
 //   warps 2..9  epilogue: warp w reads TMEM lane quarter (w & 3) -- token rows
@@ -92,8 +95,24 @@ struct WideArgs {
     float *c;                // plain: [rows, n_out] fp32
     int w_tiled;             // W in MOE_LAYOUT_TILES
     int min_rows, max_rows;  // groups whose row count lies outside are skipped
+    // Row gather (SwiGLU): with src_of_row set, row r of a tile is token
+    // t(r)'s row of the [T, k_dim] activations that tmA then maps (one row per
+    // box), fetched by TMA gather4, and its scales are x_scales[t(r)]; t(r)
+    // follows the dispatch's slot numbering (token_of_slot).
+    const int32_t *src_of_row;   // [rows]: the slot of each row; null: A in row order
+    const float *x_scales;       // [T, k_dim / 128]
+    int T, k;
     int32_t *status;
 };
+
+// Token of dispatch slot s: routed slots t k + j, then the shared experts'
+// slots T k + i T + t.  Clamped into [0, T) so that a gather stays in bounds
+// whatever the table holds.
+__device__ __forceinline__ int token_of_slot(int s, int T, int k) {
+    const int R = T * k;
+    const int t = s < R ? s / k : (s - R) % T;
+    return min(max(t, 0), T - 1);
+}
 
 struct WTile {
     int g, nt, row0, nvalid;
@@ -126,7 +145,7 @@ __device__ __forceinline__ float hi_f(uint64_t v) { return __uint_as_float((uint
 // A register file of 64K words is split over the SM's four sub-partitions;
 // with 10 warps two sub-partitions hold 3 warps, so a thread gets at most
 // 16384 / 96 -> 168 registers.
-template <bool SW>
+template <bool SW, bool GATHER = false>
 __global__ void __launch_bounds__(kThreads, 1)
     wide_gemm_kernel(const __grid_constant__ CUtensorMap tmW,
                      const __grid_constant__ CUtensorMap tmA,
@@ -226,6 +245,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicOr(args.status, MOE_DEV_BAD_OFFSETS);
 
     if (warp == 0) {
+      if constexpr (GATHER) {
+        // ------------------------------ TMA producer (gather mode)
+        // Lane 0 waits for free stages and loads the weight boxes; every lane
+        // L then fetches token rows 4L .. 4L + 3 of the tile with one gather4.
+        constexpr bool gather = true;
+        // A weight tile is read by every token tile of its group: those
+        // run on neighbouring CTAs at about the same time and share the L2
+        // copy.  An activation tile is re-read by every column tile.
+        const uint64_t pol_w_once = policy_evict_first();
+        const uint64_t pol_w_shared = policy_evict_normal();
+        const uint64_t pol_a = policy_evict_last();
+        int stage = 0;
+        uint32_t phase = 0, issued = 0, parity_bits = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const WTile tl = decode_wtile(t, G, s_tiles, s_off);
+            int tok[4] = {0, 0, 0, 0};
+            int ngather = 0;
+            if (gather) {   // this lane's four rows (the tile's last row repeats past nvalid)
+                ngather = (tl.nvalid + 3) / 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int r = min(4 * lane + i, tl.nvalid - 1);
+                    tok[i] = token_of_slot(args.src_of_row[tl.row0 + r], args.T, args.k);
+                }
+            }
+            const int nbox = gather ? 0 : (tl.nvalid + kABox - 1) / kABox;
+            const uint32_t bytes = kBBytes + (uint32_t)(gather ? ngather * 4 : nbox * kABox) * 128;
+            // the two 128-row weight blocks of the tile: SwiGLU, gate
+            // block nt and up block NT + nt; plain, blocks 2 nt, 2 nt + 1
+            const int b0 = tl.g * MTW + (SW ? tl.nt : 2 * tl.nt);
+            const int b1 = SW ? b0 + NT : b0 + 1;
+            const uint64_t pol_w =
+                (s_off[tl.g + 1] - s_off[tl.g] > kTM) ? pol_w_shared : pol_w_once;
+            for (int kb = 0; kb < KB; ++kb) {
+                int free_stage = 1;
+                if (lane == 0)
+                    free_stage = wait_bounded(smem_u32(&empty_bar[stage]), phase ^ 1u, abort_flag,
+                                              args.status, MOE_DEV_TIMEOUT);
+                if (!__shfl_sync(0xffffffffu, free_stage, 0)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t sa = smem_base + stage * kStageBytes;
+                const uint32_t sb = sa + kABytes;
+                const uint32_t fb = smem_u32(&full_bar[stage]);
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, bytes);
+                    if (args.w_tiled) {   // tile (block b, K block kb) = rows (b KB + kb) 128
+                        tma_load_2d(sb, &tmW, 0, (b0 * KB + kb) * 128, fb, pol_w);
+                        tma_load_2d(sb + 128 * 128, &tmW, 0, (b1 * KB + kb) * 128, fb, pol_w);
+                    } else {
+                        tma_load_2d(sb, &tmW, kb * 128, b0 * 128, fb, pol_w);
+                        tma_load_2d(sb + 128 * 128, &tmW, kb * 128, b1 * 128, fb, pol_w);
+                    }
+                    for (int b = 0; b < nbox; ++b)
+                        tma_load_2d(sa + b * kABox * 128, &tmA, kb * 128, tl.row0 + b * kABox, fb,
+                                    pol_a);
+                }
+                __syncwarp();   // the stage's byte count is posted before any gather lands
+                if (lane < ngather)
+                    tma_gather4(sa + lane * 4 * 128, &tmA, kb * 128, tok[0], tok[1], tok[2],
+                                tok[3], fb, pol_a);
+                issued |= 1u << stage;
+                parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+                if (++stage == kStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok && lane == 0) {   // let every copy in flight land before the CTA exits
+            for (int s = 0; s < kStages; ++s)
+                if ((issued >> s) & 1u) wait_drain(smem_u32(&full_bar[s]), (parity_bits >> s) & 1u);
+        }
+        __syncwarp();
+      } else {
         // ------------------------------ TMA producer
         if (lane == 0) {
             // A weight tile is read by every token tile of its group: those
@@ -281,6 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         __syncwarp();
+      }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer
         if (lane == 0) {
@@ -341,7 +438,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const WTile tl = decode_wtile(t, G, s_tiles, s_off);
             const bool valid = m < tl.nvalid;
             const int row = tl.row0 + (valid ? m : 0);
-            const float *xsp = args.a_scales + (size_t)row * KB;
+            const float *xsp;
+            if constexpr (GATHER)
+                xsp = args.x_scales + (size_t)token_of_slot(args.src_of_row[row], args.T, args.k) * KB;
+            else
+                xsp = args.a_scales + (size_t)row * KB;
             // block scales: SwiGLU, gate block nt (chunks 0-3) and up block
             // NT + nt (chunks 4-7); plain, block 2 nt + wgp for all chunks
             const float *wsp =
@@ -484,10 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <bool SW>
+template <bool SW, bool GATHER = false>
 int launch_wide(const WideArgs &args, const void *a, const void *w, cudaStream_t s) {
     using Sh = WideShape<SW>;
-    auto kern = wide_gemm_kernel<SW>;
+    auto kern = wide_gemm_kernel<SW, GATHER>;
     static std::once_flag attr_once[64];
     static int attr_rc[64];
     int dev = 0;
@@ -506,7 +607,10 @@ int launch_wide(const WideArgs &args, const void *a, const void *w, cudaStream_t
             : encode_2d(&tmW, w, true, (uint64_t)args.k_dim, (uint64_t)args.groups * args.n_out,
                         128);
     if (!tmw_ok) return cuda_fail("cuTensorMapEncodeTiled (weights)");
-    if (!encode_2d(&tmA, a, true, (uint64_t)args.k_dim, (uint64_t)args.rows, kABox))
+    // activations: the dispatched rows in boxes of 32, or (gather) the token
+    // rows of x, one row per box as gather4 requires
+    if (!(GATHER ? encode_2d(&tmA, a, true, (uint64_t)args.k_dim, (uint64_t)args.T, 1)
+                 : encode_2d(&tmA, a, true, (uint64_t)args.k_dim, (uint64_t)args.rows, kABox)))
         return cuda_fail("cuTensorMapEncodeTiled (activations)");
     if (SW) {
         tmC = tmA;   // unused by the SwiGLU epilogue
@@ -537,6 +641,10 @@ WideArgs wide_args(int groups, int n_out, int k_dim, int rows, const float *a_sc
     args.h_scales = nullptr;
     args.c = nullptr;
     args.w_tiled = w_tiled;
+    args.src_of_row = nullptr;
+    args.x_scales = nullptr;
+    args.T = 0;
+    args.k = 0;
     args.min_rows = 0;
     args.max_rows = 0x7fffffff;
     args.status = status;
@@ -557,6 +665,25 @@ int launch_swiglu_wide(int groups, int inter, int k_dim, int rows, const void *a
     args.h = static_cast<uint8_t *>(h);
     args.h_scales = h_scales;
     return launch_wide<true>(args, a, w13, s);
+}
+
+int launch_swiglu_wide_gather(int groups, int inter, int k_dim, int rows, const void *xq,
+                              const float *xs, int T, int top_k, const int32_t *src_of_row,
+                              const int32_t *offsets, const void *w13, const float *w13_scales,
+                              bool w_tiled, void *h, float *h_scales, int32_t *status,
+                              cudaStream_t s, int min_rows, int max_rows) {
+    if (rows == 0 || T == 0) return MOE_OK;
+    WideArgs args = wide_args(groups, 2 * inter, k_dim, rows, nullptr, offsets, w13_scales,
+                              w_tiled, status);
+    args.h = static_cast<uint8_t *>(h);
+    args.h_scales = h_scales;
+    args.src_of_row = src_of_row;
+    args.x_scales = xs;
+    args.T = T;
+    args.k = top_k;
+    args.min_rows = min_rows;
+    args.max_rows = max_rows;
+    return launch_wide<true, true>(args, xq, w13, s);
 }
 
 int launch_gemm_wide(int groups, int n_out, int k_dim, int rows, const void *a,

@@ -52,10 +52,12 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
 int launch_act_requant(const moe_config *cfg, int mode, int rows, const int32_t *rows_dev,
                        const void *in, void *out, float *out_scales, cudaStream_t s);
 size_t permute_scratch_bytes(const moe_config *cfg, int T);
+// Rows of groups with more than copy_max_rows rows get their table entries
+// but are not copied into xp / xp_scales.
 int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const void *x_rows,
                    const float *x_scales, int32_t *offsets, int32_t *src_of_row,
                    int32_t *row_of_slot, void *xp, float *xp_scales, void *ws,
-                   int32_t *status, cudaStream_t s);
+                   int32_t *status, cudaStream_t s, int copy_max_rows = 0x7fffffff);
 // Row windows: every expert launcher below processes only the groups whose
 // row count n satisfies min_rows <= n <= max_rows (the others' rows of its
 // outputs are left as they are), so that groups of few and of many rows can
@@ -78,6 +80,15 @@ int launch_swiglu_wide(int groups, int inter, int k_dim, int rows, const void *a
                        const float *w13_scales, bool w_tiled, void *h, float *h_scales,
                        int32_t *status, cudaStream_t s, int min_rows = 0,
                        int max_rows = kAllRows);
+// The same with the activation rows gathered (TMA gather4) from the token
+// rows of x: row r of group g is token t(r) of slot src_of_row[r] (routed
+// slots t top_k + j, then the shared experts' T rows each); xq e4m3
+// [T, k_dim], xs fp32 [T, k_dim / 128].  Same result bits as on dispatched rows.
+int launch_swiglu_wide_gather(int groups, int inter, int k_dim, int rows, const void *xq,
+                              const float *xs, int T, int top_k, const int32_t *src_of_row,
+                              const int32_t *offsets, const void *w13, const float *w13_scales,
+                              bool w_tiled, void *h, float *h_scales, int32_t *status,
+                              cudaStream_t s, int min_rows = 0, int max_rows = kAllRows);
 // Wide FP8 batches, fp32 C with n_out a multiple of 256: the same kernel
 // with a plain epilogue (TMA stores of 32 x 32 fp32 blocks).
 int launch_gemm_wide(int groups, int n_out, int k_dim, int rows, const void *a,

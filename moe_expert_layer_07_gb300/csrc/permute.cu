@@ -17,7 +17,9 @@
 //                    expert_offsets (shared experts: T rows each), and the
 //                    first row of every (chunk, expert).
 //   permute_scatter  one warp per row: writes row_of_slot / src_of_row and
-//                    copies the row (16-byte vectors) and its scales.
+//                    copies the row (16-byte vectors) and its scales, unless
+//                    the row's group has more rows than copy_max_rows (a
+//                    GEMM that gathers the token rows itself reads them).
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -37,6 +39,7 @@ struct PermArgs {
     int32_t *chunk_counts;   // [chunks, E]
     int32_t *chunk_base;     // [chunks, E]
     int32_t *local_rank;     // [T*k]
+    int copy_max_rows;       // rows of groups with more rows are not copied (tables only)
     int32_t *status;
 };
 
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const PermArgs a) 
     const long Rtot = R + (long)a.S * a.T;
     if (w >= Rtot) return;
     long row;
-    int t;
+    int t, group_rows;
     if (w < R) {
         const int e = a.ids[w];
         if (e < 0 || e >= a.E) {   // reported by permute_count
@@ -180,6 +183,7 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const PermArgs a) 
         }
         row = a.chunk_base[(w / kChunk) * a.E + e] + a.local_rank[w];
         t = (int)(w / a.k);
+        group_rows = a.offsets[e + 1] - a.offsets[e];
         if (lane == 0) {
             a.row_of_slot[w] = (int32_t)row;
             a.src_of_row[row] = (int32_t)w;
@@ -189,8 +193,10 @@ __global__ void __launch_bounds__(256) permute_scatter_kernel(const PermArgs a) 
         const int s = (int)(ws / a.T);
         t = (int)(ws % a.T);
         row = a.offsets[a.E + s] + t;
+        group_rows = a.T;
         if (lane == 0) a.src_of_row[row] = (int32_t)w;
     }
+    if (group_rows > a.copy_max_rows) return;   // its rows are gathered by the GEMM
     const long row_bytes = a.fp8 ? a.H : 2L * a.H;
     const uint4 *src = reinterpret_cast<const uint4 *>(a.x + (long)t * row_bytes);
     uint4 *dst = reinterpret_cast<uint4 *>(a.xp + row * row_bytes);
@@ -227,7 +233,7 @@ size_t permute_scratch_bytes(const moe_config *cfg, int T) {
 int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const void *x_rows,
                    const float *x_scales, int32_t *offsets, int32_t *src_of_row,
                    int32_t *row_of_slot, void *xp, float *xp_scales, void *ws,
-                   int32_t *status, cudaStream_t s) {
+                   int32_t *status, cudaStream_t s, int copy_max_rows) {
     PermArgs a;
     a.T = T;
     a.k = cfg->top_k;
@@ -250,6 +256,7 @@ int launch_permute(const moe_config *cfg, int T, const int32_t *topk_ids, const 
     a.chunk_counts = reinterpret_cast<int32_t *>(p);
     a.chunk_base = reinterpret_cast<int32_t *>(p + cc);
     a.local_rank = reinterpret_cast<int32_t *>(p + 2 * cc);
+    a.copy_max_rows = copy_max_rows;
     a.status = status;
 
     const size_t smem = 32 * sizeof(int32_t) * (size_t)a.E;

@@ -169,6 +169,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// Four rows r0..r3 (any order, any rows of the tensor) of 2-D tensor map
+// `tmap`, each one box of the map (whose box is one row high), starting at
+// column c0, into four consecutive box-sized rows of shared memory at dst;
+// completes on `bar` like tma_load_2d.  With a 128-byte swizzle the rows land
+// as rows (dst / 128) mod 8 .. of a tiled box would: the swizzle follows the
+// shared-memory address.  c0's byte offset must be a multiple of 16.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const void *tmap, int32_t c0,
+                                            int32_t r0, int32_t r1, int32_t r2, int32_t r3,
+                                            uint32_t bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+        "r"(bar), "l"(policy)
+        : "memory");
+}
+
 // 2-D tiled store of one box from shared memory (bulk-group completion).
 // c0 is the innermost coordinate in elements (its byte offset must be a
 // multiple of 16, and neither coordinate may be negative), c1 the row.

@@ -138,7 +138,21 @@ def test_bad_arguments_are_rejected_before_launch(L):
     # workspace too small
     need = moe.permute_workspace_size(cfg, 37)
     assert L.moe_permute(ctypes.byref(cfg), 37, fake, fake, fake, fake, fake, fake, fake, fake,
-                         fake, need - 1, None, None) == -3
+                         fake, need - 1, ALL, None, None) == -3
+    assert L.moe_permute(ctypes.byref(cfg), 37, fake, fake, fake, fake, fake, fake, fake, fake,
+                         fake, need, -1, None, None) == -1   # a negative copy window
+    # the gathering gate/up GEMM: FP8 only, token rows needed, known layouts
+    gg = lambda c, T, rows, layout=0, lo=0, xr=fake: L.moe_grouped_gemm_swiglu_gather(
+        ctypes.byref(c), 3, 256, 1024, rows, xr, fake, T, fake, fake, fake, fake, layout, fake,
+        fake, lo, ALL, None, None)
+    b16c = moe.make_config(synth.CONFIGS["bf16_mini"])
+    assert gg(b16c, 4, 10) == -1          # BF16 layer
+    assert gg(cfg, 4, 10, layout=3) == -1
+    assert gg(cfg, 4, 10, lo=-1) == -1
+    assert gg(cfg, 0, 10) == -1           # rows to fill, no token rows
+    assert gg(cfg, 4, 10, xr=None) == -1
+    assert gg(cfg, 4, 10, xr=P(0x1004)) == -1   # unaligned token rows
+    assert gg(cfg, 4, 0) == 0             # nothing to do
     # identity quantisation (alone or with routing) needs an FP8 layer; unknown enums
     b16 = moe.make_config(synth.CONFIGS["bf16_mini"])
     assert L.moe_route_quantize(ctypes.byref(b16), 4, fake, fake, None, None, None, fake, fake,

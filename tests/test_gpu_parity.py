@@ -553,9 +553,10 @@ def test_layer_all_tokens_on_few_experts(lib):
     check_close(to_np(out), ref["out"], FP8_TOL)
 
 
-@pytest.mark.parametrize("name", ["r1_mini", "r1_mini_i512"])
-def test_layer_deterministic_and_graph_capturable(lib, name):
-    wl = workload(name)
+@pytest.mark.parametrize("name,T", [("r1_mini", None), ("r1_mini_i512", None),
+                                    ("r1_mini", 130)])   # 130 tokens: the wide-batch path
+def test_layer_deterministic_and_graph_capturable(lib, name, T):
+    wl = workload(name, T=T)
     layer, out1 = run_layer(wl)
     _, out2 = run_layer(wl, layer=layer)
     assert torch.equal(out1, out2)
@@ -684,6 +685,82 @@ def dataclasses_replace(shape, **kw):
     return dataclasses.replace(shape, **kw)
 
 
+@pytest.mark.parametrize("name,T,window", [("r1_mini", 130, (0, moe.ALL_ROWS)),
+                                           ("r1_mini", 130, (33, moe.ALL_ROWS)),
+                                           ("r1_mini_zipf", None, (0, moe.ALL_ROWS)),
+                                           ("r1_mini", 1, (0, moe.ALL_ROWS)),
+                                           ("r1_prefill_t4096", None, (33, moe.ALL_ROWS))])
+def test_swiglu_gather_equals_swiglu_on_dispatched_rows(lib, name, T, window):
+    """The gate/up GEMM that gathers its rows from the token rows of x (TMA
+    gather4) gives the bits of moe_grouped_gemm_swiglu on the rows the
+    dispatch copies; the dispatch's copy window leaves the other groups' rows
+    uncopied and its tables unchanged."""
+    wl = workload(name, T=T)
+    s = wl.shape
+    T = s.tokens
+    cfg = moe.make_config(s)
+    G, H, I = s.groups, s.hidden, s.inter
+    rows = T * (s.top_k + s.num_shared)
+    layer = wl.layer()
+    out = torch.empty((T, H), device="cuda")
+    layer.forward(wl.dev["x"], out)   # routing, x quantisation and dispatch
+    torch.cuda.synchronize()
+    L, base = layer.layout, layer.ws.data_ptr()
+    xq, xs = base + L.xq, base + L.xs
+    ids = layer.view("topk_ids", torch.int32, (T, s.top_k))
+    off_full = layer.view("expert_offsets", torch.int32, (G + 1,)).clone()
+    src_full = layer.view("src_of_row", torch.int32, (rows,)).clone()
+    # the dispatch again, copying every row, and with the layer's copy window
+    perm = {}
+    for cap in (moe.ALL_ROWS, 32):
+        r = dict(off=torch.full((G + 1,), -5, dtype=torch.int32, device="cuda"),
+                 src=torch.full((rows,), -5, dtype=torch.int32, device="cuda"),
+                 ros=torch.full((T, s.top_k), -5, dtype=torch.int32, device="cuda"),
+                 xp=torch.full((rows, H), 0x55, dtype=torch.uint8, device="cuda"),
+                 xps=torch.full((rows, H // 128), -1.0, device="cuda"))
+        nws = moe.permute_workspace_size(cfg, T)
+        ws = torch.empty(max(nws, 1), dtype=torch.uint8, device="cuda")
+        moe.permute(cfg, T, ids, xq, xs, r["off"], r["src"], r["ros"], r["xp"], r["xps"], ws, nws,
+                    copy_max_group_rows=cap)
+        perm[cap] = r
+    torch.cuda.synchronize()
+    a, b = perm[moe.ALL_ROWS], perm[32]
+    for key in ("off", "src", "ros"):
+        assert torch.equal(a[key], b[key])
+    assert torch.equal(a["off"], off_full) and torch.equal(a["src"], src_full)
+    offs = to_np(a["off"])
+    counts = np.diff(offs)
+    small = np.zeros(rows, bool)
+    for g in np.nonzero(counts <= 32)[0]:
+        small[offs[g]:offs[g + 1]] = True
+    small_t = torch.as_tensor(small, device="cuda")
+    assert torch.equal(b["xp"][small_t], a["xp"][small_t])
+    assert torch.all(b["xp"][~small_t] == 0x55) and torch.all(b["xps"][~small_t] == -1.0)
+    # gate/up + SwiGLU on the copied rows against the gathered ones
+    w = layer._keep
+    outs = []
+    for gather in (False, True):
+        h = torch.full((rows, I), 0x55, dtype=torch.uint8, device="cuda")
+        hs = torch.full((rows, I // 128), -1.0, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        if gather:
+            moe.grouped_gemm_swiglu_gather(cfg, G, I, H, rows, xq, xs, T, a["src"], a["off"],
+                                           w["w13"], w["w13_s"], h, hs, st,
+                                           w_layout=layer.expert_layout,
+                                           min_group_rows=window[0], max_group_rows=window[1])
+        else:
+            moe.grouped_gemm_swiglu(cfg, G, I, H, rows, a["xp"], a["xps"], a["off"], w["w13"],
+                                    w["w13_s"], h, hs, st, w_layout=layer.expert_layout,
+                                    min_group_rows=window[0], max_group_rows=window[1])
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        outs.append((h, hs))
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    if window[0] > 0:   # the window's groups only
+        inside = torch.as_tensor(np.repeat(counts >= window[0], counts), device="cuda")
+        assert torch.all(outs[1][0][~inside] == 0x55)
+
+
 @pytest.mark.parametrize("name,T", [("r1_mini_zipf", None), ("r1_mini", 130), ("bf16_mini", None)])
 def test_group_row_windows_partition_the_groups(lib, name, T):
     """The group row windows of the expert entry points: the one-kernel FFN on
@@ -696,13 +773,19 @@ def test_group_row_windows_partition_the_groups(lib, name, T):
     s = wl.shape
     out = torch.empty((s.tokens, s.hidden), device="cuda")
     layer.forward(wl.dev["x"], out)   # routing and dispatch into the workspace
-    torch.cuda.synchronize()
     cfg, w, wlay = layer.cfg, layer._keep, layer.expert_layout
     G, H, I = s.groups, s.hidden, s.inter
     rows = s.tokens * (s.top_k + s.num_shared)
     L, base = layer.layout, layer.ws.data_ptr()
     fp8 = s.dtype == "fp8"
     xp, xps, off = base + L.xp, (base + L.xp_scales) if fp8 else None, base + L.expert_offsets
+    # the dispatch again with every row copied (wide layer calls copy only the
+    # groups the FFN reads and let the gate/up GEMM gather the others)
+    nws = moe.permute_workspace_size(cfg, s.tokens)
+    moe.permute(cfg, s.tokens, base + L.topk_ids, (base + L.xq) if fp8 else wl.dev["x"],
+                (base + L.xs) if fp8 else None, off, base + L.src_of_row, base + L.row_of_slot,
+                xp, xps, base + L.perm_scratch, nws)
+    torch.cuda.synchronize()
     offs = to_np(layer.view("expert_offsets", torch.int32, (G + 1,)))
     counts = np.diff(offs)
     X = int(np.median(counts[counts > 0]))
