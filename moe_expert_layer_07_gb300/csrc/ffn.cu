@@ -678,7 +678,8 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                                                      fmaxf(s_amax[b][2 * kBN + n], s_amax[b][3 * kBN + n]));
                             const float sc = fp8_group_scale(amax);
                             const size_t row = (size_t)(u.row0 + n);
-                            args.h[row * I + u.mt * kBM + m_local] = fp8_code(acc[j], sc);
+                            args.h[row * I + u.mt * kBM + m_local] =
+                                fp8_code(acc[j], fp8_group_inv(sc));
                             if (m_local == 0) args.h_scales[row * KB2 + u.mt] = sc;
                         }
                 }

@@ -580,7 +580,8 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                                                      fmaxf(s_amax[b][2 * BN + n], s_amax[b][3 * BN + n]));
                             const float sc = fp8_group_scale(amax);
                             const size_t row = (size_t)(tl.row0 + n);
-                            H8[row * n_h + tl.mt * kBM + m_local] = fp8_code(acc[n], sc);
+                            H8[row * n_h + tl.mt * kBM + m_local] =
+                                fp8_code(acc[n], fp8_group_inv(sc));
                             if (m_local == 0) args.h_scales[row * (n_h / 128) + tl.mt] = sc;
                         }
                 } else if (args.c_bf16) {

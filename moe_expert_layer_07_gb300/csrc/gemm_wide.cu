@@ -516,16 +516,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const float sc = fp8_group_scale(fmaxf(s_amax[par][0][m], s_amax[par][1][m]));
+                const float inv = fp8_group_inv(sc);
                 if (valid) {
                     const int inter = args.n_out / 2;
                     uint32_t w[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         const uint64_t a0 = acc[2 * i], a1 = acc[2 * i + 1];
-                        w[i] = (uint32_t)fp8_code(lo_f(a0), sc) |
-                               ((uint32_t)fp8_code(hi_f(a0), sc) << 8) |
-                               ((uint32_t)fp8_code(lo_f(a1), sc) << 16) |
-                               ((uint32_t)fp8_code(hi_f(a1), sc) << 24);
+                        w[i] = (uint32_t)fp8_code(lo_f(a0), inv) |
+                               ((uint32_t)fp8_code(hi_f(a0), inv) << 8) |
+                               ((uint32_t)fp8_code(lo_f(a1), inv) << 16) |
+                               ((uint32_t)fp8_code(hi_f(a1), inv) << 24);
                     }
                     uint4 *dst = reinterpret_cast<uint4 *>(args.h + (size_t)(tl.row0 + m) * inter +
                                                            tl.nt * 128 + wgp * 64);

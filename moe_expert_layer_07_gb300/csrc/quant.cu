@@ -61,9 +61,9 @@ __global__ void __launch_bounds__(256)
         float amax = fmaxf(fmaxf(fabsf(h[0]), fabsf(h[1])), fmaxf(fabsf(h[2]), fabsf(h[3])));
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        const float sc = fp8_group_scale(amax);
-        const uint32_t q = (uint32_t)e4m3x2(__fdiv_rn(h[0], sc), __fdiv_rn(h[1], sc)) |
-                           ((uint32_t)e4m3x2(__fdiv_rn(h[2], sc), __fdiv_rn(h[3], sc)) << 16);
+        const float sc = fp8_group_scale(amax), inv = fp8_group_inv(sc);
+        const uint32_t q = (uint32_t)e4m3x2(__fmul_rn(h[0], inv), __fmul_rn(h[1], inv)) |
+                           ((uint32_t)e4m3x2(__fmul_rn(h[2], inv), __fmul_rn(h[3], inv)) << 16);
         *reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(out) + row * I + col) = q;
         if (lane == 0) scales[row * (I / 128) + grp] = sc;
     } else {
