@@ -572,6 +572,7 @@ def measure(shape, args, world, rank, local, device, cpu):
     e2e = None
     if not args.no_e2e:
         e2e = end_to_end(layer, shape, x, device, args.steps, args.warmup, world)
+    replay = graph_replay(layer, shape, x, device)
     read_gbs = read_stream_gbs(layer, device)
 
     cpu_line = None
@@ -627,6 +628,7 @@ def measure(shape, args, world, rank, local, device, cpu):
         "device_status": status,
         "clocks": clocks.summary(),
         "e2e": e2e,
+        "graph_replay": replay,
         "cpu_baseline": cpu_line,
     }
     del stepper, layer, inp, x, out
@@ -668,6 +670,41 @@ def default_cpu_tokens(shape):
     # the whole batch up to 256 tokens: a pass of the R1 decode batch is a
     # few seconds of oracle work on a 16-core host
     return min(shape.tokens, 256)
+
+
+def graph_replay(layer, shape, x_dev, device, replays=50):
+    """The layer call captured once as a CUDA graph and replayed: the median of
+    `replays` replays, each timed alone with CUDA events on its stream, with a
+    256 MB fill (about twice L2) before each one, outside the events, so that
+    no replay finds the previous one's data in L2."""
+    import torch
+    T, H = shape.tokens, shape.hidden
+    out = torch.empty((T, H), dtype=torch.float32, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        layer.forward(x_dev, out)       # outside the capture: any lazy set-up
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        layer.forward(x_dev, out)
+    times = []
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(replays + 3):
+        flush.fill_(i & 255)
+        a.record()
+        graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        if i >= 3:
+            times.append(a.elapsed_time(b))
+    med = float(np.median(times))
+    del graph, flush, out
+    return {"median_ms": med, "value": T / (med / 1e3), "unit": "tokens/s", "replays": replays,
+            "l2_flush": "256 MB fill before every replay, outside the timed events",
+            "api": "moe_layer_forward captured in a CUDA graph"}
 
 
 def end_to_end(layer, shape, x_dev, device, steps, warmup, world):
