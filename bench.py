@@ -47,6 +47,7 @@ METRIC = "MoE-layer tokens/s at R1 shape (bs 128/1024); HBM GB/s and % of roofli
 DEFAULT_WORKLOAD = "r1_decode_t128"
 EXTRA_WORKLOADS = ("r1_zipf_t1024", "r1_prefill_t4096")
 NOMINAL_HBM_GBS = 8000.0   # GB300 HBM3e, about 8 TB/s
+L2_BYTES = 126 << 20       # GB300 L2 (about 129 MB)
 
 
 def load_peaks():
@@ -489,6 +490,50 @@ def read_stream_gbs(layer, device):
     return _READ_STREAM["gbs"]
 
 
+def l2_rotation(shape):
+    """How many copies of the layer the timed loops take in turn so that no
+    step finds its expert weights in L2: 1 when one layer's weights are more
+    than twice L2, else enough copies for two and a half L2s between two uses
+    of the same copy."""
+    w13, w2 = expert_weight_bytes(shape)
+    per_layer = shape.groups * (w13 + w2)
+    if per_layer > 2 * L2_BYTES:
+        return 1
+    return -(-(5 * L2_BYTES // 2) // per_layer) + 1
+
+
+class Rotation:
+    """Steppers over several copies of the layer (same inputs, own weights and
+    workspace), stepped in turn."""
+
+    def __init__(self, steppers):
+        self.all = steppers
+        self.i = 0
+
+    def __getattr__(self, name):
+        return getattr(self.all[0], name)
+
+    def step(self, record=None):
+        self.all[self.i % len(self.all)].step(record)
+        self.i += 1
+
+    def set_top(self):
+        for st in self.all:
+            st.set_top()
+
+    def top_ms(self):
+        ev = [e for st in self.all for e in st.top_events]
+        return sum(a.elapsed_time(b) for a, b in ev) / max(1, len(ev))
+
+    def kernel_ms(self):
+        n = [len(st.events) for st in self.all]
+        acc = {}
+        for st, k in zip(self.all, n):
+            for name, v in st.kernel_ms().items():
+                acc[name] = acc.get(name, 0.0) + v * k
+        return {name: v / max(1, sum(n)) for name, v in acc.items()}
+
+
 def measure(shape, args, world, rank, local, device, cpu):
     """All measurements of one workload (the layer resident only meanwhile)."""
     import torch
@@ -498,13 +543,18 @@ def measure(shape, args, world, rank, local, device, cpu):
     T, H = shape.tokens, shape.hidden
     x = inp["x"]
     out = torch.empty((T, H), dtype=torch.float32, device=device)
-    stepper = Stepper(layer, x, out)
-    for _ in range(args.warmup):
+    # weights that fit in L2 are taken from several copies in turn, so that
+    # every step streams them from HBM as the larger layers do
+    layers = [layer] + [moe.MoELayer(shape, inp, log2phys=log2phys)
+                        for _ in range(l2_rotation(shape) - 1)]
+    stepper = Rotation([Stepper(lay, x, out) for lay in layers])
+    for _ in range(args.warmup * len(layers)):
         stepper.step()
     torch.cuda.synchronize()
     stepper.set_top()
-    if layer.status() != 0:
-        raise RuntimeError(f"device status {layer.status()} after warm-up ({shape.name})")
+    for lay in layers:
+        if lay.status() != 0:
+            raise RuntimeError(f"device status {lay.status()} after warm-up ({shape.name})")
 
     def barrier():
         if world > 1:
@@ -522,7 +572,7 @@ def measure(shape, args, world, rank, local, device, cpu):
         torch.cuda.synchronize()
         barrier()
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world, device)
-    status = layer.status()
+    status = max(lay.status() for lay in layers)
     top_ms = stepper.top_ms()
     # per-stage split, after the timed region (events between all stages)
     for _ in range(min(args.steps, 50)):
@@ -571,7 +621,7 @@ def measure(shape, args, world, rank, local, device, cpu):
 
     e2e = None
     if not args.no_e2e:
-        e2e = end_to_end(layer, shape, x, device, args.steps, args.warmup, world)
+        e2e = end_to_end(layers, shape, x, device, args.steps, args.warmup, world)
     replay = graph_replay(layer, shape, x, device)
     read_gbs = read_stream_gbs(layer, device)
 
@@ -631,7 +681,7 @@ def measure(shape, args, world, rank, local, device, cpu):
         "graph_replay": replay,
         "cpu_baseline": cpu_line,
     }
-    del stepper, layer, inp, x, out
+    del stepper, layers, layer, inp, x, out
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
     return result
@@ -642,7 +692,15 @@ def workload_config(shape, world):
     return {"workload": shape.name, "tokens": shape.tokens, "hidden": shape.hidden,
             "inter": shape.inter, "experts": shape.num_experts, "shared": shape.num_shared,
             "top_k": shape.top_k, "parallelism": "replicas" if world > 1 else "single",
-            "l2": "inputs larger than L2 (expert weights streamed each step), no flush"}
+            "l2": l2_note(shape)}
+
+
+def l2_note(shape):
+    r = l2_rotation(shape)
+    if r == 1:
+        return "inputs larger than L2 (expert weights streamed each step), no flush"
+    return (f"inputs larger than L2: the timed loops take {r} copies of the layer's expert "
+            f"weights in turn, so no step finds its weights in L2; no flush")
 
 
 def replica_seed(seed, rank):
@@ -707,12 +765,12 @@ def graph_replay(layer, shape, x_dev, device, replays=50):
             "api": "moe_layer_forward captured in a CUDA graph"}
 
 
-def end_to_end(layer, shape, x_dev, device, steps, warmup, world):
+def end_to_end(layers, shape, x_dev, device, steps, warmup, world):
     """Tokens/s through the public layer call with every step's input copied
     from pinned host memory and its output read back.  As in a serving loop,
     step i+1's input copy and step i-1's output copy run on side streams
     while step i computes (device buffers double-buffered); the layer calls
-    themselves run in order on one stream."""
+    themselves run in order on one stream, step i on layers[i % len(layers)]."""
     import torch
     T, H = shape.tokens, shape.hidden
     x_host = x_dev.cpu().pin_memory()
@@ -735,7 +793,7 @@ def end_to_end(layer, shape, x_dev, device, steps, warmup, world):
         with torch.cuda.stream(s_run):      # the layer, in order
             s_run.wait_event(x_ready[b])
             s_run.wait_event(o_read[b])
-            layer.forward(xd[b], od[b], stream=s_run)
+            layers[i % len(layers)].forward(xd[b], od[b], stream=s_run)
             x_used[b].record(s_run)
             o_ready[b].record(s_run)
         with torch.cuda.stream(s_out):      # result of step i back to the host
@@ -743,7 +801,7 @@ def end_to_end(layer, shape, x_dev, device, steps, warmup, world):
             out_host[b].copy_(od[b], non_blocking=True)
             o_read[b].record(s_out)
 
-    for i in range(warmup):
+    for i in range(warmup * len(layers)):
         step(i)
     torch.cuda.synchronize()
     n = max(1, steps // 2)
