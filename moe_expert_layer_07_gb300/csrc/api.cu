@@ -511,14 +511,19 @@ int moe_layer_forward(const moe_config *cfg, const moe_weights *w, int32_t T, co
     // (expert u / (inter/128), weight tile u % (inter/128)).  Their first K
     // blocks go to L2 while routing leaves HBM idle: 12 of R1's 56 K blocks,
     // about 117 MB (8 blocks gained 11 us per layer over 4, and 12 another 2 us).
+    // BF16 layers take none: with it, the layer call (captured in a graph, L2
+    // flushed before each replay) took 0.231 ms instead of 0.218 for the
+    // V2-Lite-sized layer and 0.079 ms instead of 0.048 for 64 tokens over 16
+    // experts.
     L2Prefetch pf;
-    if (fused) {
+    if (fused && fp8) {
         pf.w13 = static_cast<const uint8_t *>(w->w13);
         pf.hidden = H;
         pf.inter = I;
         pf.groups = G;
         pf.units = 2 * sm_count();
-        pf.bytes = H < 1536 ? H : 1536;
+        pf.elem_bytes = fp8 ? 1 : 2;
+        pf.bytes = H * pf.elem_bytes < 1536 ? H * pf.elem_bytes : 1536;
         pf.tiled = tiled;
     }
     // FP8: the selection kernel also quantises x (while the logits run)

@@ -38,8 +38,9 @@ int cuda_fail(const char *where, cudaError_t e = cudaSuccess);
 // gate and up row of the first `units` gate/up units, taking unit u as
 // (expert u / (inter/128), weight tile u % (inter/128)).
 struct L2Prefetch {
-    const uint8_t *w13 = nullptr;   // e4m3 [groups, 2*inter, hidden]
+    const uint8_t *w13 = nullptr;   // e4m3 or bf16 [groups, 2*inter, hidden]
     int hidden = 0, inter = 0, groups = 0, units = 0, bytes = 0;
+    int elem_bytes = 1;             // 1 (e4m3) or 2 (bf16)
     int tiled = 0;                  // MOE_LAYOUT_TILES: the K prefix of a row block is contiguous
 };
 // With xq and xs (FP8 layers), the selection kernel also quantises x

@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(TB == 4 ? 256 : 128)
     if (pf.units > 0 && pf.tiled) {
         // tiled weights: the first K blocks of a 128-row block are one
         // contiguous run of 16 KB tiles; one prefetch per tile
-        const int mt1 = pf.inter / 128, kbt = pf.hidden / 128, nt = pf.bytes / 128;
+        const int mt1 = pf.inter / 128, kbt = pf.hidden * pf.elem_bytes / 128;
+        const int nt = pf.bytes / 128;
         const long jobs = (long)pf.units * 2 * nt;
         const long nthreads = (long)gridDim.x * gridDim.y * blockDim.x;
         for (long j = ((long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
@@ -111,7 +112,7 @@ __global__ void __launch_bounds__(TB == 4 ? 256 : 128)
             const int g = u / mt1, mt = u - g * mt1;
             if (g >= pf.groups) break;
             const long row = (long)g * 2 * pf.inter + (r < 128 ? 0 : pf.inter) + mt * 128 + (r & 127);
-            ptx::prefetch_l2(pf.w13 + row * pf.hidden, (uint32_t)pf.bytes);
+            ptx::prefetch_l2(pf.w13 + row * pf.hidden * pf.elem_bytes, (uint32_t)pf.bytes);
         }
     }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
