@@ -154,10 +154,25 @@ def _ptr(t):
     return t.data_ptr()
 
 
+_RAW_STREAM = []
+
+
+def _current_stream_handle():
+    """torch's current CUDA stream as a cudaStream_t value.  The raw-handle
+    query costs about 0.3 us against 3 us for torch.cuda.current_stream()
+    (which builds a Stream object); the latter stays as the fallback."""
+    import torch
+    if not _RAW_STREAM:
+        _RAW_STREAM.append(getattr(torch._C, "_cuda_getCurrentRawStream", None))
+    raw = _RAW_STREAM[0]
+    if raw is not None:
+        return raw(torch.cuda.current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
 def _stream(stream):
     if stream is None:
-        import torch
-        return torch.cuda.current_stream().cuda_stream
+        return _current_stream_handle()
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream

@@ -673,36 +673,82 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return fn;
 }
 
-// Row-major [outer, inner] matrix, box of 128 bytes x box_rows, 128-byte swizzle.
-bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint64_t outer,
-               uint32_t box_rows) {
+// Encoded descriptors, kept by everything they depend on (address, element
+// type, extents, box rows): a layer calls with the same buffers every step,
+// and the encoder costs about as much host time as a kernel launch.
+// Direct-mapped; a colliding key replaces the entry.
+namespace {
+enum TmType : uint32_t { kTmU8 = 1, kTmBf16 = 2, kTmF32 = 4 };
+struct TmKey {
+    uint64_t base, inner, outer;
+    uint32_t box_rows, type;
+    bool operator==(const TmKey &o) const {
+        return base == o.base && inner == o.inner && outer == o.outer &&
+               box_rows == o.box_rows && type == o.type;
+    }
+};
+struct TmEntry {
+    TmKey key;
+    CUtensorMap map;
+    bool valid;
+};
+constexpr int kTmCacheSize = 256;
+TmEntry g_tm_cache[kTmCacheSize];
+std::mutex g_tm_mutex;
+
+size_t tm_slot(const TmKey &k) {
+    uint64_t h = k.base >> 4;
+    h = h * 0x9E3779B97F4A7C15ull ^ k.inner;
+    h = h * 0x9E3779B97F4A7C15ull ^ k.outer;
+    h = h * 0x9E3779B97F4A7C15ull ^ ((uint64_t)k.box_rows << 8 | k.type);
+    return (size_t)((h * 0x9E3779B97F4A7C15ull) >> 56) % kTmCacheSize;
+}
+
+// Row-major [outer, inner] matrix of elements of `type`, box of 128 bytes x
+// box_rows, 128-byte swizzle.
+bool encode_rows(CUtensorMap *m, const void *base, TmType type, uint64_t inner, uint64_t outer,
+                 uint32_t box_rows) {
+    const TmKey key{reinterpret_cast<uint64_t>(base), inner, outer, box_rows, (uint32_t)type};
+    const size_t slot = tm_slot(key);
+    {
+        std::lock_guard<std::mutex> lock(g_tm_mutex);
+        if (g_tm_cache[slot].valid && g_tm_cache[slot].key == key) {
+            *m = g_tm_cache[slot].map;
+            return true;
+        }
+    }
     auto enc = tensor_map_encoder();
     if (!enc) return false;
-    const uint32_t esize = fp8 ? 1 : 2;
+    const uint32_t esize = (uint32_t)type;
     cuuint64_t dims[2] = {inner, outer};
     cuuint64_t strides[1] = {inner * esize};
     cuuint32_t box[2] = {128 / esize, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                     const_cast<void *>(base), dims, strides, box, estr,
+    const CUtensorMapDataType dt = type == kTmU8     ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : type == kTmBf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+    CUresult r = enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    if (r != CUDA_SUCCESS) return false;
+    std::lock_guard<std::mutex> lock(g_tm_mutex);
+    g_tm_cache[slot].key = key;
+    g_tm_cache[slot].map = *m;
+    g_tm_cache[slot].valid = true;
+    return true;
+}
+}  // namespace
+
+// Row-major [outer, inner] matrix, box of 128 bytes x box_rows, 128-byte swizzle.
+bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint64_t outer,
+               uint32_t box_rows) {
+    return encode_rows(m, base, fp8 ? kTmU8 : kTmBf16, inner, outer, box_rows);
 }
 
 // Row-major fp32 [outer, inner] matrix, box of 32 columns (128 bytes) x
 // box_rows, 128-byte swizzle (for TMA stores of fp32 tiles).
 bool encode_2d_f32(CUtensorMap *m, void *base, uint64_t inner, uint64_t outer, uint32_t box_rows) {
-    auto enc = tensor_map_encoder();
-    if (!enc) return false;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {inner * 4};
-    cuuint32_t box[2] = {32, box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
+    return encode_rows(m, base, kTmF32, inner, outer, box_rows);
 }
 
 namespace {
