@@ -415,26 +415,41 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(const SelectA
         w = a.norm ? __fmul_rn(__fdiv_rn(my_score, total), a.scaling)
                    : __fmul_rn(my_score, a.scaling);
     } else {
+        // The ids above depend on the logits alone; the weights are
+        // exp(l - m) / sum exp(l' - m) with m the largest logit.  Each
+        // exponential is taken in fp32 (expf, within 2 ulp) of the exact
+        // difference: l - m rounded, plus its rounding error from a two-sum,
+        // applied in fp64 as exp(d + e) = exp(d) (1 + e).  Sums, the quotient
+        // and the scaling are fp64, so a weight lies within 5.4e-7 (relative)
+        // of the fp64 definition while its exponential is a normal fp32
+        // number (l - m > -87).  This GPU's fp64 rate is a small fraction of
+        // its fp32 rate.
         float m = -FLT_MAX;
 #pragma unroll
         for (int q = 0; q < PL; ++q)
             if ((valid >> q) & 1u) m = fmaxf(m, l[q]);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        auto ex = [&](float lv) -> double {
+            const float d = __fsub_rn(lv, m);
+            const float bb = __fsub_rn(d, lv);
+            const float e = __fadd_rn(__fsub_rn(lv, __fsub_rn(d, bb)), __fsub_rn(-m, bb));
+            const double x = (double)expf(d);
+            return fma(x, (double)e, x);
+        };
         double denom = 0.0;
         if (a.norm) {
-            for (int j = 0; j < a.k; ++j)
-                denom += exp((double)__shfl_sync(0xffffffffu, my_score, j) - (double)m);
+            for (int j = 0; j < a.k; ++j) denom += ex(__shfl_sync(0xffffffffu, my_score, j));
         } else {
             double part = 0.0;
 #pragma unroll
             for (int q = 0; q < PL; ++q)
-                if ((valid >> q) & 1u) part += exp((double)l[q] - (double)m);
+                if ((valid >> q) & 1u) part += ex(l[q]);
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
             denom = part;
         }
-        w = (float)(exp((double)my_score - (double)m) / denom * (double)a.scaling);
+        w = (float)(ex(my_score) / denom * (double)a.scaling);
     }
 
     if (lane < a.k) {
