@@ -126,7 +126,10 @@ typedef struct moe_weights {
  * butterfly), so the ids are reproducible bit for bit.  Sigmoid scoring:
  * s = fp32(sigmoid(l)) evaluated in fp64, selection by s + bias, groups
  * scored by the sum of their top group_topn, weights s/sum(s) (x scaling).
- * Softmax scoring: selection by l, weights from an fp64 softmax over E. */
+ * Softmax scoring: selection by l; weights exp(l - max l) / sum over E (or
+ * over the chosen k with norm_topk), each exponential in fp32 of the exact
+ * difference, sums and quotient in fp64: within 5.4e-7 (relative) of the
+ * fp64 softmax while l - max l > -87. */
 MOE_API int moe_route(const moe_config *cfg, int32_t T, const void *x, const void *w_gate,
               const float *e_bias, const float *logit_offset, const int32_t *log2phys,
               float *logits, int32_t *topk_ids, float *topk_w,
