@@ -457,6 +457,17 @@ MOE_API int moe_stream_read(const void *src, size_t bytes, int32_t *dev_status, 
 MOE_API int moe_selftest_bounded_wait(int32_t *dev_status, int64_t limit_ns, int32_t *dev_result,
                                       void *stream);
 
+/* Self-test of the routing's sigmoid score (csrc/numerics.cuh sigmoid_score):
+ * for i < n, fast[i] is the score as the selection kernel computes it (fp32
+ * double-float arithmetic, the fp64 expression where that cannot decide the
+ * rounding) and ref[i] = fp32(1 / (1 + exp(-logits[i]))) evaluated in fp64;
+ * the two must be equal bit for bit.  *fallbacks (device int32, zeroed by the
+ * caller) is incremented once per value that took the fp64 evaluation.  All
+ * pointers are device pointers of n elements owned by the caller; the call is
+ * asynchronous on `stream`.  MOE_ERR_INVALID_ARG: n < 0 or a null pointer. */
+MOE_API int moe_selftest_sigmoid(const float *logits, int32_t n, float *fast, float *ref,
+                                 int32_t *fallbacks, void *stream);
+
 /* Self-test of moe_expert_ffn's inter-CTA wait (no counterpart on the pages:
  * a robustness check of this library).  Runs the one-kernel FFN on a tiny
  * problem (hidden 128, inter 256, one group, one row) whose scheduler

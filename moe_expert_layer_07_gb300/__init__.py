@@ -96,6 +96,7 @@ _SIGS = {
                                     ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)],
     "moe_relayout_experts": [_P, _P, _P, _I, ctypes.c_int64, _P, _P],
     "moe_selftest_ffn_flag_timeout": [_P, ctypes.c_size_t, _P, _P],
+    "moe_selftest_sigmoid": [_P, _I, _P, _P, _P, _P],
     "moe_expert_ffn": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,
                        ctypes.c_size_t, _I, _I, _P, _P],
     "moe_experts_forward": [_CP, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P,

@@ -22,6 +22,7 @@
 //                      index; weights; ids mapped through log2phys.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cfloat>
 #include <climits>
 #include <mutex>
@@ -236,9 +237,10 @@ __device__ __forceinline__ void warp_argmax(float &v, int &i) {
     }
 }
 
-// One CTA per token. The fp64 sigmoid runs on the SMs' narrow FP64 pipes, so
-// all four warps of the CTA (one per SM sub-partition) evaluate the scores
-// into shared memory; warp 0 then does the selection alone, holding expert
+// One CTA per token. All four warps of the CTA (one per SM sub-partition)
+// evaluate the scores into shared memory (the sigmoid in fp32 double-float
+// arithmetic, fp64 only where that cannot decide the rounding:
+// sigmoid_score); warp 0 then does the selection alone, holding expert
 // e = q*32 + lane in its registers.
 constexpr int kSelThreads = 128;
 
@@ -267,7 +269,7 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(const SelectA
         const float lv = ok ? lrow[e] : 0.0f;
         float sv = lv, selv = lv;
         if (a.sigmoid) {
-            sv = (float)(1.0 / (1.0 + exp(-(double)lv)));
+            sv = sigmoid_score(lv);
             selv = (ok && a.bias) ? __fadd_rn(sv, a.bias[e]) : sv;
         }
         sh_l[e] = lv;
@@ -547,3 +549,29 @@ int launch_route(const moe_config *cfg, int T, const void *x, const void *w_gate
 }
 
 }  // namespace moe
+
+// ---- self-test of the sigmoid score --------------------------------------
+namespace moe {
+namespace {
+__global__ void sigmoid_selftest_kernel(const float *l, int n, float *fast, float *ref,
+                                        int32_t *fallbacks) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+        bool fb = false;
+        fast[i] = sigmoid_score(l[i], &fb);
+        ref[i] = sigmoid_score_fp64(l[i]);
+        if (fb) atomicAdd(fallbacks, 1);
+    }
+}
+}  // namespace
+}  // namespace moe
+
+extern "C" MOE_API int moe_selftest_sigmoid(const float *logits, int32_t n, float *fast,
+                                            float *ref, int32_t *fallbacks, void *stream) {
+    if (n < 0 || (n > 0 && (!logits || !fast || !ref || !fallbacks))) return MOE_ERR_INVALID_ARG;
+    if (n == 0) return MOE_OK;
+    const int grid = (int)std::min<int64_t>(moe::ceil_div(n, 256), 4096);
+    moe::sigmoid_selftest_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        logits, n, fast, ref, fallbacks);
+    MOE_LAUNCH_CHECK();
+    return MOE_OK;
+}

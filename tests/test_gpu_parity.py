@@ -105,6 +105,36 @@ def test_route_with_random_permutation(lib):
     assert np.array_equal(ids, phys) and np.array_equal(ids, wl.log2phys[logical])
 
 
+def test_sigmoid_score_equals_fp64_bit_for_bit(lib):
+    """The selection kernel's sigmoid score (double-float fp32 arithmetic,
+    with the fp64 expression wherever that cannot decide the rounding) is
+    the fp64 sigmoid rounded to fp32 on every input: 8M normal logits at four
+    spreads, a dense sweep of [-90, 90] (it crosses many rounding midpoints)
+    and the edges of the fast range.  The oracle's numpy evaluation agrees as
+    well."""
+    g = torch.Generator(device="cuda").manual_seed(5)
+    parts = [torch.randn(2_000_000, device="cuda", generator=g) * sd for sd in (0.5, 2.0, 8.0, 30.0)]
+    parts.append(torch.linspace(-90.0, 90.0, 1_000_001, device="cuda"))
+    parts.append(torch.tensor([0.0, -0.0, 1e-30, -1e-30, 1e-7, -1e-7, 80.0, -80.0, 80.00001,
+                               -80.00001, 87.3, -87.3, 88.8, -88.8, 100.0, -100.0, 1e4, -1e4,
+                               float("inf"), float("-inf")], device="cuda"))
+    lg = torch.cat(parts).contiguous()
+    n = lg.numel()
+    fast, ref = torch.empty_like(lg), torch.empty_like(lg)
+    fb = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = moe.lib().moe_selftest_sigmoid(lg.data_ptr(), n, fast.data_ptr(), ref.data_ptr(),
+                                        fb.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert torch.equal(fast.view(torch.int32), ref.view(torch.int32))
+    # inputs beyond |l| = 80 always take the fp64 expression; the others rarely
+    out_of_range = int((~(lg.abs() <= 80.0)).sum().item())
+    assert int(fb.item()) - out_of_range < (n - out_of_range) // 1000
+    with np.errstate(over="ignore"):   # exp(1e4) is inf, as it should be
+        want = orouting.sigmoid_scores(lg.cpu().numpy())
+    assert np.array_equal(to_np(fast).view(np.uint32), want.view(np.uint32))
+
+
 @pytest.mark.parametrize("name", ["r1_mini", "bf16_mini", "tiny_bf16"])
 def test_route_ties_go_to_the_lower_index(lib, name):
     """Every odd expert's gate row (and bias) copies the even expert below it,
