@@ -7,7 +7,7 @@
 namespace moe {
 
 // Tensor map of a row-major [outer, inner] matrix (e4m3 bytes or bf16) with
-// a box of 128 bytes x box_rows and 128-byte swizzle; false when the driver's
+// a box of 128 bytes x box_rows and 128-byte swizzle; false when the CUDA driver's
 // encoder is unavailable or rejects the layout (base not 16-byte aligned,
 // row pitch not a multiple of 16 bytes).
 bool encode_2d(CUtensorMap *m, const void *base, bool fp8, uint64_t inner, uint64_t outer,
