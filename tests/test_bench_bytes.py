@@ -55,3 +55,21 @@ def test_wide_path_intermediates_not_counted():
     diff = sum(per.values()) - bench.method_bytes(s, active)
     assert y_extra < diff < y_extra + gate_up_rows / 2
     assert "silu_mul" not in per and "gemm_gate_up_swiglu" in per
+
+
+def test_weights_that_fit_in_l2_are_rotated():
+    """Layers whose expert weights fit in L2 are timed over enough copies that
+    two uses of one copy are at least 2.5 L2 capacities apart; the R1 and
+    V2-Lite layers (far beyond L2) use one copy and say so in their config."""
+    for name in ("r1_decode_t128", "r1_zipf_t1024", "r1_prefill_t4096", "v2lite_bf16"):
+        s = synth.CONFIGS[name]
+        assert bench.l2_rotation(s) == 1
+        assert bench.l2_note(s).startswith("inputs larger than L2 (expert weights streamed")
+    s = synth.CONFIGS["tiny_bf16"]
+    r = bench.l2_rotation(s)
+    w13, w2 = bench.expert_weight_bytes(s)
+    per_layer = s.groups * (w13 + w2)
+    assert per_layer < bench.L2_BYTES                    # 53.5 MB: the case this is for
+    assert (r - 1) * per_layer >= 2.5 * bench.L2_BYTES   # others' weights in between
+    assert (r - 2) * per_layer < 2.5 * bench.L2_BYTES    # and no more copies than that
+    assert f"{r} copies" in bench.l2_note(s)
