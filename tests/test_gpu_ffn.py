@@ -178,6 +178,9 @@ def _bf16_problem(H, I, counts, seed):
                                         (2048, 1408, [24, 0, 256, 5, 33]),   # V2-Lite sizes
                                         (512, 384, [7])])
 def test_expert_ffn_bf16_equals_two_kernel_path(lib, H, I, counts):
+    """Both BF16 configurations of the kernel: the first and last cases have
+    few enough gate/up units for one CTA per SM with the five-stage ring,
+    the V2-Lite-sized one takes two CTAs per SM with two stages."""
     cfg = moe.make_config(synth.MoEShape("ffn16", 1, H, I, 32, 1, 8, scoring="softmax",
                                          dtype="bf16"))
     G, rows, a, off, w13, w2 = _bf16_problem(H, I, counts, 12)
