@@ -72,10 +72,12 @@ enum { MOE_OUT_F32 = 0, MOE_OUT_BF16 = 1 };
 enum { MOE_ACT_IDENTITY = 0, MOE_ACT_SILU_MUL = 1 };
 /* Layout of an expert weight tensor W [groups, N, K] (w13, w2):
  *   MOE_LAYOUT_ROWS   row-major, K innermost;
- *   MOE_LAYOUT_TILES  128 x 128-byte tiles, each contiguous: element (g, n, k)
- *                     at ((((g * N/128 + n/128) * K/kt + k/kt) * 128 + n%128) * kt
- *                     + k%kt) with kt = 128 (e4m3) or 64 (bf16) elements, i.e.
- *                     one tensor-memory copy box per 16 KB of consecutive HBM.
+ *   MOE_LAYOUT_TILES  128 x 128-byte tiles, each contiguous, tile-major: tile
+ *                     (g, n/128, k/kt) holds rows n%128 of 128 bytes (kt = 128
+ *                     e4m3 or 64 bf16 elements), and within row r the 16-byte
+ *                     chunk c is stored at chunk position c ^ (r mod 8) (the
+ *                     128-byte swizzle the tensor cores read), so a kernel
+ *                     places a tile in shared memory with one 16 KB bulk copy.
  * moe_pack_expert_weights converts the first into the second.  Results do
  * not depend on the layout. */
 enum { MOE_LAYOUT_ROWS = 0, MOE_LAYOUT_TILES = 1 };

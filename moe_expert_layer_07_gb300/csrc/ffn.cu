@@ -109,7 +109,8 @@ struct FfnArgs {
     float *h_scales;           // [rows, inter/128]
     float *y;                  // [rows, hidden]
     int32_t *sched;            // [0] next unit; [1 + j] finished gate/up tiles of activation tile j
-    int w_tiled;               // W13, W2 in MOE_LAYOUT_TILES
+    int w_tiled;               // W13, W2 in MOE_LAYOUT_TILES (tiles read by 16 KB bulk copies)
+    const uint8_t *w13, *w2;   // weight bytes
     int min_rows, max_rows;    // groups whose row count lies outside are skipped
     int32_t *status;
 };
@@ -340,9 +341,11 @@ __global__ void __launch_bounds__(64 + 128 * EW, CPS)
                         u.down ? (two ? 2u : 1u) * (kABytes + abytes) : 2 * kABytes + abytes;
                     mbar_arrive_expect_tx(fb, bytes);
                     if (!u.down) {
-                        if (tiled) {
-                            tma_load_2d(sa, &tmW13, 0, (tb_gate + ks) * kBM, fb, pol_w);
-                            tma_load_2d(sa + kABytes, &tmW13, 0, (tb_up + ks) * kBM, fb, pol_w);
+                        if (tiled) {   // pre-swizzled 16 KB tiles: plain bulk copies
+                            bulk_load(sa, args.w13 + (size_t)(tb_gate + ks) * kABytes, kABytes, fb,
+                                      pol_w);
+                            bulk_load(sa + kABytes, args.w13 + (size_t)(tb_up + ks) * kABytes,
+                                      kABytes, fb, pol_w);
                         } else {
                             tma_load_2d(sa, &tmW13, ks * kKE, wrow, fb, pol_w);            // gate
                             tma_load_2d(sa + kABytes, &tmW13, ks * kKE, wrow + I, fb, pol_w);   // up
@@ -354,8 +357,9 @@ __global__ void __launch_bounds__(64 + 128 * EW, CPS)
                             if (hk == 1 && !two) break;
                             const int k0 = (2 * ks + hk) * kKE;
                             if (tiled)
-                                tma_load_2d(sa + hk * kABytes, &tmW2, 0,
-                                            (tb_down + 2 * ks + hk) * kBM, fb, pol_w);
+                                bulk_load(sa + hk * kABytes,
+                                          args.w2 + (size_t)(tb_down + 2 * ks + hk) * kABytes,
+                                          kABytes, fb, pol_w);
                             else
                                 tma_load_2d(sa + hk * kABytes, &tmW2, k0, wrow, fb, pol_w);
                             tma_load_2d(sb + hk * kBBytes, tmHb, k0, u.row0, fb, pol_a);
@@ -807,6 +811,8 @@ int launch_ffn_impl(int groups, int hidden, int inter, int rows, const void *xp,
     a.y = y;
     a.sched = sched;
     a.w_tiled = w_tiled;
+    a.w13 = static_cast<const uint8_t *>(w13);
+    a.w2 = static_cast<const uint8_t *>(w2);
     a.min_rows = min_rows;
     a.max_rows = max_rows;
     a.status = status;

@@ -110,7 +110,8 @@ struct GemmArgs {
     void *c;          // C [rows, n_out]; SwiGLU: h [rows, n_out/2] (e4m3 or bf16)
     float *h_scales;  // SwiGLU + FP8: [rows, n_out/256]
     int c_bf16;
-    int w_tiled;      // W in MOE_LAYOUT_TILES
+    int w_tiled;      // W in MOE_LAYOUT_TILES (tiles read by 16 KB bulk copies)
+    const uint8_t *w; // W bytes
     int min_rows, max_rows;   // groups whose row count lies outside are skipped
     int32_t *status;
 };
@@ -289,9 +290,12 @@ __global__ void __launch_bounds__(64 + 128 * EW, kCtasPerSm)
                     const uint32_t sb = sa + S::kNA * S::kABytes;
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
-                    if (args.w_tiled) {
-                        tma_load_2d(sa, &tmW, 0, (tb + kb) * kBM, fb, pol_w);
-                        if (SW) tma_load_2d(sa + S::kABytes, &tmW, 0, (tb_up + kb) * kBM, fb, pol_w);
+                    if (args.w_tiled) {   // pre-swizzled 16 KB tiles: plain bulk copies
+                        bulk_load(sa, args.w + (size_t)(tb + kb) * S::kABytes, S::kABytes, fb,
+                                  pol_w);
+                        if (SW)
+                            bulk_load(sa + S::kABytes, args.w + (size_t)(tb_up + kb) * S::kABytes,
+                                      S::kABytes, fb, pol_w);
                     } else {
                         tma_load_2d(sa, &tmW, kb * S::kKPerStage, wrow, fb, pol_w);
                         if (SW)
@@ -805,6 +809,7 @@ int launch_grouped_gemm(bool fp8, int groups, int n_out, int k_dim, int rows, co
     args.h_scales = nullptr;
     args.c_bf16 = c_dtype == MOE_OUT_BF16;
     args.w_tiled = w_tiled;
+    args.w = static_cast<const uint8_t *>(w);
     args.min_rows = min_rows;
     args.max_rows = max_rows;
     args.status = status;
@@ -839,6 +844,7 @@ int launch_grouped_gemm_swiglu(bool fp8, int groups, int inter, int k_dim, int r
     args.h_scales = h_scales;
     args.c_bf16 = !fp8;
     args.w_tiled = w_tiled;
+    args.w = static_cast<const uint8_t *>(w13);
     args.min_rows = min_rows;
     args.max_rows = max_rows;
     args.status = status;

@@ -98,7 +98,8 @@ struct WideArgs {
     uint8_t *h;              // SwiGLU: [rows, n_out / 2] e4m3
     float *h_scales;         // SwiGLU: [rows, n_out / 256]
     float *c;                // plain: [rows, n_out] fp32
-    int w_tiled;             // W in MOE_LAYOUT_TILES
+    int w_tiled;             // W in MOE_LAYOUT_TILES (tiles read by 16 KB bulk copies)
+    const uint8_t *w;        // W bytes
     int min_rows, max_rows;  // groups whose row count lies outside are skipped
     // Row gather (SwiGLU): with src_of_row set, row r of a tile is token
     // t(r)'s row of the [T, k_dim] activations that tmA then maps (one row per
@@ -298,9 +299,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t fb = smem_u32(&full_bar[stage]);
                 if (lane == 0) {
                     mbar_arrive_expect_tx(fb, bytes);
-                    if (args.w_tiled) {   // tile (block b, K block kb) = rows (b KB + kb) 128
-                        tma_load_2d(sb, &tmW, 0, (b0 * KB + kb) * 128, fb, pol_w);
-                        tma_load_2d(sb + 128 * 128, &tmW, 0, (b1 * KB + kb) * 128, fb, pol_w);
+                    if (args.w_tiled) {   // tile (block b, K block kb): 16 KB at (b KB + kb) 16 KB
+                        bulk_load(sb, args.w + (size_t)(b0 * KB + kb) * 16384, 16384, fb, pol_w);
+                        bulk_load(sb + 128 * 128, args.w + (size_t)(b1 * KB + kb) * 16384, 16384, fb,
+                                  pol_w);
                     } else {
                         tma_load_2d(sb, &tmW, kb * 128, b0 * 128, fb, pol_w);
                         tma_load_2d(sb + 128 * 128, &tmW, kb * 128, b1 * 128, fb, pol_w);
@@ -358,9 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sb = sa + kABytes;
                     const uint32_t fb = smem_u32(&full_bar[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
-                    if (args.w_tiled) {   // tile (block b, K block kb) = rows (b KB + kb) 128
-                        tma_load_2d(sb, &tmW, 0, (b0 * KB + kb) * 128, fb, pol_w);
-                        tma_load_2d(sb + 128 * 128, &tmW, 0, (b1 * KB + kb) * 128, fb, pol_w);
+                    if (args.w_tiled) {   // tile (block b, K block kb): 16 KB at (b KB + kb) 16 KB
+                        bulk_load(sb, args.w + (size_t)(b0 * KB + kb) * 16384, 16384, fb, pol_w);
+                        bulk_load(sb + 128 * 128, args.w + (size_t)(b1 * KB + kb) * 16384, 16384, fb,
+                                  pol_w);
                     } else {
                         tma_load_2d(sb, &tmW, kb * 128, b0 * 128, fb, pol_w);
                         tma_load_2d(sb + 128 * 128, &tmW, kb * 128, b1 * 128, fb, pol_w);
@@ -592,7 +595,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <bool SW, bool GATHER, int ST>
-int launch_wide(const WideArgs &args, const void *a, const void *w, cudaStream_t s) {
+int launch_wide(const WideArgs &args_in, const void *a, const void *w, cudaStream_t s) {
+    WideArgs args = args_in;
+    args.w = static_cast<const uint8_t *>(w);
     using Sh = WideShape<SW, ST>;
     auto kern = wide_gemm_kernel<SW, GATHER, ST>;
     static std::once_flag attr_once[64];
@@ -636,6 +641,7 @@ int launch_wide(const WideArgs &args, const void *a, const void *w, cudaStream_t
 WideArgs wide_args(int groups, int n_out, int k_dim, int rows, const float *a_scales,
                    const int32_t *offsets, const float *w_scales, bool w_tiled, int32_t *status) {
     WideArgs args;
+    args.w = nullptr;
     args.groups = groups;
     args.n_out = n_out;
     args.k_dim = k_dim;

@@ -2,12 +2,17 @@
 // kernels load a weight tile as one 128-row x 128-byte box per K block; in the
 // row-major layout that box gathers 128 runs of 128 bytes, one per row, K
 // bytes apart.  Packed, every box is 16 KB of consecutive memory, which HBM
-// streams more efficiently (the weights are read once per layer call).
+// streams more efficiently (the weights are read once per layer call).  Within
+// a tile the 16-byte chunks of row r are stored in the order the tensor cores
+// read them from shared memory (128-byte swizzle: chunk c at position
+// c ^ (r mod 8)), so a plain 16 KB bulk copy places a tile as the swizzling
+// tensor copy would; such copies stream faster than 2-D tensor boxes.
 //
-//   dst[((b * KBt + kb) * 128 + r) * 128 + c] = src[(b * 128 + r) * Kbytes + kb * 128 + c]
+//   dst[((b * KBt + kb) * 128 + r) * 128 + 16 (c ^ (r mod 8)) + j]
+//       = src[(b * 128 + r) * Kbytes + kb * 128 + 16 c + j]
 //
 // for row block b over all groups (N % 128 == 0, so blocks never straddle
-// groups), K block kb of 128 bytes, row r and byte c within the tile.
+// groups), K block kb of 128 bytes, row r, 16-byte chunk c and byte j.
 #include <algorithm>
 
 #include "internal.h"
@@ -26,7 +31,8 @@ __global__ void __launch_bounds__(256)
         const int r = within >> 3, c = within & 7;
         const int64_t b = tile / kbt;
         const int kb = (int)(tile - b * kbt);
-        dst[v] = __ldg(src + (b * 128 + r) * ((int64_t)kbt * 8) + kb * 8 + c);
+        // destination chunk c of row r holds source chunk c ^ (r mod 8)
+        dst[v] = __ldg(src + (b * 128 + r) * ((int64_t)kbt * 8) + kb * 8 + (c ^ (r & 7)));
     }
 }
 

@@ -31,9 +31,16 @@ def _cfg(dtype, H=1024, I=512):
 
 
 def _tiles_reference(w, fp8):
+    """Tiles of 128 rows x 128 bytes, tile-major, and within a tile the
+    16-byte chunk c of row r at chunk position c ^ (r mod 8)."""
     G, N, K = w.shape
     kt = 128 if fp8 else 64
-    return w.view(G, N // 128, 128, K // kt, kt).permute(0, 1, 3, 2, 4).contiguous().view(G, N, K)
+    t = w.view(G, N // 128, 128, K // kt, kt).permute(0, 1, 3, 2, 4).contiguous()
+    t = t.view(G, N // 128, K // kt, 128, 8, kt // 8)          # [..., row, chunk, element]
+    r = torch.arange(128, device=w.device)[:, None]
+    c = torch.arange(8, device=w.device)[None, :]
+    t = t[:, :, :, r, c ^ (r % 8), :]                          # position c holds chunk c ^ (r mod 8)
+    return t.contiguous().view(G, N, K)
 
 
 @pytest.mark.parametrize("fp8,G,N,K", [(True, 3, 256, 384), (True, 1, 128, 128),
